@@ -1,0 +1,167 @@
+"""FP8 block-scaled linear-layer path for NVIDIA GB300 (sm_103a).
+
+A thin ctypes binding over the C ABI in ``include/fp8bs.h`` (``libfp8bs.so``, built in place
+by ``fp8_block_scaled_fp8bs_gb300.build``). Every step of the path runs in the library's CUDA
+kernels; this module only marshals arguments. There is no CPU fallback: if the library is
+missing or cannot be loaded, importing the binding's functions raises.
+
+Raw entry points (same names and arguments as the C functions; pointers are ints):
+    fp8bs_act_quant(x, y, s, M, K, scale_fmt, stream)
+    fp8bs_weight_dequant(w, s, y, N, K, stream)
+    fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream)
+    fp8bs_device_error(clear=True, stream=0) -> int
+    fp8bs_probe_wait_timeout(timeout_ns, stream)
+Tensor conveniences (PyTorch CUDA tensors; outputs allocated with torch):
+    act_quant(x, scale_fmt="fp32") -> (y, s)      ("DeepSeek-V3 Administrator & Developer
+    weight_dequant(w, s) -> y                        Guide", §8.5.1, §8.5.2, §8.5.3)
+    fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32") -> c
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+BLOCK = 128
+SCALE_FP32 = 0
+SCALE_UE8M0 = 1
+STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not aligned",
+          3: "unsupported device (needs sm_103)", 4: "CUDA error"}
+DEVERR_PROBE = 0x100
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
+EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_status_string",
+           "fp8bs_device_error", "fp8bs_probe_wait_timeout")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class Fp8bsError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)} (status {status})")
+        self.status = status
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load libfp8bs.so (building it first if it is missing and nvcc is available)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            from . import build as _build
+            _build.build()
+        lib = ctypes.CDLL(p)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.fp8bs_act_quant.argtypes = [vp, vp, vp, i64, i64, i32, vp]
+        lib.fp8bs_weight_dequant.argtypes = [vp, vp, vp, i64, i64, vp]
+        lib.fp8bs_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+        lib.fp8bs_status_string.argtypes = [i32]
+        lib.fp8bs_status_string.restype = ctypes.c_char_p
+        lib.fp8bs_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, vp]
+        lib.fp8bs_probe_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        for name in EXPORTS:
+            getattr(lib, name).restype = getattr(lib, name).restype or i32
+        lib.fp8bs_status_string.restype = ctypes.c_char_p
+        _lib = lib
+        return lib
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise Fp8bsError(fn, status)
+
+
+# ----------------------------------------------------------------------- raw entry points
+
+def fp8bs_act_quant(x, y, s, M, K, scale_fmt=SCALE_FP32, stream=0) -> None:
+    _check("fp8bs_act_quant", load().fp8bs_act_quant(x, y, s, M, K, scale_fmt, stream))
+
+
+def fp8bs_weight_dequant(w, s, y, N, K, stream=0) -> None:
+    _check("fp8bs_weight_dequant", load().fp8bs_weight_dequant(w, s, y, N, K, stream))
+
+
+def fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, stream=0) -> None:
+    _check("fp8bs_gemm", load().fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream))
+
+
+def fp8bs_device_error(clear: bool = True, stream=0) -> int:
+    out = ctypes.c_uint(0)
+    _check("fp8bs_device_error", load().fp8bs_device_error(ctypes.byref(out), int(clear), stream))
+    return out.value
+
+
+def fp8bs_probe_wait_timeout(timeout_ns: int, stream=0) -> None:
+    _check("fp8bs_probe_wait_timeout", load().fp8bs_probe_wait_timeout(timeout_ns, stream))
+
+
+# ----------------------------------------------------------------------- tensor helpers
+
+def _fmt(scale_fmt) -> int:
+    if scale_fmt in (SCALE_FP32, "fp32", None):
+        return SCALE_FP32
+    if scale_fmt in (SCALE_UE8M0, "ue8m0"):
+        return SCALE_UE8M0
+    raise ValueError(f"unknown scale_fmt {scale_fmt!r}")
+
+
+def _stream():
+    import torch
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _require(t, dtype, ndim, name):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def act_quant(x, scale_fmt="fp32"):
+    """x: bf16 [M,K] (K % 128 == 0) -> (y float8_e4m3fn [M,K], s float32 [M,K/128])."""
+    import torch
+    _require(x, torch.bfloat16, 2, "x")
+    M, K = x.shape
+    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
+    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=x.device)
+    fp8bs_act_quant(x.data_ptr(), y.data_ptr(), s.data_ptr(), M, K, _fmt(scale_fmt), _stream())
+    return y, s
+
+
+def weight_dequant(w, s):
+    """w: float8_e4m3fn [N,K], s: float32 [ceil(N/128), ceil(K/128)] -> bf16 [N,K]."""
+    import torch
+    _require(w, torch.float8_e4m3fn, 2, "w")
+    _require(s, torch.float32, 2, "s")
+    N, K = w.shape
+    if tuple(s.shape) != (-(-N // BLOCK), -(-K // BLOCK)):
+        raise ValueError(f"scale shape {tuple(s.shape)} does not match weight {tuple(w.shape)}")
+    y = torch.empty((N, K), dtype=torch.bfloat16, device=w.device)
+    fp8bs_weight_dequant(w.data_ptr(), s.data_ptr(), y.data_ptr(), N, K, _stream())
+    return y
+
+
+def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None):
+    """C[M,N] bf16 = A[M,K] . B[N,K]^T with per-128-K-block scales a_s [M,K/128] and
+    b_s [ceil(N/128), K/128]."""
+    import torch
+    _require(a, torch.float8_e4m3fn, 2, "a")
+    _require(b, torch.float8_e4m3fn, 2, "b")
+    _require(a_s, torch.float32, 2, "a_s")
+    _require(b_s, torch.float32, 2, "b_s")
+    M, K = a.shape
+    N = b.shape[0]
+    if b.shape[1] != K or tuple(a_s.shape) != (M, K // BLOCK) or \
+            tuple(b_s.shape) != (-(-N // BLOCK), K // BLOCK):
+        raise ValueError("operand or scale shapes do not match")
+    c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    fp8bs_gemm(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
+               M, N, K, _fmt(scale_fmt), _stream())
+    return c

@@ -1,0 +1,177 @@
+// api.cu -- the C ABI (include/fp8bs.h): argument checks, device checks, TMA tensor-map
+// encoding and the choice of GEMM kernel. Nothing here allocates memory or synchronises.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "../../include/fp8bs.h"
+#include "kernels.h"
+
+namespace {
+
+using fp8bs::GemmArgs;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// The kernels are built for sm_103a only; arch-specific code runs on compute capability 10.3.
+int check_device(int* num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return FP8BS_ERR_CUDA;
+    }
+    if (major != 10 || minor != 3) return FP8BS_ERR_UNSUPPORTED_DEVICE;
+    return FP8BS_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// The driver's tensor-map encoder, looked up through the runtime so that the library does not
+// link libcuda directly (it then loads on machines without a driver).
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            p = nullptr;
+        }
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// 2-D map over a row-major e4m3 matrix [rows, K] with boxes of {128 bytes, box_rows} and
+// 128-byte swizzling (the tcgen05 K-major SW128 layout). Rows past the end read as zero.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K)};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+const char* fp8bs_status_string(int status) {
+    switch (status) {
+        case FP8BS_OK: return "ok";
+        case FP8BS_ERR_INVALID_ARG: return "invalid argument";
+        case FP8BS_ERR_MISALIGNED: return "pointer not aligned";
+        case FP8BS_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs sm_103)";
+        case FP8BS_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+int fp8bs_act_quant(const void* x, void* y, float* s, int64_t M, int64_t K, int scale_fmt,
+                    void* stream) {
+    if (M < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
+    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || K == 0) return FP8BS_OK;
+    if (!x || !y || !s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned4(s)) return FP8BS_ERR_MISALIGNED;
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    return status_of(fp8bs::launch_act_quant(x, y, s, M, K, scale_fmt == FP8BS_SCALE_UE8M0, sms,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_weight_dequant(const void* w, const float* s, void* y, int64_t N, int64_t K,
+                         void* stream) {
+    if (N < 0 || K < 0) return FP8BS_ERR_INVALID_ARG;
+    if (N == 0 || K == 0) return FP8BS_OK;
+    if (!w || !s || !y) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned4(s) || (reinterpret_cast<uintptr_t>(y) & 1u)) return FP8BS_ERR_MISALIGNED;
+    if (K % 16 == 0 && (!aligned16(w) || !aligned16(y))) return FP8BS_ERR_MISALIGNED;
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    return status_of(
+        fp8bs::launch_weight_dequant(w, s, y, N, K, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
+               int64_t M, int64_t N, int64_t K, int scale_fmt, void* stream) {
+    if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
+    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
+        return FP8BS_ERR_INVALID_ARG;
+    // The kernels index with 32-bit row/column coordinates (TMA coordinates are 32-bit).
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (!c) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(c)) return FP8BS_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        int sms = 0;
+        if (int e = check_device(&sms)) return e;
+        return status_of(cudaMemsetAsync(c, 0, static_cast<size_t>(M * N) * 2, st));
+    }
+    if (!a || !a_s || !b || !b_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned4(a_s) || !aligned4(b_s))
+        return FP8BS_ERR_MISALIGNED;
+    int sms = 0;
+    if (int e = check_device(&sms)) return e;
+
+    GemmArgs g;
+    g.a_s = a_s;
+    g.b_s = b_s;
+    g.c = c;
+    g.M = static_cast<int>(M);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+
+    CUtensorMap tmA, tmB;
+    if (M <= 128) {
+        // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA.
+        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, MT)) return FP8BS_ERR_CUDA;
+        cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, st);
+        if (e != cudaErrorInvalidValue) return status_of(e);
+        // K too long to stage the activation scales: fall through to the normal kernel.
+    }
+    const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
+    const int BN = tiles256 >= sms ? 256 : 128;
+    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, BN, sms, st));
+}
+
+int fp8bs_device_error(unsigned int* out, int clear, void* stream) {
+    if (!out) return FP8BS_ERR_INVALID_ARG;
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    return status_of(fp8bs::read_device_error(out, clear != 0, static_cast<cudaStream_t>(stream)));
+}
+
+int fp8bs_probe_wait_timeout(uint64_t timeout_ns, void* stream) {
+    if (timeout_ns < 1000000ull) timeout_ns = 1000000ull;
+    if (timeout_ns > 2000000000ull) timeout_ns = 2000000000ull;
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    return status_of(fp8bs::launch_probe_wait(timeout_ns, static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,564 @@
+// gemm.cu -- block-scaled FP8 GEMM on the sm_103a tensor cores (tcgen05 + TMEM + TMA).
+//
+// Computes C[M,N] (bf16) = sum_kb a_s[m,kb] * b_s[n/128,kb] * P_kb[m,n], where P_kb is the
+// fp32 product of the 128-wide K block kb of A (e4m3 [M,K]) and B (e4m3 [N,K]) --
+// "DeepSeek-V3 Administrator & Developer Guide", §8.5.3 fp8_gemm_kernel.
+//
+// Structure (one CTA per SM, warp-specialised):
+//   warp 0      TMA producer: streams 128-byte-wide K slices of A and B into a ring of
+//               shared-memory stages (128-byte swizzle), completion counted on mbarriers.
+//   warp 1      MMA issuer: for each K block, 4 x tcgen05.mma (K = 32 each) into one of two
+//               TMEM buffers, then tcgen05.commit to free the stage and publish the buffer.
+//   warps 2..   promotion/epilogue: tcgen05.ld the block's fp32 partial from TMEM, release
+//               the buffer, and fold it into fp32 registers with the block's scale
+//               a_s[m,kb] * b_s[n/128,kb]. After the last block: round to bf16 and store.
+// The two TMEM buffers let the tensor cores compute block kb+1 while block kb is promoted.
+//
+// Two orientations share this scheme:
+//   gemm_tn_kernel      128 rows of A x BN columns of B per tile, persistent over tiles.
+//   gemm_swapab_kernel  for few rows of A (decode): 128 rows of B take the MMA's M side and
+//                       the MT rows of A its N side, so the weight stream fills the tensor
+//                       core's 128 lanes and every SM streams its own 128-row weight slab.
+//
+// Every wait is bounded (ptx.cuh); a wait that runs out records a bit in the device error
+// word, the CTA stops issuing, drains its in-flight TMA copies and MMAs, frees TMEM and exits.
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "../../include/fp8bs.h"
+
+namespace fp8bs {
+
+__device__ unsigned int g_device_error = 0;
+
+namespace {
+
+constexpr int BM = 128;       // tile rows on the MMA's M side = TMEM lanes
+constexpr int BK = 128;       // K block: one scale block, one 128-byte swizzle row of e4m3
+constexpr int MMA_K = 32;     // K per tcgen05.mma for 8-bit operands
+constexpr int A_TILE = BM * BK;  // bytes of one 128 x 128 e4m3 tile
+
+__device__ __forceinline__ void record_error(unsigned bit) { atomicOr(&g_device_error, bit); }
+
+__host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t used) {
+    uint32_t c = 32;
+    while (c < used) c <<= 1;
+    return c;
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Warp-uniform bounded wait: every lane waits, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Shared-memory bookkeeping common to both kernels.
+struct Ring {
+    uint64_t* full;    // [stages] TMA bytes landed
+    uint64_t* empty;   // [stages] MMAs reading the stage are done
+    uint64_t* tfull;   // [2] TMEM buffer holds a finished partial
+    uint64_t* tempty;  // [2] TMEM buffer has been read out
+    uint64_t* drain;   // [1] all MMAs issued by the CTA are done
+    uint32_t* tmem_holder;
+};
+
+__device__ __forceinline__ Ring carve_ring(uint8_t* p, int stages) {
+    Ring r;
+    r.full = reinterpret_cast<uint64_t*>(p);
+    r.empty = r.full + stages;
+    r.tfull = r.empty + stages;
+    r.tempty = r.tfull + 2;
+    r.drain = r.tempty + 2;
+    r.tmem_holder = reinterpret_cast<uint32_t*>(r.drain + 1);
+    return r;
+}
+
+constexpr int ring_bytes(int stages) { return (2 * stages + 5) * 8 + 16; }
+
+__device__ __forceinline__ void init_ring(const Ring& r, int stages, uint32_t epi_warps) {
+    for (int s = 0; s < stages; ++s) {
+        mbar_init(&r.full[s], 1);
+        mbar_init(&r.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+        mbar_init(&r.tfull[b], 1);
+        mbar_init(&r.tempty[b], epi_warps);
+    }
+    mbar_init(r.drain, 1);
+    fence_barrier_init();
+}
+
+// After an abort, wait (briefly) for the TMA copies this producer issued but that no consumer
+// saw land, so that no copy is still writing shared memory when the CTA exits.
+__device__ __forceinline__ void drain_tma(const Ring& r, int stages, int64_t issued) {
+    const int64_t first = issued > stages ? issued - stages : 0;
+    for (int64_t i = first; i < issued; ++i) {
+        const int s = static_cast<int>(i % stages);
+        const uint32_t ph = static_cast<uint32_t>((i / stages) & 1);
+        if (!mbar_wait(&r.full[s], ph, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
+    }
+}
+
+// ================================================================ normal orientation
+
+// Tile = 128 rows of A x BN columns of B; EPI_WARPS promotion warps (4 per 128 columns).
+template <int BN>
+struct TnCfg {
+    static constexpr int EPI_WARPS = BN / 32;                 // 4 warps per 128 columns
+    static constexpr int CW = 128;                            // columns per promotion thread
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int B_TILE = BN * BK;
+    static constexpr int STAGE = A_TILE + B_TILE;
+    static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
+};
+
+template <int BN>
+__global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
+    gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmArgs g, const int stages) {
+    using Cfg = TnCfg<BN>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + stages * A_TILE;
+    const Ring ring = carve_ring(sB + stages * Cfg::B_TILE, stages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int num_kb = g.K / BK;
+    const int m_tiles = (g.M + BM - 1) / BM;
+    const int n_tiles = (g.N + BN - 1) / BN;
+    const int num_tiles = m_tiles * n_tiles;
+
+    if (threadIdx.x == 0) {
+        init_ring(ring, stages, Cfg::EPI_WARPS);
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *ring.tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile % m_tiles) * BM;
+                const int n0 = (tile / m_tiles) * BN;
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
+                        record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_expect_tx(&ring.full[stage], Cfg::STAGE);
+                    tma_load_2d(sA + stage * A_TILE, &tmA, &ring.full[stage], kb * BK, m0);
+                    tma_load_2d(sB + stage * Cfg::B_TILE, &tmB, &ring.full[stage], kb * BK, n0);
+                    ++issued;
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) drain_tma(ring, stages, issued);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, tphase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
+                        !mbar_wait(&ring.full[stage], phase)) {
+                        record_error(FP8BS_DEVERR_MMA_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_addr(sA + stage * A_TILE);
+                    const uint32_t b_addr = smem_addr(sB + stage * Cfg::B_TILE);
+                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+#pragma unroll
+                    for (int j = 0; j < BK / MMA_K; ++j)
+                        mma_f8(d_tmem, smem_desc_k_sw128(a_addr + j * MMA_K),
+                               smem_desc_k_sw128(b_addr + j * MMA_K), idesc, j > 0 ? 1u : 0u);
+                    mma_commit(&ring.empty[stage]);
+                    mma_commit(&ring.tfull[buf]);
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    buf ^= 1;
+                    if (buf == 0) tphase ^= 1;
+                }
+            }
+            // Make sure nothing this thread issued is still running before TMEM is freed.
+            mma_commit(ring.drain);
+            if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
+        }
+    } else {
+        // Promotion / epilogue warps. Warp w may only touch TMEM lanes 32*(w%4) .. +31.
+        const int ew = warp - 2;
+        const int quarter = warp & 3;
+        const int col0 = (ew >> 2) * Cfg::CW;
+        const int row_in_tile = quarter * 32 + lane;
+        const int nb_count = (g.N + 127) / 128;
+        int buf = 0;
+        uint32_t tphase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const int m0 = (tile % m_tiles) * BM;
+            const int n0 = (tile / m_tiles) * BN;
+            const int row = m0 + row_in_tile;
+            const int nb = min((n0 + col0) / 128, nb_count - 1);
+            const float* as_row = g.a_s + static_cast<int64_t>(min(row, g.M - 1)) * num_kb;
+            const float* bs_row = g.b_s + static_cast<int64_t>(nb) * num_kb;
+            float acc[Cfg::CW];
+#pragma unroll
+            for (int i = 0; i < Cfg::CW; ++i) acc[i] = 0.0f;
+            float sa_next = __ldg(as_row), sb_next = __ldg(bs_row);
+            for (int kb = 0; kb < num_kb; ++kb) {
+                const float sc = sa_next * sb_next;
+                if (kb + 1 < num_kb) {
+                    sa_next = __ldg(as_row + kb + 1);
+                    sb_next = __ldg(bs_row + kb + 1);
+                }
+                if (!warp_wait(&ring.tfull[buf], tphase)) {
+                    if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                       static_cast<uint32_t>(buf * BN + col0);
+#pragma unroll
+                for (int c = 0; c < Cfg::CW / 32; ++c) {
+                    float v[32];
+                    tmem_ld_32cols(taddr + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                buf ^= 1;
+                if (buf == 0) tphase ^= 1;
+            }
+            if (!ok) break;
+            if (row < g.M) {
+                __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(g.c) +
+                                      static_cast<int64_t>(row) * g.N + n0 + col0;
+                const int valid = min(Cfg::CW, g.N - (n0 + col0));
+                if ((g.N & 7) == 0) {
+#pragma unroll
+                    for (int j = 0; j < Cfg::CW / 8; ++j) {
+                        if (8 * j < valid) {
+                            uint4 o;
+                            o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+                            o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+                            o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+                            o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+                            *reinterpret_cast<uint4*>(crow + 8 * j) = o;
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < Cfg::CW; ++j)
+                        if (j < valid) crow[j] = __float2bfloat16_rn(acc[j]);
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// ================================================================ swapped orientation
+
+template <int MT>
+struct SwapCfg {
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int X_TILE = MT * BK;          // activation rows per stage
+    static constexpr int STAGE = A_TILE + X_TILE;   // weight slab + activation rows
+    static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * MT);
+};
+
+template <int MT>
+__global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
+    gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmA, const GemmArgs g,
+                       const int stages) {
+    using Cfg = SwapCfg<MT>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    uint8_t* sW = smem;                                   // [stages][128 x 128] weights
+    uint8_t* sX = smem + stages * A_TILE;                 // [stages][MT x 128] activations
+    const int num_kb = g.K / BK;
+    float* sAs = reinterpret_cast<float*>(sX + stages * Cfg::X_TILE);  // [num_kb][MT]
+    const Ring ring = carve_ring(reinterpret_cast<uint8_t*>(sAs + num_kb * MT), stages);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int n0 = blockIdx.x * BM;
+    const int m0 = blockIdx.y * MT;
+
+    if (threadIdx.x == 0) {
+        init_ring(ring, stages, Cfg::EPI_WARPS);
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
+    // Activation scales of this CTA's MT rows, transposed to [kb][m] (zero past row M).
+    for (int i = threadIdx.x; i < num_kb * MT; i += blockDim.x) {
+        const int kb = i / MT, j = i - kb * MT;
+        sAs[i] = (m0 + j < g.M) ? __ldg(g.a_s + static_cast<int64_t>(m0 + j) * num_kb + kb) : 0.0f;
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *ring.tmem_holder;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            const uint64_t keep = l2_policy_evict_last();   // activations: reused by every CTA
+            const uint64_t stream = l2_policy_evict_first(); // weights: read once
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
+                    record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(&ring.full[stage], Cfg::STAGE);
+                tma_load_2d_hint(sW + stage * A_TILE, &tmB, &ring.full[stage], kb * BK, n0, stream);
+                tma_load_2d_hint(sX + stage * Cfg::X_TILE, &tmA, &ring.full[stage], kb * BK, m0,
+                                 keep);
+                ++issued;
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+            }
+            if (!ok) drain_tma(ring, stages, issued);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            constexpr uint32_t idesc = idesc_e4m3_f32(BM, MT);
+            int stage = 0, buf = 0;
+            uint32_t phase = 0, tphase = 0;
+            for (int kb = 0; kb < num_kb; ++kb) {
+                if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
+                    !mbar_wait(&ring.full[stage], phase)) {
+                    record_error(FP8BS_DEVERR_MMA_WAIT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t w_addr = smem_addr(sW + stage * A_TILE);
+                const uint32_t x_addr = smem_addr(sX + stage * Cfg::X_TILE);
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * MT);
+#pragma unroll
+                for (int j = 0; j < BK / MMA_K; ++j)
+                    mma_f8(d_tmem, smem_desc_k_sw128(w_addr + j * MMA_K),
+                           smem_desc_k_sw128(x_addr + j * MMA_K), idesc, j > 0 ? 1u : 0u);
+                mma_commit(&ring.empty[stage]);
+                mma_commit(&ring.tfull[buf]);
+                if (++stage == stages) {
+                    stage = 0;
+                    phase ^= 1;
+                }
+                buf ^= 1;
+                if (buf == 0) tphase ^= 1;
+            }
+            mma_commit(ring.drain);
+            if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
+        }
+    } else {
+        const int quarter = warp & 3;
+        const int n = n0 + quarter * 32 + lane;      // output column owned by this thread
+        const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+        float acc[MT];
+#pragma unroll
+        for (int i = 0; i < MT; ++i) acc[i] = 0.0f;
+        int buf = 0;
+        uint32_t tphase = 0;
+        bool ok = true;
+        float sb_next = __ldg(bs_row);
+        for (int kb = 0; kb < num_kb; ++kb) {
+            const float sb = sb_next;
+            if (kb + 1 < num_kb) sb_next = __ldg(bs_row + kb + 1);
+            if (!warp_wait(&ring.tfull[buf], tphase)) {
+                if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(buf * MT);
+            const float* as_kb = sAs + kb * MT;
+            if constexpr (MT >= 32) {
+#pragma unroll
+                for (int c = 0; c < MT / 32; ++c) {
+                    float v[32];
+                    tmem_ld_32cols(taddr + c * 32, v);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; i += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4*>(as_kb + c * 32 + i);
+                        acc[c * 32 + i + 0] = fmaf(v[i + 0], a4.x * sb, acc[c * 32 + i + 0]);
+                        acc[c * 32 + i + 1] = fmaf(v[i + 1], a4.y * sb, acc[c * 32 + i + 1]);
+                        acc[c * 32 + i + 2] = fmaf(v[i + 2], a4.z * sb, acc[c * 32 + i + 2]);
+                        acc[c * 32 + i + 3] = fmaf(v[i + 3], a4.w * sb, acc[c * 32 + i + 3]);
+                    }
+                }
+            } else {
+                float v[16];
+                tmem_ld_16cols(taddr, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 16; i += 4) {
+                    const float4 a4 = *reinterpret_cast<const float4*>(as_kb + i);
+                    acc[i + 0] = fmaf(v[i + 0], a4.x * sb, acc[i + 0]);
+                    acc[i + 1] = fmaf(v[i + 1], a4.y * sb, acc[i + 1]);
+                    acc[i + 2] = fmaf(v[i + 2], a4.z * sb, acc[i + 2]);
+                    acc[i + 3] = fmaf(v[i + 3], a4.w * sb, acc[i + 3]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+            buf ^= 1;
+            if (buf == 0) tphase ^= 1;
+        }
+        if (ok && n < g.N) {
+            __nv_bfloat16* c = static_cast<__nv_bfloat16*>(g.c);
+#pragma unroll
+            for (int j = 0; j < MT; ++j)
+                if (m0 + j < g.M) c[static_cast<int64_t>(m0 + j) * g.N + n] = __float2bfloat16_rn(acc[j]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+}
+
+// ================================================================ diagnostics
+
+__global__ void probe_wait_kernel(uint64_t timeout_ns) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        // Nothing ever arrives on `bar`: the wait must run out and report.
+        if (!mbar_wait(&bar, 0, timeout_ns)) record_error(FP8BS_DEVERR_PROBE);
+    }
+}
+
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxStages = 8;
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+template <int BN>
+cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                      int num_sms, cudaStream_t stream) {
+    using Cfg = TnCfg<BN>;
+    int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
+    if (stages > kMaxStages) stages = kMaxStages;
+    const int smem = 1024 + stages * Cfg::STAGE + ring_bytes(stages);
+    cudaError_t e = set_smem(gemm_tn_kernel<BN>, smem);
+    if (e != cudaSuccess) return e;
+    const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+    const int grid = tiles < num_sms ? tiles : num_sms;
+    gemm_tn_kernel<BN><<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, g, stages);
+    return cudaGetLastError();
+}
+
+template <int MT>
+cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const GemmArgs& g,
+                        cudaStream_t stream) {
+    using Cfg = SwapCfg<MT>;
+    const int num_kb = g.K / BK;
+    const int fixed = 1024 + num_kb * MT * 4 + ring_bytes(kMaxStages);
+    int stages = (kSmemLimit - fixed) / Cfg::STAGE;
+    if (stages > kMaxStages) stages = kMaxStages;
+    if (stages < 2) return cudaErrorInvalidValue;   // K too large for the scale staging
+    const int smem = 1024 + stages * Cfg::STAGE + num_kb * MT * 4 + ring_bytes(stages);
+    cudaError_t e = set_smem(gemm_swapab_kernel<MT>, smem);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((g.N + BM - 1) / BM, (g.M + MT - 1) / MT);
+    gemm_swapab_kernel<MT><<<grid, Cfg::THREADS, smem, stream>>>(tmB, tmA, g, stages);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                           int BN, int num_sms, cudaStream_t stream) {
+    switch (BN) {
+        case 128: return launch_tn<128>(tmA, tmB, g, num_sms, stream);
+        case 256: return launch_tn<256>(tmA, tmB, g, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
+                               const GemmArgs& g, int MT, cudaStream_t stream) {
+    switch (MT) {
+        case 16: return launch_swap<16>(tmB, tmA, g, stream);
+        case 32: return launch_swap<32>(tmB, tmA, g, stream);
+        case 64: return launch_swap<64>(tmB, tmA, g, stream);
+        case 128: return launch_swap<128>(tmB, tmA, g, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream) {
+    probe_wait_kernel<<<1, 32, 0, stream>>>(timeout_ns);
+    return cudaGetLastError();
+}
+
+cudaError_t read_device_error(unsigned int* out, bool clear, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_device_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess) return e;
+    if (clear) {
+        static const unsigned int zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(unsigned int), 0,
+                                    cudaMemcpyHostToDevice, stream);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaStreamSynchronize(stream);
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,42 @@
+// kernels.h -- internal launchers behind the C ABI (include/fp8bs.h). Arguments are already
+// validated by the caller; each launcher only enqueues work on `stream` and returns the
+// launch status.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace fp8bs {
+
+cudaError_t launch_act_quant(const void* x, void* y, float* s, int64_t M, int64_t K, bool ue8m0,
+                             int num_sms, cudaStream_t stream);
+
+cudaError_t launch_weight_dequant(const void* w, const float* s, void* y, int64_t N, int64_t K,
+                                  cudaStream_t stream);
+
+// Tensor maps are encoded by the caller (they need the driver entry point).
+struct GemmArgs {
+    const float* a_s;   // [M, K/128]
+    const float* b_s;   // [ceil(N/128), K/128]
+    void* c;            // bf16 [M, N]
+    int M, N, K;
+};
+
+// Normal orientation: 128-row tiles of A on the MMA's M side, BN columns of B on its N side.
+// tmA: box {128, 128} over A [M,K]; tmB: box {128, BN} over B [N,K].
+cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                           int BN, int num_sms, cudaStream_t stream);
+
+// Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
+// on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K].
+cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
+                               const GemmArgs& g, int MT, cudaStream_t stream);
+
+// Diagnostic kernel: one wait on a barrier nothing signals (see fp8bs_probe_wait_timeout).
+cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream);
+
+// The device error word of the GEMM kernels (read/clear).
+cudaError_t read_device_error(unsigned int* out, bool clear, cudaStream_t stream);
+
+}  // namespace fp8bs

@@ -1,0 +1,185 @@
+// quant.cu -- the two bandwidth kernels of the path:
+//   act_quant       ("DeepSeek-V3 Administrator & Developer Guide", §8.5.1 act_quant_kernel)
+//   weight_dequant  (same guide, §8.5.2 weight_dequant_kernel; scale shape §6.3 item 2)
+//
+// Both stream HBM once with 16-byte vector accesses. act_quant: 8 threads own one 128-element
+// block (16 bf16 = 32 bytes each), reduce |x| with 3 xor-shuffles inside the 8-lane group and
+// write 16 e4m3 codes (16 bytes) each; lane 0 of the group writes the block's fp32 scale.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+
+#include "kernels.h"
+
+namespace fp8bs {
+
+namespace {
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Quotient x / s rounded to nearest binary32, from r = RN(1/s): q0 = RN(x r) is within one ulp
+// of x/s, the remainder x - q0 s is exact in one fused multiply-add, and one more fused
+// multiply-add with r lands on RN(x/s). This is Markstein's correction step (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990; stated as Theorem 8 in "Handbook of Floating-Point Arithmetic", ch. 4).
+// Where the remainder underflows (|x/s| < 2^-100 here) the quotient may be off by an ulp,
+// but such quotients convert to a zero e4m3 code either way.
+__device__ __forceinline__ float div_by_scale(float x, float s, float r) {
+    const float q0 = __fmul_rn(x, r);
+    const float rem = __fmaf_rn(-q0, s, x);
+    return __fmaf_rn(rem, r, q0);
+}
+
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+    return static_cast<uint16_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
+}
+
+// Grid-stride over groups of 16 elements; thread g handles x[16g .. 16g+15], which lie in
+// block g/8 (blocks are contiguous because K % 128 == 0).
+template <bool UE8M0>
+__global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict__ x,
+                                                        uint4* __restrict__ y,
+                                                        float* __restrict__ s,
+                                                        int64_t num_groups) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // Every lane of a warp runs the same number of iterations (num_groups is a multiple of 8
+    // and the grid covers whole warps), so the shuffles below are always full-warp.
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         g - (threadIdx.x & 31) < num_groups; g += stride) {
+        const bool active = g < num_groups;
+        uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+        if (active) {
+            v0 = __ldcs(x + 2 * g);
+            v1 = __ldcs(x + 2 * g + 1);
+        }
+        float f[16];
+        const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            f[2 * i] = bf16_lo(w[i]);
+            f[2 * i + 1] = bf16_hi(w[i]);
+        }
+        float amax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(f[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 4));
+        // s = max(amax, 1e-4) / 448 with one IEEE division.
+        float sc = __fdiv_rn(fmaxf(amax, 1e-4f), 448.0f);
+        if (UE8M0) {
+            // 2^ceil(log2 s): s is a positive normal number; if any mantissa bit is set,
+            // clear the mantissa and add one to the exponent.
+            uint32_t bits = __float_as_uint(sc);
+            if (bits & 0x007FFFFFu) bits = (bits & 0xFF800000u) + 0x00800000u;
+            sc = __uint_as_float(bits);
+        }
+        const float r = __frcp_rn(sc);
+        uint32_t out[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t lo = pack_e4m3x2(div_by_scale(f[4 * i], sc, r),
+                                            div_by_scale(f[4 * i + 1], sc, r));
+            const uint32_t hi = pack_e4m3x2(div_by_scale(f[4 * i + 2], sc, r),
+                                            div_by_scale(f[4 * i + 3], sc, r));
+            out[i] = lo | (hi << 16);
+        }
+        if (active) {
+            __stcs(y + g, make_uint4(out[0], out[1], out[2], out[3]));
+            if ((threadIdx.x & 7) == 0) s[g >> 3] = sc;
+        }
+    }
+}
+
+// weight_dequant, vector path (K % 16 == 0): thread g converts 16 consecutive codes of one row.
+__global__ void __launch_bounds__(256) weight_dequant_vec_kernel(const uint4* __restrict__ w,
+                                                                 const float* __restrict__ s,
+                                                                 uint4* __restrict__ y,
+                                                                 int64_t N, int64_t K) {
+    const int64_t groups_per_row = K >> 4;
+    const int64_t kblocks = (K + 127) >> 7;
+    const int64_t total = N * groups_per_row;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += stride) {
+        const int64_t n = g / groups_per_row;
+        const int64_t k = (g - n * groups_per_row) << 4;
+        const float sc = __ldg(s + (n >> 7) * kblocks + (k >> 7));
+        const uint4 v = __ldcs(w + g);
+        const uint32_t words[4] = {v.x, v.y, v.z, v.w};
+        uint32_t out[8];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const __nv_fp8x2_storage_t pair =
+                    static_cast<__nv_fp8x2_storage_t>((words[i] >> (16 * h)) & 0xFFFFu);
+                const float2 f = __half22float2(
+                    __half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
+                const __nv_bfloat162 b =
+                    __floats2bfloat162_rn(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
+                out[2 * i + h] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+        }
+        __stcs(y + 2 * g, make_uint4(out[0], out[1], out[2], out[3]));
+        __stcs(y + 2 * g + 1, make_uint4(out[4], out[5], out[6], out[7]));
+    }
+}
+
+// weight_dequant, general path (any K): one element per thread.
+__global__ void __launch_bounds__(256) weight_dequant_scalar_kernel(
+    const uint8_t* __restrict__ w, const float* __restrict__ s, __nv_bfloat16* __restrict__ y,
+    int64_t N, int64_t K) {
+    const int64_t kblocks = (K + 127) >> 7;
+    const int64_t total = N * K;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += stride) {
+        const int64_t n = i / K;
+        const int64_t k = i - n * K;
+        const float sc = __ldg(s + (n >> 7) * kblocks + (k >> 7));
+        const __half h = __half(__nv_cvt_fp8_to_halfraw(w[i], __NV_E4M3));
+        y[i] = __float2bfloat16_rn(__fmul_rn(__half2float(h), sc));
+    }
+}
+
+int grid_for(int64_t threads, int num_sms) {
+    const int64_t blocks = (threads + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms) * 32;  // grid-stride beyond this
+    return static_cast<int>(blocks < cap ? (blocks > 0 ? blocks : 1) : cap);
+}
+
+}  // namespace
+
+cudaError_t launch_act_quant(const void* x, void* y, float* s, int64_t M, int64_t K, bool ue8m0,
+                             int num_sms, cudaStream_t stream) {
+    const int64_t groups = M * K / 16;
+    const int grid = grid_for(groups, num_sms);
+    if (ue8m0)
+        act_quant_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x),
+                                                         static_cast<uint4*>(y), s, groups);
+    else
+        act_quant_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x),
+                                                          static_cast<uint4*>(y), s, groups);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_weight_dequant(const void* w, const float* s, void* y, int64_t N, int64_t K,
+                                  cudaStream_t stream) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const bool vec = (K % 16 == 0) && (reinterpret_cast<uintptr_t>(w) % 16 == 0) &&
+                     (reinterpret_cast<uintptr_t>(y) % 16 == 0);
+    if (vec) {
+        weight_dequant_vec_kernel<<<grid_for(N * K / 16, sms), 256, 0, stream>>>(
+            static_cast<const uint4*>(w), s, static_cast<uint4*>(y), N, K);
+    } else {
+        weight_dequant_scalar_kernel<<<grid_for(N * K, sms), 256, 0, stream>>>(
+            static_cast<const uint8_t*>(w), s, static_cast<__nv_bfloat16*>(y), N, K);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace fp8bs

@@ -1,0 +1,144 @@
+/*
+ * fp8bs.h -- C ABI of the FP8 block-scaled linear-layer library for NVIDIA GB300 (sm_103a).
+ *
+ * The library implements the three FP8 operations of the DeepSeek-V3 inference demo's linear
+ * path, as the pages describe them:
+ *   - act_quant       "DeepSeek-V3 Administrator & Developer Guide", §8.5.1 act_quant_kernel;
+ *                     ue8m0 scales: "DeepSeek-V3 User Guide", FAQ "What is scale_fmt: ue8m0?".
+ *   - weight_dequant  "DeepSeek-V3 Administrator & Developer Guide", §8.5.2 weight_dequant_kernel
+ *                     (scale shape from §6.3 The FP8 path, item 2).
+ *   - fp8_gemm        "DeepSeek-V3 Administrator & Developer Guide", §8.5.3 fp8_gemm_kernel;
+ *                     used by linear() when gemm_impl == "fp8" (§6.3 item 3).
+ *
+ * Conventions shared by every entry point:
+ *   - Every pointer is a DEVICE pointer into memory the caller owns; the library allocates and
+ *     frees nothing and keeps no per-call state, so calls from several host threads are safe.
+ *   - Matrices are row-major and contiguous. bf16 is the 16-bit brain float; e4m3 is
+ *     float8_e4m3fn (1 byte, largest magnitude 448, no infinity).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is only enqueued:
+ *     no call synchronises the host. Errors that happen while a kernel runs surface at the
+ *     caller's next synchronisation (or through fp8bs_device_error for bounded waits).
+ *   - Arguments are checked before anything is launched; a failed check launches nothing and
+ *     returns a nonzero fp8bs_status. A size of zero (M, N or K where allowed) is a no-op that
+ *     returns FP8BS_OK (fp8bs_gemm with K == 0 writes zeros).
+ *   - Inputs and outputs must not overlap.
+ */
+#ifndef FP8BS_H
+#define FP8BS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Exported symbols stay visible when the library is built with -fvisibility=hidden. */
+#if defined(__GNUC__)
+#define FP8BS_API __attribute__((visibility("default")))
+#else
+#define FP8BS_API
+#endif
+
+/* Quantisation block along K (1 x 128 for activations, 128 x 128 for weights). */
+#define FP8BS_BLOCK 128
+
+typedef enum {
+    FP8BS_SCALE_FP32 = 0,  /* s = max(amax, 1e-4) / 448, one IEEE binary32 division */
+    FP8BS_SCALE_UE8M0 = 1  /* s as above, then rounded up to the nearest power of two */
+} fp8bs_scale_fmt;
+
+typedef enum {
+    FP8BS_OK = 0,
+    FP8BS_ERR_INVALID_ARG = 1,        /* null pointer, negative size, K % 128 != 0, bad enum */
+    FP8BS_ERR_MISALIGNED = 2,         /* a pointer is not 16-byte aligned */
+    FP8BS_ERR_UNSUPPORTED_DEVICE = 3, /* current device is not compute capability 10.3 */
+    FP8BS_ERR_CUDA = 4                /* a CUDA runtime call or launch failed */
+} fp8bs_status;
+
+/*
+ * fp8bs_act_quant -- quantise bf16 activations to e4m3 with one fp32 scale per 1x128 block.
+ * ("DeepSeek-V3 Administrator & Developer Guide", §8.5.1.)
+ *
+ *   x  [in]  bf16 [M, K], 16-byte aligned.
+ *   y  [out] e4m3 [M, K], 16-byte aligned.
+ *   s  [out] fp32 [M, K/128], 4-byte aligned: s[m, b] is the scale of x[m, 128b : 128b+128].
+ *   M >= 0, K >= 0 with K % 128 == 0.
+ *   scale_fmt: FP8BS_SCALE_FP32 or FP8BS_SCALE_UE8M0.
+ *
+ * Per block: amax = max |x|; s = max(amax, 1e-4f) / 448.0f (IEEE binary32 division);
+ * for UE8M0, s = 2^ceil(log2 s) exactly; y = x / s (IEEE binary32 division), converted to
+ * e4m3 with round-to-nearest-even and saturation at +-448. Results are bit-exact.
+ */
+FP8BS_API int fp8bs_act_quant(const void* x, void* y, float* s, int64_t M, int64_t K,
+                              int scale_fmt, void* stream);
+
+/*
+ * fp8bs_weight_dequant -- expand e4m3 weights with 128x128 block scales to bf16.
+ * ("DeepSeek-V3 Administrator & Developer Guide", §8.5.2 and §6.3 item 2.)
+ *
+ *   w  [in]  e4m3 [N, K].
+ *   s  [in]  fp32 [ceil(N/128), ceil(K/128)], 4-byte aligned: one scale per 128x128 block;
+ *            a partial edge block uses its own single scale.
+ *   y  [out] bf16 [N, K].
+ *   N >= 0, K >= 0 (any values). w and y must be 16-byte aligned when K % 16 == 0
+ *   (the vectorised path); otherwise only element alignment is needed.
+ *
+ * y[n, k] = bf16_rne(fp32(w[n, k]) * s[n/128, k/128]) with the product rounded to binary32
+ * first. Results are bit-exact.
+ */
+FP8BS_API int fp8bs_weight_dequant(const void* w, const float* s, void* y, int64_t N,
+                                   int64_t K, void* stream);
+
+/*
+ * fp8bs_gemm -- block-scaled FP8 GEMM C = A . B^T with bf16 output.
+ * ("DeepSeek-V3 Administrator & Developer Guide", §8.5.3.)
+ *
+ *   a    [in]  e4m3 [M, K], 16-byte aligned (typically the act_quant output).
+ *   a_s  [in]  fp32 [M, K/128], 4-byte aligned (per row, per 128-wide K block).
+ *   b    [in]  e4m3 [N, K], 16-byte aligned (a Linear weight, out x in).
+ *   b_s  [in]  fp32 [ceil(N/128), K/128], 4-byte aligned (per 128x128 block of b).
+ *   c    [out] bf16 [M, N], 16-byte aligned.
+ *   M >= 0, N >= 0, K >= 0 with K % 128 == 0.
+ *   scale_fmt: FP8BS_SCALE_FP32 or FP8BS_SCALE_UE8M0; a hint about the scale values only
+ *   (both are read as fp32).
+ *
+ * C[m, n] = sum_kb a_s[m, kb] * b_s[n/128, kb] * sum_{k in block kb} a[m, k] * b[n, k]:
+ * each block's partial product is formed on the tensor cores in fp32, scaled and accumulated
+ * in fp32, and the sum is rounded once to bf16. Accuracy: |C - C_exact| <=
+ * 2^-7 |C_exact| + 1e-3 rms(C_exact) elementwise on the documented workloads.
+ */
+FP8BS_API int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
+                         void* c, int64_t M, int64_t N, int64_t K, int scale_fmt, void* stream);
+
+/* Human-readable name of an fp8bs_status value (a static string; never NULL). */
+FP8BS_API const char* fp8bs_status_string(int status);
+
+/*
+ * fp8bs_device_error -- read (and, if `clear` != 0, reset) the library's device error word
+ * on the current device. Every wait inside the library's kernels is bounded in time; a wait
+ * that runs out sets a bit here (see FP8BS_DEVERR_*), abandons the kernel's remaining work
+ * (its output is then undefined) and lets the kernel exit cleanly. Synchronises `stream`.
+ *   out [out] host pointer receiving the word (0 = no error since the last clear).
+ */
+FP8BS_API int fp8bs_device_error(unsigned int* out, int clear, void* stream);
+
+#define FP8BS_DEVERR_PRODUCER_WAIT 0x1u  /* TMA producer waited too long for a free stage */
+#define FP8BS_DEVERR_MMA_WAIT 0x2u       /* MMA issuer waited too long for data or TMEM */
+#define FP8BS_DEVERR_EPILOGUE_WAIT 0x4u  /* promotion/epilogue waited too long for TMEM */
+#define FP8BS_DEVERR_DRAIN_WAIT 0x8u     /* in-flight copies did not drain after an abort */
+#define FP8BS_DEVERR_PROBE 0x100u        /* set by fp8bs_probe_wait_timeout */
+
+/*
+ * fp8bs_probe_wait_timeout -- diagnostic: launch one block that waits on a shared-memory
+ * barrier that nothing signals, with the given limit in nanoseconds (clamped to 1 ms..2 s).
+ * The wait runs out and sets FP8BS_DEVERR_PROBE in the device error word, exercising the
+ * same bounded-wait path the GEMM kernels use. Enqueued only; read the word with
+ * fp8bs_device_error.
+ */
+FP8BS_API int fp8bs_probe_wait_timeout(uint64_t timeout_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8BS_H */

@@ -53,10 +53,17 @@ uint8_t oracle_e4m3_encode(float v) {
     uint8_t sign = signbit(v) ? 0x80 : 0x00;
     double a = fabs((double)v);
     if (a >= 448.0) return (uint8_t)(sign | 0x7E);
+    /* values of the finite non-negative codes 0x00..0x7E, filled on first use */
+    static double code_value[0x7F];
+    static int have_values = 0;
+    if (!have_values) {
+        for (int c = 0; c <= 0x7E; ++c) code_value[c] = oracle_e4m3_decode((uint8_t)c);
+        have_values = 1;
+    }
     int best = 0;
     double best_err = a; /* distance to code 0x00 (value 0) */
     for (int c = 1; c <= 0x7E; ++c) {
-        double err = fabs(oracle_e4m3_decode((uint8_t)c) - a);
+        double err = fabs(code_value[c] - a);
         /* adjacent codes tie only at their midpoint: take the one with even mantissa LSB */
         if (err < best_err || (err == best_err && (c & 1) == 0)) {
             best = c;

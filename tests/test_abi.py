@@ -1,0 +1,110 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds and loads, exports every
+function that include/*.h declares, and rejects bad arguments before touching the device."""
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import fp8_block_scaled_fp8bs_gb300 as fp8bs
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+OK, INVALID, MISALIGNED, UNSUPPORTED, CUDA = 0, 1, 2, 3, 4
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return fp8bs.load()
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"FP8BS_API\s+[\w\s\*]+?\b(fp8bs_\w+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_library_exports_every_declared_function(lib):
+    names = declared_functions()
+    assert {"fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), f"{n} declared in include/ but not exported"
+
+
+def test_status_strings(lib):
+    for code, text in fp8bs.STATUS.items():
+        assert lib.fp8bs_status_string(code).decode() == text
+    assert lib.fp8bs_status_string(99) == b"unknown status"
+
+
+A16, B16, C16 = 0x10000, 0x20000, 0x30000  # fake, 16-byte aligned; never dereferenced
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, 4, 100, 0), INVALID),   # K % 128
+    ((A16, B16, C16, -1, 128, 0), INVALID),  # negative M
+    ((A16, B16, C16, 4, 128, 7), INVALID),   # bad scale format
+    ((None, B16, C16, 4, 128, 0), INVALID),  # null input
+    ((A16 + 2, B16, C16, 4, 128, 0), MISALIGNED),
+    ((A16, B16 + 8, C16, 4, 128, 0), MISALIGNED),
+    ((A16, B16, C16 + 2, 4, 128, 0), MISALIGNED),
+    ((None, None, None, 0, 128, 0), OK),     # empty: no-op
+    ((None, None, None, 4, 0, 0), OK),
+])
+def test_act_quant_argument_checks(lib, args, expect):
+    assert lib.fp8bs_act_quant(*args, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, -1, 5), INVALID),
+    ((None, B16, C16, 3, 5), INVALID),
+    ((A16, B16 + 1, C16, 3, 5), MISALIGNED),
+    ((A16 + 4, B16, C16, 3, 32), MISALIGNED),  # vector path needs 16-byte alignment
+    ((None, None, None, 0, 5), OK),
+])
+def test_weight_dequant_argument_checks(lib, args, expect):
+    assert lib.fp8bs_weight_dequant(*args, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, B16, C16, 8, 256, 200, 0), INVALID),       # K % 128
+    ((A16, B16, C16, B16, C16, 8, -2, 256, 0), INVALID),
+    ((A16, B16, C16, B16, C16, 8, 256, 256, 3), INVALID),
+    ((A16, B16, None, B16, C16, 8, 256, 256, 0), INVALID),
+    ((A16, B16, C16, B16, None, 8, 256, 256, 0), INVALID),
+    ((A16 + 8, B16, C16, B16, C16, 8, 256, 256, 0), MISALIGNED),
+    ((A16, B16, C16 + 4, B16, C16, 8, 256, 256, 0), MISALIGNED),
+    ((A16, B16 + 2, C16, B16, C16, 8, 256, 256, 0), MISALIGNED),
+    ((A16, B16, C16, B16, C16 + 8, 8, 256, 256, 0), MISALIGNED),
+    ((None, None, None, None, None, 0, 256, 256, 0), OK),
+    ((None, None, None, None, None, 8, 0, 256, 0), OK),
+    ((A16, B16, C16, B16, C16, 1 << 32, 256, 256, 0), INVALID),  # beyond 32-bit coordinates
+])
+def test_gemm_argument_checks(lib, args, expect):
+    assert lib.fp8bs_gemm(*args, None) == expect
+
+
+def test_valid_call_without_a_gpu_reports_an_error_not_a_crash(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert lib.fp8bs_act_quant(A16, B16, C16, 4, 128, 0, None) in (CUDA, UNSUPPORTED)
+    assert lib.fp8bs_gemm(A16, B16, C16, B16, C16, 8, 256, 256, 0, None) in (CUDA, UNSUPPORTED)
+
+
+def test_python_binding_raises_on_error_status():
+    with pytest.raises(fp8bs.Fp8bsError) as ei:
+        fp8bs.fp8bs_gemm(A16, B16, C16, B16, C16, 8, 256, 200)
+    assert ei.value.status == INVALID
+
+
+def test_product_package_does_not_reference_the_oracle():
+    pkg = os.path.join(ROOT, "fp8_block_scaled_fp8bs_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if os.path.isfile(path) and path.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+            text = open(path).read()
+            assert "import oracle" not in text and "oracle." not in text, path
+            assert "liboracle" not in text, path

@@ -1,0 +1,264 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the CPU oracle on seeded
+synthetic inputs. act_quant codes and scales and weight_dequant outputs must be bit-exact;
+fp8_gemm must lie within |C - C_ref| <= 2^-7 |C_ref| + 1e-3 rms(C_ref).
+
+Small shapes compare every element and span several tiles with ragged tails; the full-size
+workloads (decode, prefill, MoE experts, ue8m0 MLA projections) run the kernels in the same
+launch configuration as the benchmark and compare sampled rows/positions, with every output
+tile sampled. Oracle inputs always come from synth or the oracle itself, never from the GPU.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_fp8bs_gb300 as fp8bs
+import oracle
+import synth
+from parity_util import (assert_gemm_close, dev_bf16, dev_e4m3, dev_f32, host_bf16_bits,
+                         host_bf16_f64, host_codes, tile_samples)
+
+pytestmark = pytest.mark.gpu
+
+FMTS = {"fp32": oracle.SCALE_FP32, "ue8m0": oracle.SCALE_UE8M0}
+
+
+@pytest.fixture(autouse=True)
+def _clean_device_error():
+    fp8bs.fp8bs_device_error(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_error(clear=True) == 0, "a kernel wait ran out"
+
+
+def gpu_act_quant(x_bits, fmt):
+    y, s = fp8bs.act_quant(dev_bf16(x_bits), fmt)
+    torch.cuda.synchronize()
+    return host_codes(y), s.cpu().numpy()
+
+
+def assert_quant_equal(y, s, y_ref, s_ref, what):
+    assert np.array_equal(s.view(np.uint32), s_ref.view(np.uint32)), f"{what}: scales differ"
+    bad = np.argwhere(y != y_ref)
+    assert bad.size == 0, f"{what}: {len(bad)} codes differ, first at {bad[:3].tolist()}"
+
+
+# ------------------------------------------------------------------------------ act_quant
+
+@pytest.mark.parametrize("fmt", ["fp32", "ue8m0"])
+@pytest.mark.parametrize("M,K", [(1, 128), (16, 512), (3, 640), (37, 1024), (300, 7168),
+                                 (129, 18432)])
+def test_act_quant_bit_exact_small(fmt, M, K):
+    x = synth.activations(M, K, seed=M * 7 + K, name="pq", outlier_frac=0.01)
+    y, s = gpu_act_quant(x, fmt)
+    y_ref, s_ref = oracle.act_quant(x, FMTS[fmt])
+    assert_quant_equal(y, s, y_ref, s_ref, f"{M}x{K} {fmt}")
+
+
+@pytest.mark.parametrize("fmt", ["fp32", "ue8m0"])
+def test_act_quant_special_blocks(fmt):
+    rng = np.random.default_rng(5)
+    blocks = [np.zeros(128), -np.zeros(128), np.full(128, 448.0), np.full(128, -1e-30),
+              np.r_[1.0, np.zeros(127)], np.r_[-2.0, 1.0, 0.5, -0.25, np.zeros(124)],
+              rng.standard_normal(128) * 1e-6,           # amax below the 1e-4 clamp
+              rng.standard_normal(128) * 3e4,            # large magnitudes
+              np.ldexp(1.0, rng.integers(-133, -120, 128)) * rng.choice([-1, 1], 128),  # tiny
+              rng.standard_normal(128) * np.exp2(rng.uniform(-20, 20, 128)),  # wide range
+              np.linspace(-448, 448, 128),
+              # every value a midpoint-ish neighbour of e4m3 grid points after scaling
+              (np.arange(128) + 0.5) / 128 * 448.0]
+    x = synth.to_bf16_bits(np.stack(blocks).astype(np.float32).reshape(3, -1))
+    y, s = gpu_act_quant(x, fmt)
+    y_ref, s_ref = oracle.act_quant(x, FMTS[fmt])
+    assert_quant_equal(y, s, y_ref, s_ref, f"special {fmt}")
+
+
+def test_act_quant_every_bf16_value_against_every_scale_exponent():
+    """All 65536 bf16 bit patterns (minus NaN/inf) as x, placed in blocks whose amax sets
+    scales across the whole exponent range, so that each x meets many scales."""
+    pats = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = synth.bf16_bits_to_f32(pats)
+    pats = pats[np.isfinite(f)]
+    f = np.abs(synth.bf16_bits_to_f32(pats))
+    rng = np.random.default_rng(17)
+    rows = []
+    for amax_exp in range(-20, 128, 3):
+        amax = np.float32(np.ldexp(1.0 + rng.integers(0, 128) / 128.0, amax_exp))
+        cand = pats[f <= amax]
+        cand = cand[rng.permutation(cand.size)][: 127 * 64]
+        n = cand.size // 127 * 127
+        blk = cand[:n].reshape(-1, 127)
+        lead = np.full((blk.shape[0], 1), synth.to_bf16_bits(np.array([amax]))[0], np.uint16)
+        rows.append(np.concatenate([lead, blk], axis=1))
+    x = np.concatenate(rows).reshape(-1, 128)
+    for fmt in ("fp32", "ue8m0"):
+        y, s = gpu_act_quant(x, fmt)
+        y_ref, s_ref = oracle.act_quant(x, FMTS[fmt])
+        assert_quant_equal(y, s, y_ref, s_ref, f"sweep {fmt}")
+
+
+@pytest.mark.parametrize("name,M,K,fmt", [("decode", 64, 7168, "fp32"),
+                                          ("moe_gathered", 8192, 7168, "fp32"),
+                                          ("prefill_down", 4096, 18432, "fp32"),
+                                          ("mla", 2048, 7168, "ue8m0")])
+def test_act_quant_full_size_sampled_rows(name, M, K, fmt):
+    x = synth.activations(M, K, seed=0, name=f"full/{name}",
+                          outlier_frac=0.0 if name == "mla" else 0.01)
+    y, s = gpu_act_quant(x, fmt)
+    rows = np.unique(np.r_[0, M - 1, np.random.default_rng(1).integers(0, M, 48)])
+    y_ref, s_ref = oracle.act_quant(x[rows], FMTS[fmt])
+    assert_quant_equal(y[rows], s[rows], y_ref, s_ref, name)
+
+
+# ------------------------------------------------------------------------------ weight_dequant
+
+@pytest.mark.parametrize("N,K", [(1, 1), (5, 33), (128, 128), (300, 272), (333, 391),
+                                 (576, 7168), (1000, 1040)])
+def test_weight_dequant_bit_exact_small(N, K):
+    b, s = synth.weights(N, K, seed=N + K, name="pd")
+    y = fp8bs.weight_dequant(dev_e4m3(b), dev_f32(s))
+    torch.cuda.synchronize()
+    assert np.array_equal(host_bf16_bits(y), oracle.weight_dequant(b, s))
+
+
+def test_weight_dequant_full_size_sampled_rows():
+    N, K = synth.INTER, synth.DIM
+    b, s = synth.weights(N, K, seed=0, name="full/dequant")
+    y = host_bf16_bits(fp8bs.weight_dequant(dev_e4m3(b), dev_f32(s)))
+    rows = np.unique(np.r_[0, N - 1, np.random.default_rng(2).integers(0, N, 200)])
+    for r in rows:  # per row: the oracle on one row with its scale row
+        ref = oracle.weight_dequant(b[r:r + 1], s[r // 128:r // 128 + 1])
+        assert np.array_equal(y[r], ref[0]), f"row {r}"
+
+
+# ------------------------------------------------------------------------------ fp8_gemm
+
+def run_gemm(a_codes, a_s, b_codes, b_s, fmt="fp32"):
+    c = fp8bs.fp8_gemm(dev_e4m3(a_codes), dev_f32(a_s), dev_e4m3(b_codes), dev_f32(b_s), fmt)
+    torch.cuda.synchronize()
+    return host_bf16_f64(c)
+
+
+def test_gemm_tiny_config():
+    t = synth.tiny(0)
+    a, a_s = oracle.act_quant(t["x"])
+    b, b_s = t["b"]
+    assert b_s.shape == (2, 4)
+    assert_gemm_close(run_gemm(a, a_s, b, b_s), oracle.gemm(a, a_s, b, b_s), "tiny")
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 256, 512), (8, 576, 1024), (16, 384, 128), (33, 1000, 640), (64, 1536, 1024),
+    (100, 130, 256), (128, 2048, 512),                  # swapped-orientation kernel
+    (129, 256, 512), (200, 640, 1024), (300, 576, 384), (256, 2304, 256), (513, 97, 256),
+    (1200, 4608, 256),                                  # normal kernel, several tiles, tails
+])
+def test_gemm_shapes_full_compare(M, N, K):
+    x = synth.activations(M, K, seed=M + N + K, name="pgA", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x)
+    b, b_s = synth.weights(N, K, seed=M * N + K, name="pgB")
+    assert_gemm_close(run_gemm(a, a_s, b, b_s), oracle.gemm(a, a_s, b, b_s), f"{M}x{N}x{K}")
+
+
+def test_gemm_k_zero_writes_zeros():
+    c = torch.full((5, 24), 3.0, dtype=torch.bfloat16, device="cuda")
+    a = torch.empty((5, 0), dtype=torch.float8_e4m3fn, device="cuda")
+    b = torch.empty((24, 0), dtype=torch.float8_e4m3fn, device="cuda")
+    e = torch.empty((5, 0), dtype=torch.float32, device="cuda")
+    f = torch.empty((1, 0), dtype=torch.float32, device="cuda")
+    fp8bs.fp8_gemm(a, e, b, f, out=c)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c).item() == 0
+
+
+def test_gemm_deterministic():
+    x = synth.activations(256, 1024, seed=3, name="detA")
+    a, a_s = oracle.act_quant(x)
+    b, b_s = synth.weights(4096, 1024, seed=3, name="detB")
+    c1 = run_gemm(a, a_s, b, b_s)
+    c2 = run_gemm(a, a_s, b, b_s)
+    assert np.array_equal(c1, c2)
+
+
+def pipeline_check(x_bits, b, b_s, fmt, what, per_tile=2):
+    """The whole path on the GPU (act_quant then fp8_gemm, as the benchmark runs it); the
+    oracle recomputes act_quant on the sampled rows from the same bf16 input, checks those rows
+    bit-exactly, and evaluates the GEMM at sampled positions from its own codes."""
+    M, K = x_bits.shape
+    N = b.shape[0]
+    y, s = fp8bs.act_quant(dev_bf16(x_bits), fmt)
+    c = fp8bs.fp8_gemm(y, s, dev_e4m3(b), dev_f32(b_s), fmt)
+    torch.cuda.synchronize()
+    mi, ni = tile_samples(M, N, per_tile, seed=M + N)
+    rows = np.unique(mi)
+    a_ref, as_ref = oracle.act_quant(x_bits[rows], FMTS[fmt])
+    assert_quant_equal(host_codes(y)[rows], s.cpu().numpy()[rows], a_ref, as_ref, what)
+    # the oracle's GEMM on its own codes of the sampled rows
+    row_of = {r: i for i, r in enumerate(rows)}
+    local = np.array([row_of[m] for m in mi], dtype=np.int64)
+    ref = oracle.gemm_at(a_ref, as_ref, b, b_s, local, ni)
+    got = host_bf16_f64(c[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()])
+    return assert_gemm_close(got, ref, what)
+
+
+@pytest.mark.parametrize("M", synth.DECODE_MS)
+def test_pipeline_decode_full_size(M):
+    b, b_s = synth.weights(synth.INTER, synth.DIM, seed=0, name="decode/B")
+    pipeline_check(synth.decode(M), b, b_s, "fp32", f"decode M={M}", per_tile=4)
+
+
+@pytest.mark.parametrize("which", ["up", "down"])
+def test_pipeline_prefill_full_size(which):
+    if which == "up":
+        x, (b, b_s) = synth.prefill_up(), synth.weights(synth.INTER, synth.DIM, 0, "prefill/B_up")
+    else:
+        x, (b, b_s) = synth.prefill_down(), synth.weights(synth.DIM, synth.INTER, 0, "prefill/B_down")
+    pipeline_check(x, b, b_s, "fp32", f"prefill {which}", per_tile=1)
+
+
+@pytest.mark.parametrize("N", [synth.Q_LORA, synth.KV_LORA_ROPE])
+def test_pipeline_mla_ue8m0_full_size(N):
+    b, b_s = synth.weights(N, synth.DIM, seed=0, name=f"mla/B{N}", pow2=True)
+    pipeline_check(synth.mla_acts(), b, b_s, "ue8m0", f"mla N={N}", per_tile=2)
+
+
+def test_moe_experts_full_size():
+    rows, counts = synth.moe_routing(0)
+    assert counts.sum() == 8192 and counts.size == 32
+    tokens = synth.activations(1024, synth.DIM, seed=0, name="moe/tokens", outlier_frac=0.01)
+    x = tokens[rows]
+    y, s = fp8bs.act_quant(dev_bf16(x), "fp32")
+    offsets = np.r_[0, np.cumsum(counts)]
+    outs = []
+    weights = [synth.weights(synth.MOE_INTER, synth.DIM, seed=0, name=f"moe/B{e}") for e in range(32)]
+    for e in range(32):
+        lo, hi = offsets[e], offsets[e + 1]
+        b, b_s = weights[e]
+        outs.append(fp8bs.fp8_gemm(y[lo:hi], s[lo:hi], dev_e4m3(b), dev_f32(b_s)))
+    torch.cuda.synchronize()
+    y_h, s_h = host_codes(y), s.cpu().numpy()
+    for e in range(32):
+        lo, hi = offsets[e], offsets[e + 1]
+        if hi == lo:
+            continue
+        b, b_s = weights[e]
+        mi, ni = tile_samples(hi - lo, synth.MOE_INTER, 1, seed=e)
+        rows_e = np.unique(mi)
+        a_ref, as_ref = oracle.act_quant(x[lo + rows_e])
+        assert_quant_equal(y_h[lo + rows_e], s_h[lo + rows_e], a_ref, as_ref, f"expert {e}")
+        row_of = {r: i for i, r in enumerate(rows_e)}
+        ref = oracle.gemm_at(a_ref, as_ref, b, b_s, np.array([row_of[m] for m in mi]), ni)
+        got = host_bf16_f64(outs[e])[mi, ni]
+        assert_gemm_close(got, ref, f"expert {e} (M_e={hi - lo})")
+
+
+# ------------------------------------------------------------------------------ bounded waits
+
+def test_bounded_wait_reports_instead_of_hanging():
+    fp8bs.fp8bs_probe_wait_timeout(5_000_000)  # 5 ms on a barrier nothing signals
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_error(clear=True) & fp8bs.DEVERR_PROBE
+    # the context is still usable
+    t = synth.tiny(0)
+    a, a_s = oracle.act_quant(t["x"])
+    b, b_s = t["b"]
+    assert_gemm_close(run_gemm(a, a_s, b, b_s), oracle.gemm(a, a_s, b, b_s), "after probe")
