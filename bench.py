@@ -1,0 +1,617 @@
+"""Benchmark of the FP8 block-scaled linear path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl {ours,reference}] [--quick]
+
+Headline workload (one JSON line on rank 0): the decode configuration -- for each
+M in {1, 8, 32, 64}: act_quant of a bf16 [M, 7168] activation, then fp8_gemm against an e4m3
+[18432, 7168] weight with 128x128 fp32 block scales. One step runs the four (act_quant, gemm)
+pairs; each M uses its own weight matrix, so a step streams 4 x 132 MB of weights and no
+weight is resident in L2 (129 MB) when it is read again. The metric is algorithmic bytes
+moved per second (GB/s): weights, weight scales, activations, codes, scales and outputs.
+
+Also reported (rank 0, N=1): prefill GEMM TFLOPS, weight_dequant / act_quant GB/s, the MoE
+expert GEMMs and the ue8m0 MLA projections, each against its roofline; the CPU oracle on a
+bounded sample of the decode workload (cpu_baseline); clocks sampled during the timed region.
+
+--impl reference times the CPU oracle instead (the pages publish no runnable reference), on a
+bounded sample of the same workload, and prints the same metric with "impl": "reference".
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (replicas; the path
+has no exchange step): weak scaling, value = bytes of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = ("fp8_gemm TFLOPS & % FP8 peak (prefill M); GB/s & % HBM (quant, decode M)")
+K_DIM, N_DIM = synth.DIM, synth.INTER
+DECODE_MS = synth.DECODE_MS
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
+
+
+# ----------------------------------------------------------------------------- accounting
+
+def act_quant_bytes(M, K):
+    """read bf16 x, write e4m3 y and fp32 scales."""
+    return 2 * M * K + M * K + 4 * M * (K // 128)
+
+
+def gemm_bytes(M, N, K):
+    """read A codes + a_s, B codes + b_s once, write bf16 C."""
+    return M * K + 4 * M * (K // 128) + N * K + 4 * (-(-N // 128)) * (K // 128) + 2 * M * N
+
+
+def dequant_bytes(N, K):
+    return N * K + 4 * (-(-N // 128)) * (-(-K // 128)) + 2 * N * K
+
+
+def gemm_flops(M, N, K):
+    return 2.0 * M * N * K
+
+
+def decode_step_bytes():
+    return sum(act_quant_bytes(M, K_DIM) + gemm_bytes(M, N_DIM, K_DIM) for M in DECODE_MS)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, path: str | None = None):
+        self.index = index
+        self.path = path
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+            if self.path:
+                with open(self.path, "w") as fh:
+                    fh.write(self.QUERY + "\n" + "\n".join(self.lines) + "\n")
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+
+class Gpu:
+    def __init__(self):
+        import torch
+        import fp8_block_scaled_fp8bs_gb300 as fp8bs
+        self.torch = torch
+        self.fp8bs = fp8bs
+        fp8bs.load()
+        self.stream = torch.cuda.current_stream()
+        self.sh = self.stream.cuda_stream
+        self._flush_buf = None
+
+    def bf16(self, bits):
+        return self.torch.from_numpy(np.ascontiguousarray(bits)).view(self.torch.bfloat16).cuda()
+
+    def e4m3(self, codes):
+        return self.torch.from_numpy(np.ascontiguousarray(codes)).view(
+            self.torch.float8_e4m3fn).cuda()
+
+    def f32(self, a):
+        return self.torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
+
+    def flush_l2(self):
+        if self._flush_buf is None:
+            self._flush_buf = self.torch.empty(256 * 1024 * 1024, dtype=self.torch.uint8,
+                                               device="cuda")
+        self._flush_buf.fill_(1)
+
+    def event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    # raw C-ABI calls on the benchmark stream
+    def act_quant(self, x, y, s, M, K, fmt=0):
+        self.fp8bs.fp8bs_act_quant(x.data_ptr(), y.data_ptr(), s.data_ptr(), M, K, fmt, self.sh)
+
+    def gemm(self, a, a_s, b, b_s, c, M, N, K, fmt=0):
+        self.fp8bs.fp8bs_gemm(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
+                              c.data_ptr(), M, N, K, fmt, self.sh)
+
+    def dequant(self, w, s, y, N, K):
+        self.fp8bs.fp8bs_weight_dequant(w.data_ptr(), s.data_ptr(), y.data_ptr(), N, K, self.sh)
+
+    def time_each(self, fn, reps, flush=True):
+        """Median device time (ms) of fn() over reps launches, L2 flushed before each."""
+        ts = []
+        for _ in range(reps):
+            if flush:
+                self.flush_l2()
+            e0, e1 = self.event(), self.event()
+            e0.record()
+            fn()
+            e1.record()
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+
+def decode_setup(g: Gpu, seed=0):
+    torch = g.torch
+    b_codes, b_s = synth.weights(N_DIM, K_DIM, seed, "decode/B")
+    B0, S0 = g.e4m3(b_codes), g.f32(b_s)
+    del b_codes
+    state = []
+    for i, M in enumerate(DECODE_MS):
+        # one distinct weight matrix per M (a perturbed copy of the first: same distribution)
+        B = B0 if i == 0 else torch.roll(B0.view(torch.uint8), shifts=i * 4096, dims=0) \
+            .contiguous().view(torch.float8_e4m3fn)
+        S = S0 if i == 0 else torch.roll(S0, shifts=i * 32, dims=0).contiguous()
+        x = g.bf16(synth.decode(M, seed))
+        state.append(dict(M=M, x=x, B=B, S=S,
+                          y=torch.empty((M, K_DIM), dtype=torch.float8_e4m3fn, device="cuda"),
+                          s=torch.empty((M, K_DIM // 128), dtype=torch.float32, device="cuda"),
+                          c=torch.empty((M, N_DIM), dtype=torch.bfloat16, device="cuda")))
+    return state
+
+
+def decode_step(g: Gpu, state, events=None):
+    for i, st in enumerate(state):
+        M = st["M"]
+        g.act_quant(st["x"], st["y"], st["s"], M, K_DIM)
+        if events is not None:
+            events[i][0].record()
+        g.gemm(st["y"], st["s"], st["B"], st["S"], st["c"], M, N_DIM, K_DIM)
+        if events is not None:
+            events[i][1].record()
+
+
+def run_decode(g: Gpu, steps, warmup, rank, world, clocks_path):
+    torch = g.torch
+    state = decode_setup(g)
+    for _ in range(warmup):
+        decode_step(g, state)
+    torch.cuda.synchronize()
+    ev = [[[g.event(), g.event()] for _ in state] for _ in range(steps)]
+    sampler = ClockSampler(torch.cuda.current_device(), clocks_path)
+    with sampler:
+        time.sleep(0.25)
+        barrier(world)
+        torch.cuda.synchronize()
+        t0, t1 = g.event(), g.event()
+        t0.record()
+        for k in range(steps):
+            decode_step(g, state, ev[k])
+        t1.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        time.sleep(0.25)
+    ms_total = t0.elapsed_time(t1)
+    per_m = []
+    for i, st in enumerate(state):
+        d = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(steps)]
+        per_m.append((st["M"], statistics.mean(d)))
+    return ms_total, per_m, sampler.summary()
+
+
+def run_decode_e2e(g: Gpu, steps, warmup, world):
+    """The same step through the C ABI with host buffers: pinned host -> device copy of each
+    activation, act_quant + fp8_gemm, device -> pinned host copy of each output."""
+    torch = g.torch
+    state = decode_setup(g, seed=1)
+    hx = [st["x"].cpu().pin_memory() for st in state]
+    hc = [torch.empty(st["c"].shape, dtype=torch.bfloat16).pin_memory() for st in state]
+
+    def step():
+        for i, st in enumerate(state):
+            st["x"].copy_(hx[i], non_blocking=True)
+            g.act_quant(st["x"], st["y"], st["s"], st["M"], K_DIM)
+            g.gemm(st["y"], st["s"], st["B"], st["S"], st["c"], st["M"], N_DIM, K_DIM)
+            hc[i].copy_(st["c"], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    barrier(world)
+    t0, t1 = g.event(), g.event()
+    t0.record()
+    for _ in range(steps):
+        step()
+    t1.record()
+    torch.cuda.synchronize()
+    barrier(world)
+    h2d = sum(2 * st["M"] * K_DIM for st in state)
+    d2h = sum(2 * st["M"] * N_DIM for st in state)
+    return t0.elapsed_time(t1), h2d, d2h
+
+
+def secondary(g: Gpu, peaks, reps=10):
+    """Other workloads of the path, each kernel timed alone with L2 flushed before every
+    launch; reported against its roofline."""
+    torch = g.torch
+    out = {}
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = peaks["bf16_tflops"] * FP8_OVER_BF16
+
+    def gemm_entry(name, M, N, K, fmt, x_bits, b_codes, b_s):
+        x = g.bf16(x_bits)
+        y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+        g.act_quant(x, y, s, M, K, fmt)
+        B, S = g.e4m3(b_codes), g.f32(b_s)
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            g.gemm(y, s, B, S, c, M, N, K, fmt)
+        ms = g.time_each(lambda: g.gemm(y, s, B, S, c, M, N, K, fmt), reps)
+        tf = gemm_flops(M, N, K) / ms / 1e9
+        gb = gemm_bytes(M, N, K) / ms / 1e6
+        bound_ms = max(gemm_flops(M, N, K) / (fp8_peak * 1e9), gemm_bytes(M, N, K) / (hbm * 1e6))
+        out[name] = {"M": M, "N": N, "K": K, "us": round(ms * 1e3, 2), "TFLOP/s": round(tf, 1),
+                     "GB/s": round(gb, 1), "frac_fp8_peak": round(tf / fp8_peak, 4),
+                     "frac_roofline": round(bound_ms / ms, 4)}
+        del x, y, s, B, S, c
+
+    xb = synth.prefill_up()
+    bc, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up")
+    gemm_entry("prefill_up", 4096, N_DIM, K_DIM, 0, xb, bc, bs)
+    # weight_dequant of the same [18432, 7168] matrix
+    W, WS = g.e4m3(bc), g.f32(bs)
+    Y = torch.empty((N_DIM, K_DIM), dtype=torch.bfloat16, device="cuda")
+    ms = g.time_each(lambda: g.dequant(W, WS, Y, N_DIM, K_DIM), reps)
+    gbs = dequant_bytes(N_DIM, K_DIM) / ms / 1e6
+    out["weight_dequant"] = {"N": N_DIM, "K": K_DIM, "us": round(ms * 1e3, 2),
+                             "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
+    del W, WS, Y, bc
+    xb = synth.prefill_down()
+    bc, bs = synth.weights(K_DIM, N_DIM, 0, "prefill/B_down")
+    gemm_entry("prefill_down", 4096, K_DIM, N_DIM, 0, xb, bc, bs)
+    del bc
+
+    # act_quant at large row counts (MoE gathered rows; ue8m0 MLA input)
+    for name, M, K, fmt, bits in (("act_quant_moe", 8192, K_DIM, 0, None),
+                                  ("act_quant_mla_ue8m0", 2048, K_DIM, 1, synth.mla_acts())):
+        if bits is None:
+            rows, _ = synth.moe_routing(0)
+            bits = synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows]
+        x = g.bf16(bits)
+        y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+        ms = g.time_each(lambda: g.act_quant(x, y, s, M, K, fmt), reps)
+        gbs = act_quant_bytes(M, K) / ms / 1e6
+        out[name] = {"M": M, "K": K, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                     "frac_hbm": round(gbs / hbm, 4)}
+
+    # ue8m0 MLA projections
+    xa = synth.mla_acts()
+    for N in (synth.Q_LORA, synth.KV_LORA_ROPE):
+        bc, bs = synth.weights(N, K_DIM, 0, f"mla/B{N}", pow2=True)
+        gemm_entry(f"mla_ue8m0_N{N}", 2048, N, K_DIM, 1, xa, bc, bs)
+
+    # MoE: 32 expert GEMMs back to back on one stream, timed as a group
+    rows, counts = synth.moe_routing(0)
+    tokens = synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)
+    x = g.bf16(tokens[rows])
+    y = torch.empty((8192, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+    s = torch.empty((8192, K_DIM // 128), dtype=torch.float32, device="cuda")
+    g.act_quant(x, y, s, 8192, K_DIM)
+    Bs = []
+    for e in range(32):
+        bc, bs = synth.weights(synth.MOE_INTER, K_DIM, 0, f"moe/B{e}")
+        Bs.append((g.e4m3(bc), g.f32(bs)))
+    offs = np.r_[0, np.cumsum(counts)]
+    cs = [torch.empty((int(counts[e]), synth.MOE_INTER), dtype=torch.bfloat16, device="cuda")
+          for e in range(32)]
+
+    def moe():
+        for e in range(32):
+            lo, hi = int(offs[e]), int(offs[e + 1])
+            if hi > lo:
+                g.gemm(y[lo:hi], s[lo:hi], Bs[e][0], Bs[e][1], cs[e], hi - lo,
+                       synth.MOE_INTER, K_DIM)
+    moe()
+    ms = g.time_each(moe, reps)
+    flops = sum(gemm_flops(int(m), synth.MOE_INTER, K_DIM) for m in counts)
+    bound = sum(max(gemm_flops(int(m), synth.MOE_INTER, K_DIM) / (fp8_peak * 1e9),
+                    gemm_bytes(int(m), synth.MOE_INTER, K_DIM) / (hbm * 1e6))
+                for m in counts if m > 0)
+    out["moe_32_experts"] = {"M_e_min": int(counts.min()), "M_e_max": int(counts.max()),
+                             "N": synth.MOE_INTER, "K": K_DIM, "us": round(ms * 1e3, 2),
+                             "TFLOP/s": round(flops / ms / 1e9, 1),
+                             "frac_roofline": round(bound / ms, 4)}
+    return out
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_sample(n_rows: int = 256, seed: int = 0):
+    """Inputs of the bounded decode sample: all four activations, the first n_rows of the
+    weight matrix (2 scale rows)."""
+    b_codes, b_s = synth.weights(N_DIM, K_DIM, seed, "decode/B")
+    b = np.ascontiguousarray(b_codes[:n_rows])
+    bs = np.ascontiguousarray(b_s[: -(-n_rows // 128)])
+    xs = [synth.decode(M, seed) for M in DECODE_MS]
+    return xs, b, bs
+
+
+def oracle_step(xs, b, bs):
+    import oracle
+    for x in xs:
+        y, s = oracle.act_quant(x)
+        oracle.gemm(y, s, b, bs)
+
+
+def oracle_sample_bytes(n_rows):
+    return sum(act_quant_bytes(M, K_DIM) + gemm_bytes(M, n_rows, K_DIM) for M in DECODE_MS)
+
+
+def cpu_baseline(target_s: float = 12.0):
+    n_rows = 256
+    xs, b, bs = oracle_sample(n_rows)
+    t0 = time.perf_counter()
+    oracle_step(xs, b, bs)
+    one = time.perf_counter() - t0
+    reps = max(1, int(target_s / max(one, 1e-3)))
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle_step(xs, b, bs)
+    dt = (time.perf_counter() - t0) / reps
+    return {"value": round(oracle_sample_bytes(n_rows) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": (f"decode workload with N cut to the first {n_rows} of {N_DIM} weight rows: "
+                       f"act_quant of all M in {list(DECODE_MS)} rows x {K_DIM} and fp8_gemm "
+                       f"[M x {n_rows} x {K_DIM}]; single-threaded C, {reps} repetitions, "
+                       f"{dt * 1e3:.1f} ms each")}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+_pg = None
+
+
+def init_dist(world, backend):
+    global _pg
+    if world > 1:
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend)
+        _pg = dist
+
+
+def barrier(world):
+    if world > 1 and _pg is not None:
+        _pg.barrier()
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world == 1 or _pg is None:
+        return value
+    import torch
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    _pg.all_reduce(t, op=_pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- main
+
+def run_profile(case: str, launches: int, warmup: int):
+    """One kernel of the path on its full-size workload, `warmup` + `launches` times, with no
+    other work: the command profiled by ncu (one kernel name per case)."""
+    import torch
+    g = Gpu()
+    if case.startswith("decode"):
+        M = int(case[len("decode"):] or 64)
+        b, bs = synth.weights(N_DIM, K_DIM, 0, "decode/B")
+        B, S = g.e4m3(b), g.f32(bs)
+        x = g.bf16(synth.decode(M))
+        y = torch.empty((M, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((M, K_DIM // 128), dtype=torch.float32, device="cuda")
+        c = torch.empty((M, N_DIM), dtype=torch.bfloat16, device="cuda")
+        g.act_quant(x, y, s, M, K_DIM)
+        fn = lambda: g.gemm(y, s, B, S, c, M, N_DIM, K_DIM)  # noqa: E731
+    elif case in ("prefill_up", "prefill_down"):
+        up = case == "prefill_up"
+        N, K = (N_DIM, K_DIM) if up else (K_DIM, N_DIM)
+        b, bs = synth.weights(N, K, 0, "prefill/B_up" if up else "prefill/B_down")
+        B, S = g.e4m3(b), g.f32(bs)
+        x = g.bf16(synth.prefill_up() if up else synth.prefill_down())
+        y = torch.empty((4096, K), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((4096, K // 128), dtype=torch.float32, device="cuda")
+        c = torch.empty((4096, N), dtype=torch.bfloat16, device="cuda")
+        g.act_quant(x, y, s, 4096, K)
+        fn = lambda: g.gemm(y, s, B, S, c, 4096, N, K)  # noqa: E731
+    elif case == "act_quant":
+        rows, _ = synth.moe_routing(0)
+        x = g.bf16(synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows])
+        y = torch.empty((8192, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((8192, K_DIM // 128), dtype=torch.float32, device="cuda")
+        fn = lambda: g.act_quant(x, y, s, 8192, K_DIM)  # noqa: E731
+    elif case == "dequant":
+        b, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up")
+        W, WS = g.e4m3(b), g.f32(bs)
+        Y = torch.empty((N_DIM, K_DIM), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: g.dequant(W, WS, Y, N_DIM, K_DIM)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown profile case {case!r}")
+    torch.cuda.synchronize()
+    for _ in range(warmup + launches):
+        fn()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile": case, "launches": warmup + launches}), flush=True)
+    return 0
+
+
+def workload_config():
+    return {"workload": (f"decode: act_quant + fp8_gemm for M in {list(DECODE_MS)}, "
+                         f"K={K_DIM}, N={N_DIM}, fp32 block scales"),
+            "M": list(DECODE_MS), "K": K_DIM, "N": N_DIM,
+            "l2": "inputs larger than L2: each M has its own 132 MB weight (528 MB per step)",
+            "parallelism": "replicas"}
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    n_rows = 256
+    xs, b, bs = oracle_sample(n_rows)
+    for _ in range(args.warmup):
+        oracle_step(xs, b, bs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step(xs, b, bs)
+    dt = time.perf_counter() - t0
+    value = oracle_sample_bytes(n_rows) * args.steps / dt / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle",
+                             "sample": f"per step: decode workload with N cut to {n_rows} of "
+                                       f"{N_DIM} weight rows (all M rows of act_quant)"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--quick", action="store_true", help="headline only: no secondary workloads "
+                    "and no CPU baseline")
+    ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
+    ap.add_argument("--profile", metavar="CASE", default=None,
+                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, "
+                         "act_quant, dequant): warmup + steps launches, for ncu")
+    args = ap.parse_args(argv)
+    if args.warmup < 3 and not args.profile:
+        ap.error("--warmup must be at least 3")
+    world, rank, local = dist_env()
+
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    if args.profile:
+        return run_profile(args.profile, args.steps, args.warmup)
+
+    import torch
+    torch.cuda.set_device(local)
+    init_dist(world, "nccl")
+    g = Gpu()
+    peaks = load_peaks()
+    os.makedirs(args.out_dir, exist_ok=True)
+    clocks_path = os.path.join(args.out_dir, f"clocks_rank{rank}.csv")
+
+    ms_total, per_m, clocks = run_decode(g, args.steps, args.warmup, rank, world, clocks_path)
+    ms_total = max_over_ranks(ms_total, world, "cuda")
+    e2e_ms, h2d, d2h = run_decode_e2e(g, args.steps, args.warmup, world)
+    e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
+
+    step_bytes = decode_step_bytes()
+    ms_per_step = ms_total / args.steps
+    value = world * step_bytes / (ms_per_step * 1e6)
+    e2e_value = world * step_bytes / (e2e_ms / args.steps * 1e6)
+
+    gemm_bytes_total = sum(gemm_bytes(M, N_DIM, K_DIM) for M in DECODE_MS)
+    gemm_ms = sum(d for _, d in per_m)
+    achieved = gemm_bytes_total / (gemm_ms * 1e6)
+    roofline = {"kernel": "gemm_swapab_kernel (decode fp8_gemm, all four M)",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+                "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
+                "traffic": None,
+                "per_launch": [{"M": M, "us": round(d * 1e3, 2),
+                                "GB/s": round(gemm_bytes(M, N_DIM, K_DIM) / (d * 1e6), 1)}
+                               for M, d in per_m]}
+
+    line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
+            "data": "synthetic", "config": workload_config(),
+            "clocks": clocks, "roofline": roofline,
+            "e2e": {"value": round(e2e_value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": 2 * len(DECODE_MS) * args.steps}
+    if rank == 0 and world == 1 and not args.quick:
+        line["secondary"] = secondary(g, peaks)
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        _pg.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

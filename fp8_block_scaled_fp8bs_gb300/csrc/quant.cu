@@ -21,13 +21,16 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 // of x/s, the remainder x - q0 s is exact in one fused multiply-add, and one more fused
 // multiply-add with r lands on RN(x/s). This is Markstein's correction step (P. Markstein,
 // "Computation of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
-// Dev. 34(1), 1990; stated as Theorem 8 in "Handbook of Floating-Point Arithmetic", ch. 4).
-// Where the remainder underflows (|x/s| < 2^-100 here) the quotient may be off by an ulp,
-// but such quotients convert to a zero e4m3 code either way.
+// Dev. 34(1), 1990; also in Muller et al., "Handbook of Floating-Point Arithmetic"). For the
+// values that occur here (x and amax bf16, s = RN(max(amax, 1e-4) / 448)) the identity is
+// checked exhaustively on the host by the test suite.
+// The correction step adds +0 to a zero quotient, which would turn x = -0 into +0; the sign
+// of x is put back (for x != 0 the quotient already carries it, as s > 0).
 __device__ __forceinline__ float div_by_scale(float x, float s, float r) {
     const float q0 = __fmul_rn(x, r);
     const float rem = __fmaf_rn(-q0, s, x);
-    return __fmaf_rn(rem, r, q0);
+    const float q = __fmaf_rn(rem, r, q0);
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(x) & 0x80000000u));
 }
 
 __device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
