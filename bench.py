@@ -163,10 +163,12 @@ class Gpu:
         return self.torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
 
     def flush_l2(self):
+        """Evict L2 by reading 256 MB: the cache then holds clean lines, so the next kernel
+        pays no write-back of the flush (a write-based flush would leave ~129 MB dirty)."""
         if self._flush_buf is None:
-            self._flush_buf = self.torch.empty(256 * 1024 * 1024, dtype=self.torch.uint8,
-                                               device="cuda")
-        self._flush_buf.fill_(1)
+            self._flush_buf = self.torch.ones(32 * 1024 * 1024, dtype=self.torch.int64,
+                                              device="cuda")
+        self._flush_buf.sum()
 
     def event(self):
         return self.torch.cuda.Event(enable_timing=True)
