@@ -5,13 +5,14 @@
 // "DeepSeek-V3 Administrator & Developer Guide", §8.5.3 fp8_gemm_kernel.
 //
 // Structure (one CTA per SM, warp-specialised):
-//   warp 0      TMA producer: streams 128-byte-wide K slices of A and B into a ring of
-//               shared-memory stages (128-byte swizzle), completion counted on mbarriers.
-//   warp 1      MMA issuer: for each K block, 4 x tcgen05.mma (K = 32 each) into one of two
-//               TMEM buffers, then tcgen05.commit to free the stage and publish the buffer.
-//   warps 2..   promotion/epilogue: tcgen05.ld the block's fp32 partial from TMEM, release
-//               the buffer, and fold it into fp32 registers with the block's scale
-//               a_s[m,kb] * b_s[n/128,kb]. After the last block: round to bf16 and store.
+//   TMA producer warp   streams 128-byte-wide K slices of A and B into a ring of shared-memory
+//                       stages (128-byte swizzle), completion counted on mbarriers.
+//   MMA issuer warp     for each K block, 4 x tcgen05.mma (K = 32 each) into one of two TMEM
+//                       buffers, then tcgen05.commit to free the stage and publish the buffer.
+//   promotion warps     tcgen05.ld the block's fp32 partial from TMEM in 32-column chunks (the
+//                       next chunk's load in flight while the current one is folded in),
+//                       release the buffer, and fold it into fp32 registers with the block's
+//                       scale a_s[m,kb] * b_s[n/128,kb]. After the last block: bf16 and store.
 // The two TMEM buffers let the tensor cores compute block kb+1 while block kb is promoted.
 //
 // Two orientations share this scheme:
@@ -111,16 +112,56 @@ __device__ __forceinline__ void drain_tma(const Ring& r, int stages, int64_t iss
 
 // ================================================================ normal orientation
 
-// Tile = 128 rows of A x BN columns of B; EPI_WARPS promotion warps (4 per 128 columns).
+// Scales of four consecutive K blocks starting at block k (k a multiple of 4): one 16-byte
+// load when the row is 16-byte aligned and holds whole groups of four, else scalar loads.
+__device__ __forceinline__ float4 load_scales4(const float* row, int k, int n, bool vec) {
+    if (vec && k + 4 <= n) return __ldg(reinterpret_cast<const float4*>(row + k));
+    float4 r;
+    r.x = k < n ? __ldg(row + k) : 0.0f;
+    r.y = k + 1 < n ? __ldg(row + k + 1) : 0.0f;
+    r.z = k + 2 < n ? __ldg(row + k + 2) : 0.0f;
+    r.w = k + 3 < n ? __ldg(row + k + 3) : 0.0f;
+    return r;
+}
+
+__device__ __forceinline__ float pick4(const float4& v, int j) {
+    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
+}
+
+// Tile = 128 rows of A x BN columns of B. Warp layout (whole warpgroups, so that register
+// budgets can be moved between them):
+//   warps 0 .. EPI_WARPS-1   promotion/epilogue, 4 warps per 128 columns (warp w reads TMEM
+//                            lanes 32*(w%4) .. +31, columns 128*(w/4) .. +127 of the tile)
+//   warp EPI_WARPS           TMA producer
+//   warp EPI_WARPS+1         MMA issuer (also allocates and frees TMEM)
+//   warps EPI_WARPS+2, +3    idle (they complete the last warpgroup)
+// With BN = 256 the block has 384 threads and each thread starts with 168 registers; the
+// control warpgroup gives registers back (kCtlRegs) and the promotion warpgroups take them
+// (kEpiRegs). 4*32*kCtlRegs + 8*32*kEpiRegs <= 384*168 keeps the split inside the block's
+// launch allocation, so setmaxnreg.inc never waits.
 template <int BN>
 struct TnCfg {
-    static constexpr int EPI_WARPS = BN / 32;                 // 4 warps per 128 columns
+    static constexpr int EPI_WARPS = BN / 32;
     static constexpr int CW = 128;                            // columns per promotion thread
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
+    static constexpr int THREADS = 32 * EPI_WARPS + 128;
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
+    static constexpr bool SPLIT_REGS = (BN == 256);
+    static constexpr uint32_t kCtlRegs = 40;
+    static constexpr uint32_t kEpiRegs = 232;
+    static_assert(!SPLIT_REGS || 4 * 32 * kCtlRegs + 8 * 32 * kEpiRegs <= 384 * 168,
+                  "register split exceeds the launch allocation");
 };
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
 
 template <int BN>
 __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
@@ -139,20 +180,23 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     const int m_tiles = (g.M + BM - 1) / BM;
     const int n_tiles = (g.N + BN - 1) / BN;
     const int num_tiles = m_tiles * n_tiles;
+    constexpr int PRODUCER = Cfg::EPI_WARPS;
+    constexpr int ISSUER = Cfg::EPI_WARPS + 1;
 
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
+    if (warp == ISSUER) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
 
-    if (warp == 0) {
-        if (lane == 0) {
+    if (warp >= Cfg::EPI_WARPS) {
+        if constexpr (Cfg::SPLIT_REGS) regs_dec<Cfg::kCtlRegs>();
+        if (warp == PRODUCER && lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
@@ -177,9 +221,7 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                 }
             }
             if (!ok) drain_tma(ring, stages, issued);
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
+        } else if (warp == ISSUER && lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, BN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
@@ -215,12 +257,15 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
             if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
         }
     } else {
-        // Promotion / epilogue warps. Warp w may only touch TMEM lanes 32*(w%4) .. +31.
-        const int ew = warp - 2;
+        if constexpr (Cfg::SPLIT_REGS) regs_inc<Cfg::kEpiRegs>();
+        // Promotion / epilogue warps.
         const int quarter = warp & 3;
-        const int col0 = (ew >> 2) * Cfg::CW;
+        const int col0 = (warp >> 2) * Cfg::CW;
         const int row_in_tile = quarter * 32 + lane;
         const int nb_count = (g.N + 127) / 128;
+        const bool vec_scales = (num_kb % 4 == 0) &&
+                                ((reinterpret_cast<uintptr_t>(g.a_s) & 15u) == 0) &&
+                                ((reinterpret_cast<uintptr_t>(g.b_s) & 15u) == 0);
         int buf = 0;
         uint32_t tphase = 0;
         bool ok = true;
@@ -234,12 +279,19 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
             float acc[Cfg::CW];
 #pragma unroll
             for (int i = 0; i < Cfg::CW; ++i) acc[i] = 0.0f;
-            float sa_next = __ldg(as_row), sb_next = __ldg(bs_row);
+            // Scales in groups of four K blocks, the next group in flight.
+            float4 a_cur = load_scales4(as_row, 0, num_kb, vec_scales);
+            float4 b_cur = load_scales4(bs_row, 0, num_kb, vec_scales);
+            float4 a_nxt = load_scales4(as_row, 4, num_kb, vec_scales);
+            float4 b_nxt = load_scales4(bs_row, 4, num_kb, vec_scales);
             for (int kb = 0; kb < num_kb; ++kb) {
-                const float sc = sa_next * sb_next;
-                if (kb + 1 < num_kb) {
-                    sa_next = __ldg(as_row + kb + 1);
-                    sb_next = __ldg(bs_row + kb + 1);
+                const int j = kb & 3;
+                const float sc = pick4(a_cur, j) * pick4(b_cur, j);
+                if (j == 3) {
+                    a_cur = a_nxt;
+                    b_cur = b_nxt;
+                    a_nxt = load_scales4(as_row, kb + 5, num_kb, vec_scales);
+                    b_nxt = load_scales4(bs_row, kb + 5, num_kb, vec_scales);
                 }
                 if (!warp_wait(&ring.tfull[buf], tphase)) {
                     if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
@@ -249,17 +301,25 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + col0);
+                // Four chunks of 32 columns: the load of chunk c+1 is in flight while chunk c is
+                // folded in; the buffer is handed back as soon as the last chunk has landed.
+                float va[32], vb[32];
+                tmem_ld_32cols(taddr, va);
+                tmem_wait_ld_32(va);
 #pragma unroll
                 for (int c = 0; c < Cfg::CW / 32; ++c) {
-                    float v[32];
-                    tmem_ld_32cols(taddr + c * 32, v);
-                    tmem_wait_ld();
+                    float* cur = (c & 1) ? vb : va;
+                    float* nxt = (c & 1) ? va : vb;
+                    if (c + 1 < Cfg::CW / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+                    if (c + 1 == Cfg::CW / 32) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                    }
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(v[i], sc, acc[c * 32 + i]);
+                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(cur[i], sc, acc[c * 32 + i]);
+                    if (c + 1 < Cfg::CW / 32) tmem_wait_ld_32(nxt);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&ring.tempty[buf]);
                 buf ^= 1;
                 if (buf == 0) tphase ^= 1;
             }
@@ -292,7 +352,7 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (warp == ISSUER) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
 // ================================================================ swapped orientation
@@ -331,11 +391,6 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
         tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
-    // Activation scales of this CTA's MT rows, transposed to [kb][m] (zero past row M).
-    for (int i = threadIdx.x; i < num_kb * MT; i += blockDim.x) {
-        const int kb = i / MT, j = i - kb * MT;
-        sAs[i] = (m0 + j < g.M) ? __ldg(g.a_s + static_cast<int64_t>(m0 + j) * num_kb + kb) : 0.0f;
-    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -399,19 +454,26 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
             if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
         }
     } else {
+        // Combined scales a_s[m, kb] * b_s[slab, kb] of this CTA's MT rows, transposed to
+        // [kb][m] (zero past row M). Only the promotion warps need them, so the producer and
+        // the MMA issuer start streaming while they are staged; reads are coalesced along kb.
+        const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+        for (int i = threadIdx.x - 64; i < num_kb * MT; i += 32 * Cfg::EPI_WARPS) {
+            const int j = i / num_kb, kb = i - j * num_kb;
+            sAs[kb * MT + j] = (m0 + j < g.M) ? __ldg(g.a_s + static_cast<int64_t>(m0 + j) * num_kb + kb) *
+                                                     __ldg(bs_row + kb)
+                                               : 0.0f;
+        }
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         const int quarter = warp & 3;
         const int n = n0 + quarter * 32 + lane;      // output column owned by this thread
-        const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
         float acc[MT];
 #pragma unroll
         for (int i = 0; i < MT; ++i) acc[i] = 0.0f;
         int buf = 0;
         uint32_t tphase = 0;
         bool ok = true;
-        float sb_next = __ldg(bs_row);
         for (int kb = 0; kb < num_kb; ++kb) {
-            const float sb = sb_next;
-            if (kb + 1 < num_kb) sb_next = __ldg(bs_row + kb + 1);
             if (!warp_wait(&ring.tfull[buf], tphase)) {
                 if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
                 ok = false;
@@ -422,36 +484,47 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
                                    static_cast<uint32_t>(buf * MT);
             const float* as_kb = sAs + kb * MT;
             if constexpr (MT >= 32) {
+                // Chunks of 32 columns, the next load in flight while one is folded in.
+                constexpr int NCH = MT / 32;
+                float va[32], vb[32];
+                tmem_ld_32cols(taddr, va);
+                tmem_wait_ld_32(va);
 #pragma unroll
-                for (int c = 0; c < MT / 32; ++c) {
-                    float v[32];
-                    tmem_ld_32cols(taddr + c * 32, v);
-                    tmem_wait_ld();
+                for (int c = 0; c < NCH; ++c) {
+                    float* cur = (c & 1) ? vb : va;
+                    float* nxt = (c & 1) ? va : vb;
+                    if (c + 1 < NCH) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+                    if (c + 1 == NCH) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                    }
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         const float4 a4 = *reinterpret_cast<const float4*>(as_kb + c * 32 + i);
-                        acc[c * 32 + i + 0] = fmaf(v[i + 0], a4.x * sb, acc[c * 32 + i + 0]);
-                        acc[c * 32 + i + 1] = fmaf(v[i + 1], a4.y * sb, acc[c * 32 + i + 1]);
-                        acc[c * 32 + i + 2] = fmaf(v[i + 2], a4.z * sb, acc[c * 32 + i + 2]);
-                        acc[c * 32 + i + 3] = fmaf(v[i + 3], a4.w * sb, acc[c * 32 + i + 3]);
+                        acc[c * 32 + i + 0] = fmaf(cur[i + 0], a4.x, acc[c * 32 + i + 0]);
+                        acc[c * 32 + i + 1] = fmaf(cur[i + 1], a4.y, acc[c * 32 + i + 1]);
+                        acc[c * 32 + i + 2] = fmaf(cur[i + 2], a4.z, acc[c * 32 + i + 2]);
+                        acc[c * 32 + i + 3] = fmaf(cur[i + 3], a4.w, acc[c * 32 + i + 3]);
                     }
+                    if (c + 1 < NCH) tmem_wait_ld_32(nxt);
                 }
             } else {
                 float v[16];
                 tmem_ld_16cols(taddr, v);
-                tmem_wait_ld();
+                tmem_wait_ld_16(v);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ring.tempty[buf]);
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
                     const float4 a4 = *reinterpret_cast<const float4*>(as_kb + i);
-                    acc[i + 0] = fmaf(v[i + 0], a4.x * sb, acc[i + 0]);
-                    acc[i + 1] = fmaf(v[i + 1], a4.y * sb, acc[i + 1]);
-                    acc[i + 2] = fmaf(v[i + 2], a4.z * sb, acc[i + 2]);
-                    acc[i + 3] = fmaf(v[i + 3], a4.w * sb, acc[i + 3]);
+                    acc[i + 0] = fmaf(v[i + 0], a4.x, acc[i + 0]);
+                    acc[i + 1] = fmaf(v[i + 1], a4.y, acc[i + 1]);
+                    acc[i + 2] = fmaf(v[i + 2], a4.z, acc[i + 2]);
+                    acc[i + 3] = fmaf(v[i + 3], a4.w, acc[i + 3]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
             buf ^= 1;
             if (buf == 0) tphase ^= 1;
         }
