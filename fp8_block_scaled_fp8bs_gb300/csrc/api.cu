@@ -153,6 +153,12 @@ int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
         if (e != cudaErrorInvalidValue) return status_of(e);
         // K too long to stage the activation scales: fall through to the normal kernel.
     }
+    // Enough 256 x 256 tiles to give every SM pair one: CTA pairs (cta_group::2).
+    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
+    if (pair_tiles >= sms / 2) {
+        if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, 128)) return FP8BS_ERR_CUDA;
+        return status_of(fp8bs::launch_gemm_pair(tmA, tmB, g, sms, st));
+    }
     const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
     const int BN = tiles256 >= sms ? 256 : 128;
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;

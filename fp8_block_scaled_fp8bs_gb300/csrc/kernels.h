@@ -28,6 +28,12 @@ struct GemmArgs {
 cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
                            int BN, int num_sms, cudaStream_t stream);
 
+// CTA pairs: 256-row tiles of A x 256 columns of B, computed by two CTAs with cta_group::2.
+// tmA: box {128, 128} over A [M,K]; tmB: box {128, 128} over B [N,K] (each CTA loads half of
+// the tile's 256 rows of B).
+cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                             int num_sms, cudaStream_t stream);
+
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
 // on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K].
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,

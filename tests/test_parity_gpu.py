@@ -150,7 +150,9 @@ def test_gemm_tiny_config():
     (1, 256, 512), (8, 576, 1024), (16, 384, 128), (33, 1000, 640), (64, 1536, 1024),
     (100, 130, 256), (128, 2048, 512),                  # swapped-orientation kernel
     (129, 256, 512), (200, 640, 1024), (300, 576, 384), (256, 2304, 256), (513, 97, 256),
-    (1200, 4608, 256),                                  # normal kernel, several tiles, tails
+                                                        # one-CTA kernel, several tiles, tails
+    (1200, 4608, 256), (1100, 4736, 256), (1024, 4800, 384), (768, 5120, 1280),
+                                                        # CTA-pair kernel, ragged pair tiles
 ])
 def test_gemm_shapes_full_compare(M, N, K):
     x = synth.activations(M, K, seed=M + N + K, name="pgA", outlier_frac=0.01)
