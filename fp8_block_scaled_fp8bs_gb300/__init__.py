@@ -9,12 +9,14 @@ Raw entry points (same names and arguments as the C functions; pointers are ints
     fp8bs_act_quant(x, y, s, M, K, scale_fmt, stream)
     fp8bs_weight_dequant(w, s, y, N, K, stream)
     fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream)
+    fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt, stream)
     fp8bs_device_error(clear=True, stream=0) -> int
     fp8bs_probe_wait_timeout(timeout_ns, stream)
 Tensor conveniences (PyTorch CUDA tensors; outputs allocated with torch):
     act_quant(x, scale_fmt="fp32") -> (y, s)      ("DeepSeek-V3 Administrator & Developer
     weight_dequant(w, s) -> y                        Guide", §8.5.1, §8.5.2, §8.5.3)
     fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32") -> c
+    fp8_gemm_grouped(a, a_s, b, b_s, row_offsets, scale_fmt="fp32") -> c
 """
 from __future__ import annotations
 
@@ -31,8 +33,8 @@ DEVERR_PROBE = 0x100
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
-EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_status_string",
-           "fp8bs_device_error", "fp8bs_probe_wait_timeout")
+EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_grouped",
+           "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
 
 _lock = threading.Lock()
 _lib = None
@@ -59,6 +61,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_act_quant.argtypes = [vp, vp, vp, i64, i64, i32, vp]
         lib.fp8bs_weight_dequant.argtypes = [vp, vp, vp, i64, i64, vp]
         lib.fp8bs_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+        lib.fp8bs_gemm_grouped.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
+                                           i64, i64, i64, i32, vp]
         lib.fp8bs_status_string.argtypes = [i32]
         lib.fp8bs_status_string.restype = ctypes.c_char_p
         lib.fp8bs_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, vp]
@@ -87,6 +91,14 @@ def fp8bs_weight_dequant(w, s, y, N, K, stream=0) -> None:
 
 def fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, stream=0) -> None:
     _check("fp8bs_gemm", load().fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream))
+
+
+def fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt=SCALE_FP32,
+                       stream=0) -> None:
+    """row_offsets: a sequence of groups+1 ints (host memory)."""
+    offs = (ctypes.c_int64 * (int(groups) + 1))(*[int(x) for x in row_offsets])
+    _check("fp8bs_gemm_grouped", load().fp8bs_gemm_grouped(a, a_s, b, b_s, c, offs, groups, N, K,
+                                                           scale_fmt, stream))
 
 
 def fp8bs_device_error(clear: bool = True, stream=0) -> int:
@@ -164,4 +176,24 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None):
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
     fp8bs_gemm(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
                M, N, K, _fmt(scale_fmt), _stream())
+    return c
+
+
+def fp8_gemm_grouped(a, a_s, b, b_s, row_offsets, scale_fmt="fp32", out=None):
+    """Per-group block-scaled GEMMs: a [T,K] e4m3 with rows grouped by row_offsets (groups+1
+    host ints), b [G,N,K] e4m3, b_s [G, ceil(N/128), K/128] -> c [T,N] bf16."""
+    import torch
+    _require(a, torch.float8_e4m3fn, 2, "a")
+    _require(b, torch.float8_e4m3fn, 3, "b")
+    _require(a_s, torch.float32, 2, "a_s")
+    _require(b_s, torch.float32, 3, "b_s")
+    T, K = a.shape
+    G, N = b.shape[0], b.shape[1]
+    offs = [int(x) for x in row_offsets]
+    if len(offs) != G + 1 or offs[0] != 0 or offs[-1] != T or b.shape[2] != K or \
+            tuple(a_s.shape) != (T, K // BLOCK) or tuple(b_s.shape) != (G, -(-N // BLOCK), K // BLOCK):
+        raise ValueError("operand, scale or offset shapes do not match")
+    c = out if out is not None else torch.empty((T, N), dtype=torch.bfloat16, device=a.device)
+    fp8bs_gemm_grouped(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
+                       offs, G, N, K, _fmt(scale_fmt), _stream())
     return c

@@ -153,16 +153,58 @@ int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
         if (e != cudaErrorInvalidValue) return status_of(e);
         // K too long to stage the activation scales: fall through to the normal kernel.
     }
-    // Enough 256 x 256 tiles to give every SM pair one: CTA pairs (cta_group::2).
-    const int64_t pair_tiles = ((M + 255) / 256) * ((N + 255) / 256);
-    if (pair_tiles >= sms / 2) {
-        if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, 128)) return FP8BS_ERR_CUDA;
-        return status_of(fp8bs::launch_gemm_pair(tmA, tmB, g, sms, st));
-    }
     const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
     const int BN = tiles256 >= sms ? 256 : 128;
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
-    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, BN, sms, st));
+    const int64_t rows[2] = {0, M};
+    fp8bs::GroupTable gt;
+    fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), BN);
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
+}
+
+int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
+                       const int64_t* row_offsets, int64_t groups, int64_t N, int64_t K,
+                       int scale_fmt, void* stream) {
+    if (groups < 0 || groups > fp8bs::kMaxGroups || N < 0 || K < 0 || K % FP8BS_BLOCK != 0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (groups == 0 || N == 0) return FP8BS_OK;
+    if (!row_offsets || row_offsets[0] != 0) return FP8BS_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < groups; ++i)
+        if (row_offsets[i + 1] < row_offsets[i]) return FP8BS_ERR_INVALID_ARG;
+    const int64_t M = row_offsets[groups];
+    if (M > INT32_MAX || N * groups > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (M == 0) return FP8BS_OK;
+    if (!c) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(c)) return FP8BS_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        int sms = 0;
+        if (int e = check_device(&sms)) return e;
+        return status_of(cudaMemsetAsync(c, 0, static_cast<size_t>(M * N) * 2, st));
+    }
+    if (!a || !a_s || !b || !b_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned4(a_s) || !aligned4(b_s))
+        return FP8BS_ERR_MISALIGNED;
+    int sms = 0;
+    if (int e = check_device(&sms)) return e;
+
+    GemmArgs g;
+    g.a_s = a_s;
+    g.b_s = b_s;
+    g.c = c;
+    g.M = static_cast<int>(M);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    fp8bs::GroupTable gt;
+    fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, 256);
+    const int BN = gt.tile_off[groups] >= sms ? 256 : 128;
+    if (BN != 256) fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, BN);
+    CUtensorMap tmA, tmB;
+    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
+        return FP8BS_ERR_CUDA;
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
 }
 
 int fp8bs_device_error(unsigned int* out, int clear, void* stream) {

@@ -58,6 +58,13 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
     return __all_sync(0xffffffffu, ok);
 }
 
+// acc[0..1] += (v0, v1) * (s0, s1) as one packed fp32x2 FMA (round-to-nearest per component).
+__device__ __forceinline__ void fma2_into(float* acc, float v0, float v1, float s0, float s1) {
+    const float2 r = __ffma2_rn(make_float2(v0, v1), make_float2(s0, s1), make_float2(acc[0], acc[1]));
+    acc[0] = r.x;
+    acc[1] = r.y;
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&b);
@@ -163,10 +170,30 @@ __device__ __forceinline__ void regs_dec() {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
 }
 
+// Coordinates of one output tile: group, first row (global), first column, end of the group's
+// rows. Tiles are numbered group by group, m tiles fastest within a group.
+struct TileCoord {
+    int g, m0, n0, row_end;
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord decode_tile(const GroupTable& gt, int tile, int n_tiles) {
+    int grp = 0;
+    while (tile >= gt.tile_off[grp + 1]) ++grp;   // groups without tiles are skipped
+    const int local = tile - gt.tile_off[grp];
+    const int m_tiles = (gt.tile_off[grp + 1] - gt.tile_off[grp]) / n_tiles;
+    TileCoord t;
+    t.g = grp;
+    t.m0 = gt.row_off[grp] + (local % m_tiles) * BM;
+    t.n0 = (local / m_tiles) * BN;
+    t.row_end = gt.row_off[grp + 1];
+    return t;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs g, const int stages) {
+                   const GemmArgs g, const __grid_constant__ GroupTable gt, const int stages) {
     using Cfg = TnCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -177,9 +204,8 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int num_kb = g.K / BK;
-    const int m_tiles = (g.M + BM - 1) / BM;
     const int n_tiles = (g.N + BN - 1) / BN;
-    const int num_tiles = m_tiles * n_tiles;
+    const int num_tiles = gt.tile_off[gt.num_groups];
     constexpr int PRODUCER = Cfg::EPI_WARPS;
     constexpr int ISSUER = Cfg::EPI_WARPS + 1;
 
@@ -202,8 +228,8 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % m_tiles) * BM;
-                const int n0 = (tile / m_tiles) * BN;
+                const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
+                const int b_row = t.g * g.N + t.n0;      // row of the stacked B
                 for (int kb = 0; kb < num_kb; ++kb) {
                     if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
                         record_error(FP8BS_DEVERR_PRODUCER_WAIT);
@@ -211,8 +237,8 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                         break;
                     }
                     mbar_arrive_expect_tx(&ring.full[stage], Cfg::STAGE);
-                    tma_load_2d(sA + stage * A_TILE, &tmA, &ring.full[stage], kb * BK, m0);
-                    tma_load_2d(sB + stage * Cfg::B_TILE, &tmB, &ring.full[stage], kb * BK, n0);
+                    tma_load_2d(sA + stage * A_TILE, &tmA, &ring.full[stage], kb * BK, t.m0);
+                    tma_load_2d(sB + stage * Cfg::B_TILE, &tmB, &ring.full[stage], kb * BK, b_row);
                     ++issued;
                     if (++stage == stages) {
                         stage = 0;
@@ -270,12 +296,13 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
         uint32_t tphase = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-            const int m0 = (tile % m_tiles) * BM;
-            const int n0 = (tile / m_tiles) * BN;
-            const int row = m0 + row_in_tile;
+            const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
+            const int n0 = t.n0;
+            const int row = t.m0 + row_in_tile;
             const int nb = min((n0 + col0) / 128, nb_count - 1);
             const float* as_row = g.a_s + static_cast<int64_t>(min(row, g.M - 1)) * num_kb;
-            const float* bs_row = g.b_s + static_cast<int64_t>(nb) * num_kb;
+            const float* bs_row =
+                g.b_s + (static_cast<int64_t>(t.g) * nb_count + nb) * num_kb;
             float acc[Cfg::CW];
 #pragma unroll
             for (int i = 0; i < Cfg::CW; ++i) acc[i] = 0.0f;
@@ -316,15 +343,21 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&ring.tempty[buf]);
                     }
+                    // Packed fp32x2 FMAs (round-to-nearest per component): half the issue slots.
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(cur[i], sc, acc[c * 32 + i]);
+                    for (int i = 0; i < 32; i += 2) {
+                        const float2 r = __ffma2_rn(make_float2(cur[i], cur[i + 1]), make_float2(sc, sc),
+                                                    make_float2(acc[c * 32 + i], acc[c * 32 + i + 1]));
+                        acc[c * 32 + i] = r.x;
+                        acc[c * 32 + i + 1] = r.y;
+                    }
                     if (c + 1 < Cfg::CW / 32) tmem_wait_ld_32(nxt);
                 }
                 buf ^= 1;
                 if (buf == 0) tphase ^= 1;
             }
             if (!ok) break;
-            if (row < g.M) {
+            if (row < t.row_end) {
                 __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(g.c) +
                                       static_cast<int64_t>(row) * g.N + n0 + col0;
                 const int valid = min(Cfg::CW, g.N - (n0 + col0));
@@ -353,243 +386,6 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == ISSUER) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
-}
-
-// ================================================================ CTA-pair orientation
-
-// A cluster of two CTAs computes a 256 x BN tile with cta_group::2 MMAs: CTA r (cluster rank r)
-// loads rows 128r .. 128r+127 of the A tile and rows (BN/2)r .. (BN/2)(r+1)-1 of the B tile into
-// its own shared memory, and receives its 128 rows x BN columns of the accumulator in its own
-// TMEM. Per SM this halves the B bytes that TMA writes and the tensor cores read from shared
-// memory per K block (one SM's shared memory cannot feed both at the full MMA rate).
-//   - Both CTAs' TMA loads complete on the even CTA's `full` barrier (it expects both CTAs'
-//     bytes); the even CTA alone issues the MMAs and commits them to the `empty`/`tfull`
-//     barriers of both CTAs at once; both CTAs' promotion warps release a TMEM buffer on the
-//     even CTA's `tempty` barrier.
-//   - Warp layout and register split as in gemm_tn_kernel.
-template <int BN>
-struct PairCfg {
-    static constexpr int EPI_WARPS = BN / 32;
-    static constexpr int CW = 128;
-    static constexpr int THREADS = 32 * EPI_WARPS + 128;
-    static constexpr int B_HALF = (BN / 2) * BK;             // this CTA's half of the B tile
-    static constexpr int STAGE = A_TILE + B_HALF;
-    static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
-    static constexpr bool SPLIT_REGS = (BN == 256);
-    static constexpr uint32_t kCtlRegs = 40;
-    static constexpr uint32_t kEpiRegs = 232;
-    static_assert(!SPLIT_REGS || 4 * 32 * kCtlRegs + 8 * 32 * kEpiRegs <= 384 * 168,
-                  "register split exceeds the launch allocation");
-};
-
-template <int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PairCfg<BN>::THREADS, 1)
-    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                     const __grid_constant__ CUtensorMap tmB, const GemmArgs g,
-                     const int stages) {
-    using Cfg = PairCfg<BN>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = align_1024(smem_raw);
-    uint8_t* sA = smem;
-    uint8_t* sB = smem + stages * A_TILE;
-    const Ring ring = carve_ring(sB + stages * Cfg::B_HALF, stages);
-
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool leader = rank == 0;
-    const int pair = blockIdx.x >> 1;
-    const int num_pairs = gridDim.x >> 1;
-    const int num_kb = g.K / BK;
-    const int m_pairs = (g.M + 2 * BM - 1) / (2 * BM);
-    const int n_tiles = (g.N + BN - 1) / BN;
-    const int num_tiles = m_pairs * n_tiles;
-    constexpr int PRODUCER = Cfg::EPI_WARPS;
-    constexpr int ISSUER = Cfg::EPI_WARPS + 1;
-
-    if (threadIdx.x == 0) {
-        init_ring(ring, stages, 2 * Cfg::EPI_WARPS);   // tempty: promotion warps of both CTAs
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
-    }
-    if (warp == ISSUER) tmem_alloc_pair(ring.tmem_holder, Cfg::TMEM_COLS);
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // both CTAs' barriers are initialised before either signals the other
-    tc_fence_after();
-    const uint32_t tmem_base = *ring.tmem_holder;
-
-    if (warp >= Cfg::EPI_WARPS) {
-        if constexpr (Cfg::SPLIT_REGS) regs_dec<Cfg::kCtlRegs>();
-        if (warp == PRODUCER && lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
-            bool ok = true;
-            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-                // This CTA's rows of A and of B. Where they start past the end of the matrix
-                // (ragged last tiles), load an in-range box instead: the rows it feeds are
-                // never stored, and the byte count the barrier expects stays the same.
-                const int m0 = min((tile % m_pairs) * (2 * BM) + static_cast<int>(rank) * BM,
-                                   g.M - 1);
-                const int nb0 = min((tile / m_pairs) * BN + static_cast<int>(rank) * (BN / 2),
-                                    g.N - 1);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
-                        record_error(FP8BS_DEVERR_PRODUCER_WAIT);
-                        ok = false;
-                        break;
-                    }
-                    if (leader) mbar_arrive_expect_tx(&ring.full[stage], 2 * Cfg::STAGE);
-                    const uint32_t full_leader = peer_smem_addr(&ring.full[stage], 0);
-                    tma_load_2d_pair(sA + stage * A_TILE, &tmA, full_leader, kb * BK, m0);
-                    tma_load_2d_pair(sB + stage * Cfg::B_HALF, &tmB, full_leader, kb * BK, nb0);
-                    ++issued;
-                    if (++stage == stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                }
-            }
-            if (!ok) {
-                if (leader) {
-                    drain_tma(ring, stages, issued);
-                } else {
-                    // Completions of this CTA's copies are counted on the other CTA's barriers;
-                    // give copies still in flight time to land before the CTA can exit.
-                    const uint64_t t0 = global_timer_ns();
-                    while (global_timer_ns() - t0 < 200000ull) {
-                    }
-                }
-            }
-        } else if (warp == ISSUER && lane == 0 && leader) {
-            constexpr uint32_t idesc = idesc_e4m3_f32(2 * BM, BN);
-            int stage = 0, buf = 0;
-            uint32_t phase = 0, tphase = 0;
-            bool ok = true;
-            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
-                        !mbar_wait(&ring.full[stage], phase)) {
-                        record_error(FP8BS_DEVERR_MMA_WAIT);
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t a_addr = smem_addr(sA + stage * A_TILE);
-                    const uint32_t b_addr = smem_addr(sB + stage * Cfg::B_HALF);
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-#pragma unroll
-                    for (int j = 0; j < BK / MMA_K; ++j)
-                        mma_f8_pair(d_tmem, smem_desc_k_sw128(a_addr + j * MMA_K),
-                                    smem_desc_k_sw128(b_addr + j * MMA_K), idesc, j > 0 ? 1u : 0u);
-                    mma_commit_pair(&ring.empty[stage]);
-                    mma_commit_pair(&ring.tfull[buf]);
-                    if (++stage == stages) {
-                        stage = 0;
-                        phase ^= 1;
-                    }
-                    buf ^= 1;
-                    if (buf == 0) tphase ^= 1;
-                }
-            }
-            mma_commit_pair(ring.drain);
-            if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
-        }
-    } else {
-        if constexpr (Cfg::SPLIT_REGS) regs_inc<Cfg::kEpiRegs>();
-        const int quarter = warp & 3;
-        const int col0 = (warp >> 2) * Cfg::CW;
-        const int row_in_tile = quarter * 32 + lane;
-        const int nb_count = (g.N + 127) / 128;
-        const bool vec_scales = (num_kb % 4 == 0) &&
-                                ((reinterpret_cast<uintptr_t>(g.a_s) & 15u) == 0) &&
-                                ((reinterpret_cast<uintptr_t>(g.b_s) & 15u) == 0);
-        int buf = 0;
-        uint32_t tphase = 0;
-        bool ok = true;
-        for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
-            const int m0 = (tile % m_pairs) * (2 * BM) + static_cast<int>(rank) * BM;
-            const int n0 = (tile / m_pairs) * BN;
-            const int row = m0 + row_in_tile;
-            const int nb = min((n0 + col0) / 128, nb_count - 1);
-            const float* as_row = g.a_s + static_cast<int64_t>(min(row, g.M - 1)) * num_kb;
-            const float* bs_row = g.b_s + static_cast<int64_t>(nb) * num_kb;
-            float acc[Cfg::CW];
-#pragma unroll
-            for (int i = 0; i < Cfg::CW; ++i) acc[i] = 0.0f;
-            float4 a_cur = load_scales4(as_row, 0, num_kb, vec_scales);
-            float4 b_cur = load_scales4(bs_row, 0, num_kb, vec_scales);
-            float4 a_nxt = load_scales4(as_row, 4, num_kb, vec_scales);
-            float4 b_nxt = load_scales4(bs_row, 4, num_kb, vec_scales);
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const int j = kb & 3;
-                const float sc = pick4(a_cur, j) * pick4(b_cur, j);
-                if (j == 3) {
-                    a_cur = a_nxt;
-                    b_cur = b_nxt;
-                    a_nxt = load_scales4(as_row, kb + 5, num_kb, vec_scales);
-                    b_nxt = load_scales4(bs_row, kb + 5, num_kb, vec_scales);
-                }
-                if (!warp_wait(&ring.tfull[buf], tphase)) {
-                    if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                       static_cast<uint32_t>(buf * BN + col0);
-                float va[32], vb[32];
-                tmem_ld_32cols(taddr, va);
-                tmem_wait_ld_32(va);
-#pragma unroll
-                for (int c = 0; c < Cfg::CW / 32; ++c) {
-                    float* cur = (c & 1) ? vb : va;
-                    float* nxt = (c & 1) ? va : vb;
-                    if (c + 1 < Cfg::CW / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
-                    if (c + 1 == Cfg::CW / 32) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive_cluster(peer_smem_addr(&ring.tempty[buf], 0));
-                    }
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) acc[c * 32 + i] = fmaf(cur[i], sc, acc[c * 32 + i]);
-                    if (c + 1 < Cfg::CW / 32) tmem_wait_ld_32(nxt);
-                }
-                buf ^= 1;
-                if (buf == 0) tphase ^= 1;
-            }
-            if (!ok) break;
-            if (row < g.M) {
-                __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(g.c) +
-                                      static_cast<int64_t>(row) * g.N + n0 + col0;
-                const int valid = min(Cfg::CW, g.N - (n0 + col0));
-                if ((g.N & 7) == 0) {
-#pragma unroll
-                    for (int jj = 0; jj < Cfg::CW / 8; ++jj) {
-                        if (8 * jj < valid) {
-                            uint4 o;
-                            o.x = pack_bf16x2(acc[8 * jj + 0], acc[8 * jj + 1]);
-                            o.y = pack_bf16x2(acc[8 * jj + 2], acc[8 * jj + 3]);
-                            o.z = pack_bf16x2(acc[8 * jj + 4], acc[8 * jj + 5]);
-                            o.w = pack_bf16x2(acc[8 * jj + 6], acc[8 * jj + 7]);
-                            *reinterpret_cast<uint4*>(crow + 8 * jj) = o;
-                        }
-                    }
-                } else {
-#pragma unroll
-                    for (int jj = 0; jj < Cfg::CW; ++jj)
-                        if (jj < valid) crow[jj] = __float2bfloat16_rn(acc[jj]);
-                }
-            }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();   // no CTA leaves while its pair may still signal or read it
-    tc_fence_after();
-    if (warp == ISSUER) tmem_dealloc_pair(tmem_base, Cfg::TMEM_COLS);
 }
 
 // ================================================================ swapped orientation
@@ -739,10 +535,8 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
                         const float4 a4 = *reinterpret_cast<const float4*>(as_kb + c * 32 + i);
-                        acc[c * 32 + i + 0] = fmaf(cur[i + 0], a4.x, acc[c * 32 + i + 0]);
-                        acc[c * 32 + i + 1] = fmaf(cur[i + 1], a4.y, acc[c * 32 + i + 1]);
-                        acc[c * 32 + i + 2] = fmaf(cur[i + 2], a4.z, acc[c * 32 + i + 2]);
-                        acc[c * 32 + i + 3] = fmaf(cur[i + 3], a4.w, acc[c * 32 + i + 3]);
+                        fma2_into(acc + c * 32 + i, cur[i + 0], cur[i + 1], a4.x, a4.y);
+                        fma2_into(acc + c * 32 + i + 2, cur[i + 2], cur[i + 3], a4.z, a4.w);
                     }
                     if (c + 1 < NCH) tmem_wait_ld_32(nxt);
                 }
@@ -756,10 +550,8 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
                     const float4 a4 = *reinterpret_cast<const float4*>(as_kb + i);
-                    acc[i + 0] = fmaf(v[i + 0], a4.x, acc[i + 0]);
-                    acc[i + 1] = fmaf(v[i + 1], a4.y, acc[i + 1]);
-                    acc[i + 2] = fmaf(v[i + 2], a4.z, acc[i + 2]);
-                    acc[i + 3] = fmaf(v[i + 3], a4.w, acc[i + 3]);
+                    fma2_into(acc + i, v[i + 0], v[i + 1], a4.x, a4.y);
+                    fma2_into(acc + i + 2, v[i + 2], v[i + 3], a4.z, a4.w);
                 }
             }
             buf ^= 1;
@@ -801,31 +593,17 @@ cudaError_t set_smem(K kernel, int bytes) {
 
 template <int BN>
 cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                      int num_sms, cudaStream_t stream) {
+                      const GroupTable& gt, int num_sms, cudaStream_t stream) {
     using Cfg = TnCfg<BN>;
     int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
     const int smem = 1024 + stages * Cfg::STAGE + ring_bytes(stages);
     cudaError_t e = set_smem(gemm_tn_kernel<BN>, smem);
     if (e != cudaSuccess) return e;
-    const int tiles = ((g.M + BM - 1) / BM) * ((g.N + BN - 1) / BN);
+    const int tiles = gt.tile_off[gt.num_groups];
+    if (tiles == 0) return cudaSuccess;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    gemm_tn_kernel<BN><<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, g, stages);
-    return cudaGetLastError();
-}
-
-template <int BN>
-cudaError_t launch_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                        int num_sms, cudaStream_t stream) {
-    using Cfg = PairCfg<BN>;
-    int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
-    if (stages > kMaxStages) stages = kMaxStages;
-    const int smem = 1024 + stages * Cfg::STAGE + ring_bytes(stages);
-    cudaError_t e = set_smem(gemm_pair_kernel<BN>, smem);
-    if (e != cudaSuccess) return e;
-    const int tiles = ((g.M + 2 * BM - 1) / (2 * BM)) * ((g.N + BN - 1) / BN);
-    const int pairs = tiles < num_sms / 2 ? tiles : num_sms / 2;
-    gemm_pair_kernel<BN><<<2 * pairs, Cfg::THREADS, smem, stream>>>(tmA, tmB, g, stages);
+    gemm_tn_kernel<BN><<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, g, gt, stages);
     return cudaGetLastError();
 }
 
@@ -848,18 +626,25 @@ cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const Ge
 
 }  // namespace
 
-cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           int BN, int num_sms, cudaStream_t stream) {
-    switch (BN) {
-        case 128: return launch_tn<128>(tmA, tmB, g, num_sms, stream);
-        case 256: return launch_tn<256>(tmA, tmB, g, num_sms, stream);
-        default: return cudaErrorInvalidValue;
+void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N, int bn) {
+    const int n_tiles = (N + bn - 1) / bn;
+    gt->num_groups = groups;
+    gt->row_off[0] = static_cast<int>(row_off[0]);
+    gt->tile_off[0] = 0;
+    for (int i = 0; i < groups; ++i) {
+        const int rows = static_cast<int>(row_off[i + 1] - row_off[i]);
+        gt->row_off[i + 1] = static_cast<int>(row_off[i + 1]);
+        gt->tile_off[i + 1] = gt->tile_off[i] + ((rows + BM - 1) / BM) * n_tiles;
     }
 }
 
-cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                             int num_sms, cudaStream_t stream) {
-    return launch_pair<256>(tmA, tmB, g, num_sms, stream);
+cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                           const GroupTable& gt, int BN, int num_sms, cudaStream_t stream) {
+    switch (BN) {
+        case 128: return launch_tn<128>(tmA, tmB, g, gt, num_sms, stream);
+        case 256: return launch_tn<256>(tmA, tmB, g, gt, num_sms, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,

@@ -18,21 +18,29 @@ cudaError_t launch_weight_dequant(const void* w, const float* s, void* y, int64_
 // Tensor maps are encoded by the caller (they need the driver entry point).
 struct GemmArgs {
     const float* a_s;   // [M, K/128]
-    const float* b_s;   // [ceil(N/128), K/128]
+    const float* b_s;   // [ceil(N/128), K/128] per group
     void* c;            // bf16 [M, N]
-    int M, N, K;
+    int M, N, K;        // M: all rows (of every group); N, K: per group
 };
 
-// Normal orientation: 128-row tiles of A on the MMA's M side, BN columns of B on its N side.
-// tmA: box {128, 128} over A [M,K]; tmB: box {128, BN} over B [N,K].
-cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           int BN, int num_sms, cudaStream_t stream);
+// Row groups of a grouped GEMM. Group i owns rows row_off[i] .. row_off[i+1]-1 of A, a_s and
+// C, rows i*N .. i*N+N-1 of the stacked B, and scale rows i*ceil(N/128) .. of the stacked b_s.
+// tile_off[i] is the first linear tile of group i (its m tiles times the n tiles of N). A plain
+// GEMM is one group.
+constexpr int kMaxGroups = 256;
+struct GroupTable {
+    int num_groups;
+    int row_off[kMaxGroups + 1];
+    int tile_off[kMaxGroups + 1];
+};
 
-// CTA pairs: 256-row tiles of A x 256 columns of B, computed by two CTAs with cta_group::2.
-// tmA: box {128, 128} over A [M,K]; tmB: box {128, 128} over B [N,K] (each CTA loads half of
-// the tile's 256 rows of B).
-cudaError_t launch_gemm_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                             int num_sms, cudaStream_t stream);
+// Tiles of 128 rows and `bn` columns for the given group row offsets (host-side helper).
+void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N, int bn);
+
+// Normal orientation: 128-row tiles of A on the MMA's M side, BN columns of B on its N side.
+// tmA: box {128, 128} over A [rows, K]; tmB: box {128, BN} over B [groups*N, K].
+cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                           const GroupTable& gt, int BN, int num_sms, cudaStream_t stream);
 
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
 // on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K].

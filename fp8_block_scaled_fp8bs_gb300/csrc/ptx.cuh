@@ -240,82 +240,4 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
            | ((M >> 4) << 24);    // M / 16
 }
 
-// ------------------------------------------------------------------------- CTA pairs
-// A cluster of two CTAs on neighbouring SMs computes one 256-row MMA tile (cta_group::2): the
-// even-ranked CTA issues the MMAs, each CTA holds half of A and half of B in its own shared
-// memory and its 128 rows of the accumulator in its own TMEM.
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Address, in the shared::cluster window, of the same shared-memory offset in CTA `rank`.
-__device__ __forceinline__ uint32_t peer_smem_addr(const void* p, uint32_t rank) {
-    uint32_t d;
-    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(d) : "r"(smem_addr(p)), "r"(rank));
-    return d;
-}
-
-// Every thread of both CTAs: arrive and wait (release / acquire at cluster scope).
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile(
-        "barrier.cluster.arrive.release.aligned;\n\t"
-        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// Arrive on an mbarrier in either CTA of the cluster (address from peer_smem_addr).
-__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
-                 : "memory");
-}
-
-// 2-D tiled load into this CTA's shared memory whose completion is counted on an mbarrier that
-// may live in the peer CTA of the pair (address from peer_smem_addr).
-__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
-                                                 uint32_t bar_cluster_addr, int32_t c0,
-                                                 int32_t c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
-        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
-        : "memory");
-}
-
-// TMEM allocation shared by the pair: one warp in each CTA executes it with the same count.
-__device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(holder)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
-// D (+)= A * B^T over the pair: M = 256 rows (128 per CTA), issued by the even CTA.
-__device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive once on the mbarrier at this shared-memory offset in both CTAs of the pair when every
-// tcgen05 operation issued so far by this thread completes.
-__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %1;" ::"r"(smem_addr(bar)),
-        "h"(static_cast<uint16_t>(0x3))
-        : "memory");
-}
-
 }  // namespace fp8bs

@@ -110,6 +110,28 @@ FP8BS_API int fp8bs_weight_dequant(const void* w, const float* s, void* y, int64
 FP8BS_API int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
                          void* c, int64_t M, int64_t N, int64_t K, int scale_fmt, void* stream);
 
+/*
+ * fp8bs_gemm_grouped -- several independent block-scaled GEMMs in one launch, one per group of
+ * rows of A: the MoE expert loop of "DeepSeek-V3 Administrator & Developer Guide", §6.4 MoE
+ * expert routing (each local expert runs its Linear on the tokens routed to it), with every
+ * expert's GEMM as in §8.5.3.
+ *
+ *   a           [in]  e4m3 [T, K], 16-byte aligned: the rows of all groups, group i's rows
+ *                     row_offsets[i] .. row_offsets[i+1]-1 (tokens gathered by expert).
+ *   a_s         [in]  fp32 [T, K/128], 4-byte aligned.
+ *   b           [in]  e4m3 [groups, N, K] (the experts' weights stacked), 16-byte aligned.
+ *   b_s         [in]  fp32 [groups, ceil(N/128), K/128], 4-byte aligned.
+ *   c           [out] bf16 [T, N], 16-byte aligned: row r of group i is A[r] . B[i]^T.
+ *   row_offsets [in]  HOST array of groups+1 non-decreasing row offsets, row_offsets[0] == 0,
+ *                     T = row_offsets[groups]; empty groups are allowed.
+ *   groups      0 .. 256.  N >= 0, K >= 0 with K % 128 == 0.  scale_fmt as in fp8bs_gemm.
+ *
+ * Results and accuracy are those of fp8bs_gemm on each group's rows.
+ */
+FP8BS_API int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const float* b_s,
+                                 void* c, const int64_t* row_offsets, int64_t groups, int64_t N,
+                                 int64_t K, int scale_fmt, void* stream);
+
 /* Human-readable name of an fp8bs_status value (a static string; never NULL). */
 FP8BS_API const char* fp8bs_status_string(int status);
 

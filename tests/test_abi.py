@@ -108,3 +108,28 @@ def test_product_package_does_not_reference_the_oracle():
             text = open(path).read()
             assert "import oracle" not in text and "oracle." not in text, path
             assert "liboracle" not in text, path
+
+
+def _offs(*v):
+    return (ctypes.c_int64 * len(v))(*v)
+
+
+@pytest.mark.parametrize("offs,groups,N,K,expect", [
+    ((0, 4, 9), 2, 256, 100, INVALID),            # K % 128
+    ((0, 4, 9), 2, -1, 256, INVALID),
+    ((0, 4, 9), 300, 256, 256, INVALID),          # more groups than supported
+    ((1, 4, 9), 2, 256, 256, INVALID),            # offsets must start at 0
+    ((0, 5, 3), 2, 256, 256, INVALID),            # offsets must not decrease
+    ((0, 0, 0), 2, 256, 256, OK),                 # no rows: no-op
+    ((0,), 0, 256, 256, OK),                      # no groups: no-op
+])
+def test_gemm_grouped_argument_checks(lib, offs, groups, N, K, expect):
+    assert lib.fp8bs_gemm_grouped(A16, B16, C16, B16, C16, _offs(*offs), groups, N, K, 0,
+                                  None) == expect
+
+
+def test_gemm_grouped_rejects_misaligned_and_null(lib):
+    o = _offs(0, 3, 8)
+    assert lib.fp8bs_gemm_grouped(A16 + 4, B16, C16, B16, C16, o, 2, 256, 256, 0, None) == MISALIGNED
+    assert lib.fp8bs_gemm_grouped(A16, B16, C16, B16, None, o, 2, 256, 256, 0, None) == INVALID
+    assert lib.fp8bs_gemm_grouped(A16, B16, C16, B16, C16, None, 2, 256, 256, 0, None) == INVALID

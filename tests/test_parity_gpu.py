@@ -150,9 +150,8 @@ def test_gemm_tiny_config():
     (1, 256, 512), (8, 576, 1024), (16, 384, 128), (33, 1000, 640), (64, 1536, 1024),
     (100, 130, 256), (128, 2048, 512),                  # swapped-orientation kernel
     (129, 256, 512), (200, 640, 1024), (300, 576, 384), (256, 2304, 256), (513, 97, 256),
-                                                        # one-CTA kernel, several tiles, tails
     (1200, 4608, 256), (1100, 4736, 256), (1024, 4800, 384), (768, 5120, 1280),
-                                                        # CTA-pair kernel, ragged pair tiles
+                                                        # normal kernel, several tiles, tails
 ])
 def test_gemm_shapes_full_compare(M, N, K):
     x = synth.activations(M, K, seed=M + N + K, name="pgA", outlier_frac=0.01)
@@ -251,6 +250,56 @@ def test_moe_experts_full_size():
         ref = oracle.gemm_at(a_ref, as_ref, b, b_s, np.array([row_of[m] for m in mi]), ni)
         got = host_bf16_f64(outs[e])[mi, ni]
         assert_gemm_close(got, ref, f"expert {e} (M_e={hi - lo})")
+
+
+def grouped_check(counts, N, K, seed, what, per_tile=None):
+    """Grouped GEMM of stacked experts against the oracle, group by group."""
+    counts = np.asarray(counts, dtype=np.int64)
+    offs = np.r_[0, np.cumsum(counts)]
+    T = int(offs[-1])
+    x = synth.activations(max(T, 1), K, seed=seed, name="grpA", outlier_frac=0.01)[:T]
+    a, a_s = oracle.act_quant(x) if T else (np.zeros((0, K), np.uint8), np.zeros((0, K // 128), np.float32))
+    ws = [synth.weights(N, K, seed=seed + 1 + e, name="grpB") for e in range(len(counts))]
+    b = np.stack([w for w, _ in ws])
+    b_s = np.stack([s for _, s in ws])
+    c = fp8bs.fp8_gemm_grouped(dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), offs)
+    torch.cuda.synchronize()
+    c = host_bf16_f64(c)
+    for e in range(len(counts)):
+        lo, hi = offs[e], offs[e + 1]
+        if hi == lo:
+            continue
+        if per_tile is None:
+            ref = oracle.gemm(a[lo:hi], a_s[lo:hi], b[e], b_s[e])
+            assert_gemm_close(c[lo:hi], ref, f"{what} group {e}")
+        else:
+            mi, ni = tile_samples(hi - lo, N, per_tile, seed=e)
+            ref = oracle.gemm_at(a[lo:hi], a_s[lo:hi], b[e], b_s[e], mi, ni)
+            assert_gemm_close(c[lo:hi][mi, ni], ref, f"{what} group {e}")
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([37], 256, 256),                          # one group
+    ([0, 130, 5, 0, 257, 1], 384, 256),        # empty groups, ragged counts, N tail vs BN
+    ([64] * 8, 576, 512),                      # N not a multiple of the tile width
+    ([300, 0, 200], 2048, 256),
+])
+def test_gemm_grouped_against_oracle(counts, N, K):
+    grouped_check(counts, N, K, seed=sum(counts) + N, what=f"grouped {counts}")
+
+
+def test_gemm_grouped_moe_full_size():
+    """The MoE workload (1024 tokens x 8 slots over 32 experts, N=2048, K=7168) in one call."""
+    rows, counts = synth.moe_routing(0)
+    grouped_check(counts, synth.MOE_INTER, synth.DIM, seed=7, what="moe", per_tile=1)
+
+
+def test_gemm_grouped_k_zero_and_no_rows():
+    c = torch.full((6, 16), 2.0, dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8bs_gemm_grouped(0, 0, 0, 0, c.data_ptr(), [0, 2, 6], 2, 16, 0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(c).item() == 0
+    fp8bs.fp8bs_gemm_grouped(0, 0, 0, 0, 0, [0, 0, 0], 2, 16, 128)   # no rows: nothing runs
 
 
 # ------------------------------------------------------------------------------ bounded waits
