@@ -153,8 +153,7 @@ int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
         if (e != cudaErrorInvalidValue) return status_of(e);
         // K too long to stage the activation scales: fall through to the normal kernel.
     }
-    const int64_t tiles256 = ((M + 127) / 128) * ((N + 255) / 256);
-    const int BN = tiles256 >= sms ? 256 : 128;
+    const int BN = fp8bs::pick_tile_n((M + 127) / 128, N, sms);
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
     const int64_t rows[2] = {0, M};
     fp8bs::GroupTable gt;
@@ -197,10 +196,12 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     g.M = static_cast<int>(M);
     g.N = static_cast<int>(N);
     g.K = static_cast<int>(K);
+    int64_t m_tiles_total = 0;
+    for (int64_t i = 0; i < groups; ++i)
+        m_tiles_total += (row_offsets[i + 1] - row_offsets[i] + 127) / 128;
+    const int BN = fp8bs::pick_tile_n(m_tiles_total, N, sms);
     fp8bs::GroupTable gt;
-    fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, 256);
-    const int BN = gt.tile_off[groups] >= sms ? 256 : 128;
-    if (BN != 256) fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, BN);
+    fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, BN);
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
         return FP8BS_ERR_CUDA;

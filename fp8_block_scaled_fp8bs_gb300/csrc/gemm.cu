@@ -135,21 +135,21 @@ __device__ __forceinline__ float pick4(const float4& v, int j) {
     return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
 }
 
-// Tile = 128 rows of A x BN columns of B. Warp layout (whole warpgroups, so that register
-// budgets can be moved between them):
-//   warps 0 .. EPI_WARPS-1   promotion/epilogue, 4 warps per 128 columns (warp w reads TMEM
-//                            lanes 32*(w%4) .. +31, columns 128*(w/4) .. +127 of the tile)
-//   warp EPI_WARPS           TMA producer
-//   warp EPI_WARPS+1         MMA issuer (also allocates and frees TMEM)
-//   warps EPI_WARPS+2, +3    idle (they complete the last warpgroup)
-// With BN = 256 the block has 384 threads and each thread starts with 168 registers; the
-// control warpgroup gives registers back (kCtlRegs) and the promotion warpgroups take them
-// (kEpiRegs). 4*32*kCtlRegs + 8*32*kEpiRegs <= 384*168 keeps the split inside the block's
-// launch allocation, so setmaxnreg.inc never waits.
+// Tile = 128 rows of A x BN columns of B (BN = 64, 128 or 256). Warp layout (whole
+// warpgroups, so that register budgets can be moved between them):
+//   warps 0 .. 7     promotion/epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
+//                    columns (BN/2)*(w/4) .. +BN/2-1 of the tile
+//   warp 8           TMA producer
+//   warp 9           MMA issuer (also allocates and frees TMEM)
+//   warps 10, 11     idle (they complete the last warpgroup)
+// The block has 384 threads, so each thread starts with 168 registers. With BN = 256 (128
+// accumulator columns per thread) the control warpgroup gives registers back (kCtlRegs) and
+// the promotion warpgroups take them (kEpiRegs): 4*32*kCtlRegs + 8*32*kEpiRegs <= 384*168
+// keeps the split inside the block's launch allocation, so setmaxnreg.inc never waits.
 template <int BN>
 struct TnCfg {
-    static constexpr int EPI_WARPS = BN / 32;
-    static constexpr int CW = 128;                            // columns per promotion thread
+    static constexpr int EPI_WARPS = 8;
+    static constexpr int CW = BN / 2;                         // columns per promotion thread
     static constexpr int THREADS = 32 * EPI_WARPS + 128;
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
@@ -626,6 +626,12 @@ cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const Ge
 
 }  // namespace
 
+int pick_tile_n(int64_t m_tiles_total, int64_t N, int num_sms) {
+    if (m_tiles_total * ((N + 255) / 256) >= num_sms) return 256;
+    if (m_tiles_total * ((N + 127) / 128) * 5 >= num_sms * 4) return 128;
+    return 64;
+}
+
 void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N, int bn) {
     const int n_tiles = (N + bn - 1) / bn;
     gt->num_groups = groups;
@@ -641,6 +647,7 @@ void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N,
 cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
                            const GroupTable& gt, int BN, int num_sms, cudaStream_t stream) {
     switch (BN) {
+        case 64: return launch_tn<64>(tmA, tmB, g, gt, num_sms, stream);
         case 128: return launch_tn<128>(tmA, tmB, g, gt, num_sms, stream);
         case 256: return launch_tn<256>(tmA, tmB, g, gt, num_sms, stream);
         default: return cudaErrorInvalidValue;

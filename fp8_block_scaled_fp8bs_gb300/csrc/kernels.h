@@ -37,6 +37,10 @@ struct GroupTable {
 // Tiles of 128 rows and `bn` columns for the given group row offsets (host-side helper).
 void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N, int bn);
 
+// Tile width for the normal orientation: the widest of 256, 128, 64 columns whose tile count
+// still keeps the SMs busy (wider tiles re-read A less often; narrower ones fill more SMs).
+int pick_tile_n(int64_t m_tiles_total, int64_t N, int num_sms);
+
 // Normal orientation: 128-row tiles of A on the MMA's M side, BN columns of B on its N side.
 // tmA: box {128, 128} over A [rows, K]; tmB: box {128, BN} over B [groups*N, K].
 cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,

@@ -151,7 +151,9 @@ def test_gemm_tiny_config():
     (100, 130, 256), (128, 2048, 512),                  # swapped-orientation kernel
     (129, 256, 512), (200, 640, 1024), (300, 576, 384), (256, 2304, 256), (513, 97, 256),
     (1200, 4608, 256), (1100, 4736, 256), (1024, 4800, 384), (768, 5120, 1280),
-                                                        # normal kernel, several tiles, tails
+    (1024, 2048, 256), (2048, 1536, 512), (700, 1000, 256),
+                                                        # normal kernel: 64/128/256-wide tiles,
+                                                        # several tiles, ragged tails
 ])
 def test_gemm_shapes_full_compare(M, N, K):
     x = synth.activations(M, K, seed=M + N + K, name="pgA", outlier_frac=0.01)
