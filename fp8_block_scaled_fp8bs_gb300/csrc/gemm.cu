@@ -411,13 +411,34 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     uint8_t* sX = smem + stages * A_TILE;                 // [stages][MT x 128] activations
     const int num_kb = g.K / BK;
     float* sAs = reinterpret_cast<float*>(sX + stages * Cfg::X_TILE);  // [num_kb][MT]
-    const Ring ring = carve_ring(reinterpret_cast<uint8_t*>(sAs + num_kb * MT), stages);
+    float* sRaw = sAs + num_kb * MT;             // a_s rows m0 .. m0+MT-1 as stored: [MT][num_kb]
+    float* sBs = sRaw + num_kb * MT;             // b_s row of this slab: [num_kb]
+    const Ring ring = carve_ring(reinterpret_cast<uint8_t*>(sBs + ((num_kb + 3) & ~3)), stages);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * BM;
     const int m0 = blockIdx.y * MT;
 
+    // The producer thread initialises the barriers and fills the whole ring before the block
+    // synchronises, so the weight stream starts while TMEM is being allocated.
+    const uint64_t keep = l2_policy_evict_last();    // activations: reused by every CTA
+    const uint64_t stream = l2_policy_evict_first(); // weights: read once
+    const int prefill = min(stages, num_kb);
+    // The scales (a few hundred bytes: rows a_s[m0 .. m0+rows) and the slab's b_s row, both
+    // contiguous) are requested by the promotion threads before the block synchronises, and the
+    // weight stream only starts after it: the scales then return at unloaded latency instead of
+    // queueing behind megabytes of weights.
+    const int scale_rows = min(MT, g.M - m0);
+    const float* as_rows = g.a_s + static_cast<int64_t>(m0) * num_kb;
+    const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+    if (warp >= 2) {
+        const int t = threadIdx.x - 64;
+        for (int i = t; i < scale_rows * num_kb; i += 32 * Cfg::EPI_WARPS)
+            cp_async_4(sRaw + i, as_rows + i);
+        for (int i = t; i < num_kb; i += 32 * Cfg::EPI_WARPS) cp_async_4(sBs + i, bs_row + i);
+        cp_async_commit();
+    }
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
         tma_prefetch_desc(&tmA);
@@ -428,16 +449,22 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
+    if (threadIdx.x == 0) {
+        // fill the whole ring at once
+        for (int kb = 0; kb < prefill; ++kb) {
+            mbar_arrive_expect_tx(&ring.full[kb], Cfg::STAGE);
+            tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
+            tma_load_2d_hint(sX + kb * Cfg::X_TILE, &tmA, &ring.full[kb], kb * BK, m0, keep);
+        }
+    }
 
     if (warp == 0) {
         if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int64_t issued = 0;
+            int stage = prefill % stages;
+            uint32_t phase = prefill == stages ? 1u : 0u;
+            int64_t issued = prefill;
             bool ok = true;
-            const uint64_t keep = l2_policy_evict_last();   // activations: reused by every CTA
-            const uint64_t stream = l2_policy_evict_first(); // weights: read once
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = prefill; kb < num_kb; ++kb) {
                 if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
                     record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                     ok = false;
@@ -490,12 +517,14 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
         // Combined scales a_s[m, kb] * b_s[slab, kb] of this CTA's MT rows, transposed to
         // [kb][m] (zero past row M). Only the promotion warps need them, so the producer and
         // the MMA issuer start streaming while they are staged; reads are coalesced along kb.
-        const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
-        for (int i = threadIdx.x - 64; i < num_kb * MT; i += 32 * Cfg::EPI_WARPS) {
+        // Combined scales sAs[kb][m] = a_s[m0+m, kb] * b_s[slab, kb] (zero past row M), from the
+        // rows copied at kernel start.
+        cp_async_wait_all();
+        asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
+        const int valid = scale_rows * num_kb;
+        for (int i = threadIdx.x - 64; i < MT * num_kb; i += 32 * Cfg::EPI_WARPS) {
             const int j = i / num_kb, kb = i - j * num_kb;
-            sAs[kb * MT + j] = (m0 + j < g.M) ? __ldg(g.a_s + static_cast<int64_t>(m0 + j) * num_kb + kb) *
-                                                     __ldg(bs_row + kb)
-                                               : 0.0f;
+            sAs[kb * MT + j] = i < valid ? sRaw[i] * sBs[kb] : 0.0f;
         }
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         const int quarter = warp & 3;
@@ -612,11 +641,13 @@ cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const Ge
                         cudaStream_t stream) {
     using Cfg = SwapCfg<MT>;
     const int num_kb = g.K / BK;
-    const int fixed = 1024 + num_kb * MT * 4 + ring_bytes(kMaxStages);
+    // scale staging: transposed [num_kb][MT], raw rows [MT][num_kb], b_s row, one barrier
+    const int scale_bytes = 2 * num_kb * MT * 4 + ((num_kb + 3) & ~3) * 4 + 16;
+    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages);
     int stages = (kSmemLimit - fixed) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;   // K too large for the scale staging
-    const int smem = 1024 + stages * Cfg::STAGE + num_kb * MT * 4 + ring_bytes(stages);
+    const int smem = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages);
     cudaError_t e = set_smem(gemm_swapab_kernel<MT>, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((g.N + BM - 1) / BM, (g.M + MT - 1) / MT);
