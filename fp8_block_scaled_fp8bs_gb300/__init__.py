@@ -9,6 +9,7 @@ Raw entry points (same names and arguments as the C functions; pointers are ints
     fp8bs_act_quant(x, y, s, M, K, scale_fmt, stream)
     fp8bs_weight_dequant(w, s, y, N, K, stream)
     fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream)
+    fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, stream)
     fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt, stream)
     fp8bs_device_error(clear=True, stream=0) -> int
     fp8bs_probe_wait_timeout(timeout_ns, stream)
@@ -33,7 +34,9 @@ DEVERR_PROBE = 0x100
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
-EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_grouped",
+GEMM_WEIGHTS_CONSTANT = 0x1
+EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_ex",
+           "fp8bs_gemm_grouped",
            "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
 
 _lock = threading.Lock()
@@ -61,6 +64,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_act_quant.argtypes = [vp, vp, vp, i64, i64, i32, vp]
         lib.fp8bs_weight_dequant.argtypes = [vp, vp, vp, i64, i64, vp]
         lib.fp8bs_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
+        lib.fp8bs_gemm_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint, vp]
         lib.fp8bs_gemm_grouped.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
                                            i64, i64, i64, i32, vp]
         lib.fp8bs_status_string.argtypes = [i32]
@@ -91,6 +95,11 @@ def fp8bs_weight_dequant(w, s, y, N, K, stream=0) -> None:
 
 def fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, stream=0) -> None:
     _check("fp8bs_gemm", load().fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream))
+
+
+def fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0, stream=0) -> None:
+    _check("fp8bs_gemm_ex", load().fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags,
+                                                 stream))
 
 
 def fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt=SCALE_FP32,
@@ -160,7 +169,7 @@ def weight_dequant(w, s):
     return y
 
 
-def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None):
+def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False):
     """C[M,N] bf16 = A[M,K] . B[N,K]^T with per-128-K-block scales a_s [M,K/128] and
     b_s [ceil(N/128), K/128]."""
     import torch
@@ -174,8 +183,9 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None):
             tuple(b_s.shape) != (-(-N // BLOCK), K // BLOCK):
         raise ValueError("operand or scale shapes do not match")
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
-    fp8bs_gemm(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
-               M, N, K, _fmt(scale_fmt), _stream())
+    fp8bs_gemm_ex(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
+                  M, N, K, _fmt(scale_fmt), GEMM_WEIGHTS_CONSTANT if weights_constant else 0,
+                  _stream())
     return c
 
 

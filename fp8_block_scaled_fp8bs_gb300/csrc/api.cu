@@ -116,6 +116,13 @@ int fp8bs_weight_dequant(const void* w, const float* s, void* y, int64_t N, int6
 
 int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
                int64_t M, int64_t N, int64_t K, int scale_fmt, void* stream) {
+    return fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt, 0u, stream);
+}
+
+int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
+                  int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
+                  void* stream) {
+    if ((flags & ~FP8BS_GEMM_WEIGHTS_CONSTANT) != 0) return FP8BS_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
     if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
         return FP8BS_ERR_INVALID_ARG;
@@ -143,6 +150,7 @@ int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
     g.M = static_cast<int>(M);
     g.N = static_cast<int>(N);
     g.K = static_cast<int>(K);
+    g.weights_constant = (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0;
 
     CUtensorMap tmA, tmB;
     if (M <= 128) {
@@ -196,6 +204,7 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     g.M = static_cast<int>(M);
     g.N = static_cast<int>(N);
     g.K = static_cast<int>(K);
+    g.weights_constant = 0;
     int64_t m_tiles_total = 0;
     for (int64_t i = 0; i < groups; ++i)
         m_tiles_total += (row_offsets[i + 1] - row_offsets[i] + 127) / 128;

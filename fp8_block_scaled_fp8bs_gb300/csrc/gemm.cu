@@ -209,6 +209,8 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     constexpr int PRODUCER = Cfg::EPI_WARPS;
     constexpr int ISSUER = Cfg::EPI_WARPS + 1;
 
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
         tma_prefetch_desc(&tmA);
@@ -420,8 +422,8 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     const int n0 = blockIdx.x * BM;
     const int m0 = blockIdx.y * MT;
 
-    // The producer thread initialises the barriers and fills the whole ring before the block
-    // synchronises, so the weight stream starts while TMEM is being allocated.
+    // Prologue order: barriers; (weights declared constant: the whole weight ring, before
+    // waiting for earlier kernels); wait; scales; TMEM; block sync; activations (and weights).
     const uint64_t keep = l2_policy_evict_last();    // activations: reused by every CTA
     const uint64_t stream = l2_policy_evict_first(); // weights: read once
     const int prefill = min(stages, num_kb);
@@ -432,17 +434,27 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     const int scale_rows = min(MT, g.M - m0);
     const float* as_rows = g.a_s + static_cast<int64_t>(m0) * num_kb;
     const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+    if (threadIdx.x == 0) {
+        init_ring(ring, stages, Cfg::EPI_WARPS);
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        // Weights the caller declared constant need not wait for the kernels before this one:
+        // the ring starts filling while they finish.
+        if (g.weights_constant) {
+            for (int kb = 0; kb < prefill; ++kb) {
+                mbar_arrive_expect_tx(&ring.full[kb], Cfg::STAGE);
+                tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
+            }
+        }
+    }
+    grid_dependency_wait();
+    grid_launch_dependents();
     if (warp >= 2) {
         const int t = threadIdx.x - 64;
         for (int i = t; i < scale_rows * num_kb; i += 32 * Cfg::EPI_WARPS)
             cp_async_4(sRaw + i, as_rows + i);
         for (int i = t; i < num_kb; i += 32 * Cfg::EPI_WARPS) cp_async_4(sBs + i, bs_row + i);
         cp_async_commit();
-    }
-    if (threadIdx.x == 0) {
-        init_ring(ring, stages, Cfg::EPI_WARPS);
-        tma_prefetch_desc(&tmA);
-        tma_prefetch_desc(&tmB);
     }
     if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
     tc_fence_before();
@@ -452,8 +464,10 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     if (threadIdx.x == 0) {
         // fill the whole ring at once
         for (int kb = 0; kb < prefill; ++kb) {
-            mbar_arrive_expect_tx(&ring.full[kb], Cfg::STAGE);
-            tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
+            if (!g.weights_constant) {
+                mbar_arrive_expect_tx(&ring.full[kb], Cfg::STAGE);
+                tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
+            }
             tma_load_2d_hint(sX + kb * Cfg::X_TILE, &tmA, &ring.full[kb], kb * BK, m0, keep);
         }
     }
@@ -632,8 +646,8 @@ cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
     const int grid = tiles < num_sms ? tiles : num_sms;
-    gemm_tn_kernel<BN><<<grid, Cfg::THREADS, smem, stream>>>(tmA, tmB, g, gt, stages);
-    return cudaGetLastError();
+    return launch_pdl(gemm_tn_kernel<BN>, grid, Cfg::THREADS, smem, stream, tmA, tmB, g, gt,
+                      stages);
 }
 
 template <int MT>
@@ -651,8 +665,8 @@ cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const Ge
     cudaError_t e = set_smem(gemm_swapab_kernel<MT>, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((g.N + BM - 1) / BM, (g.M + MT - 1) / MT);
-    gemm_swapab_kernel<MT><<<grid, Cfg::THREADS, smem, stream>>>(tmB, tmA, g, stages);
-    return cudaGetLastError();
+    return launch_pdl(gemm_swapab_kernel<MT>, grid, Cfg::THREADS, smem, stream, tmB, tmA, g,
+                      stages);
 }
 
 }  // namespace

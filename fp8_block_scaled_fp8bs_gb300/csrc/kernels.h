@@ -9,6 +9,24 @@
 
 namespace fp8bs {
 
+// Launch with programmatic stream serialisation (see grid_dependency_wait in ptx.cuh): the
+// launch may begin while the previous kernel on the stream is finishing.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_act_quant(const void* x, void* y, float* s, int64_t M, int64_t K, bool ue8m0,
                              int num_sms, cudaStream_t stream);
 
@@ -21,6 +39,7 @@ struct GemmArgs {
     const float* b_s;   // [ceil(N/128), K/128] per group
     void* c;            // bf16 [M, N]
     int M, N, K;        // M: all rows (of every group); N, K: per group
+    int weights_constant;  // B and b_s may be read before earlier kernels on the stream finish
 };
 
 // Row groups of a grouped GEMM. Group i owns rows row_off[i] .. row_off[i+1]-1 of A, a_s and

@@ -25,6 +25,19 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 
 __device__ __forceinline__ uint32_t lane_id() { return threadIdx.x & 31u; }
 
+// ------------------------------------------------------------------------- grid dependencies
+// Kernels of this library are launched with programmatic stream serialisation: the next kernel
+// on the stream may start once every CTA of the current one has called launch_dependents, and
+// must call wait before it touches memory written by kernels enqueued before it.
+
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------- mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

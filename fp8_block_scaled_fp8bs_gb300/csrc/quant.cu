@@ -9,6 +9,7 @@
 #include <cuda_fp8.h>
 
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace fp8bs {
 
@@ -45,6 +46,8 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict_
                                                         uint4* __restrict__ y,
                                                         float* __restrict__ s,
                                                         int64_t num_groups) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     // Every lane of a warp runs the same number of iterations (num_groups is a multiple of 8
     // and the grid covers whole warps), so the shuffles below are always full-warp.
@@ -100,6 +103,8 @@ __global__ void __launch_bounds__(256) weight_dequant_vec_kernel(const uint4* __
                                                                  const float* __restrict__ s,
                                                                  uint4* __restrict__ y,
                                                                  int64_t N, int64_t K) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t groups_per_row = K >> 4;
     const int64_t kblocks = (K + 127) >> 7;
     const int64_t total = N * groups_per_row;
@@ -134,6 +139,8 @@ __global__ void __launch_bounds__(256) weight_dequant_vec_kernel(const uint4* __
 __global__ void __launch_bounds__(256) weight_dequant_scalar_kernel(
     const uint8_t* __restrict__ w, const float* __restrict__ s, __nv_bfloat16* __restrict__ y,
     int64_t N, int64_t K) {
+    grid_dependency_wait();
+    grid_launch_dependents();
     const int64_t kblocks = (K + 127) >> 7;
     const int64_t total = N * K;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
@@ -159,13 +166,10 @@ cudaError_t launch_act_quant(const void* x, void* y, float* s, int64_t M, int64_
                              int num_sms, cudaStream_t stream) {
     const int64_t groups = M * K / 16;
     const int grid = grid_for(groups, num_sms);
-    if (ue8m0)
-        act_quant_kernel<true><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x),
-                                                         static_cast<uint4*>(y), s, groups);
-    else
-        act_quant_kernel<false><<<grid, 256, 0, stream>>>(static_cast<const uint4*>(x),
-                                                          static_cast<uint4*>(y), s, groups);
-    return cudaGetLastError();
+    const uint4* xv = static_cast<const uint4*>(x);
+    uint4* yv = static_cast<uint4*>(y);
+    if (ue8m0) return launch_pdl(act_quant_kernel<true>, grid, 256, 0, stream, xv, yv, s, groups);
+    return launch_pdl(act_quant_kernel<false>, grid, 256, 0, stream, xv, yv, s, groups);
 }
 
 cudaError_t launch_weight_dequant(const void* w, const float* s, void* y, int64_t N, int64_t K,
@@ -175,14 +179,11 @@ cudaError_t launch_weight_dequant(const void* w, const float* s, void* y, int64_
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const bool vec = (K % 16 == 0) && (reinterpret_cast<uintptr_t>(w) % 16 == 0) &&
                      (reinterpret_cast<uintptr_t>(y) % 16 == 0);
-    if (vec) {
-        weight_dequant_vec_kernel<<<grid_for(N * K / 16, sms), 256, 0, stream>>>(
-            static_cast<const uint4*>(w), s, static_cast<uint4*>(y), N, K);
-    } else {
-        weight_dequant_scalar_kernel<<<grid_for(N * K, sms), 256, 0, stream>>>(
-            static_cast<const uint8_t*>(w), s, static_cast<__nv_bfloat16*>(y), N, K);
-    }
-    return cudaGetLastError();
+    if (vec)
+        return launch_pdl(weight_dequant_vec_kernel, grid_for(N * K / 16, sms), 256, 0, stream,
+                          static_cast<const uint4*>(w), s, static_cast<uint4*>(y), N, K);
+    return launch_pdl(weight_dequant_scalar_kernel, grid_for(N * K, sms), 256, 0, stream,
+                      static_cast<const uint8_t*>(w), s, static_cast<__nv_bfloat16*>(y), N, K);
 }
 
 }  // namespace fp8bs

@@ -111,6 +111,24 @@ FP8BS_API int fp8bs_gemm(const void* a, const float* a_s, const void* b, const f
                          void* c, int64_t M, int64_t N, int64_t K, int scale_fmt, void* stream);
 
 /*
+ * fp8bs_gemm_ex -- fp8bs_gemm with flags (fp8bs_gemm is fp8bs_gemm_ex with flags == 0).
+ *
+ *   flags: 0 or FP8BS_GEMM_WEIGHTS_CONSTANT. With FP8BS_GEMM_WEIGHTS_CONSTANT the caller
+ *   promises that b and b_s are not written by any work enqueued earlier on `stream` (model
+ *   weights during inference): the kernel may then start reading them before the kernel
+ *   ahead of it on the stream has finished (the act_quant that produces `a`, typically),
+ *   which hides the start of the weight stream behind it. Unknown flag bits are rejected.
+ *
+ * Every kernel of this library is launched with programmatic stream serialisation: it may
+ * begin while the kernel before it finishes, and waits for that kernel before reading anything
+ * it could have written (all inputs, or all but b and b_s with the flag above).
+ */
+#define FP8BS_GEMM_WEIGHTS_CONSTANT 0x1u
+FP8BS_API int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b_s,
+                            void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                            unsigned int flags, void* stream);
+
+/*
  * fp8bs_gemm_grouped -- several independent block-scaled GEMMs in one launch, one per group of
  * rows of A: the MoE expert loop of "DeepSeek-V3 Administrator & Developer Guide", §6.4 MoE
  * expert routing (each local expert runs its Linear on the tokens routed to it), with every

@@ -133,3 +133,8 @@ def test_gemm_grouped_rejects_misaligned_and_null(lib):
     assert lib.fp8bs_gemm_grouped(A16 + 4, B16, C16, B16, C16, o, 2, 256, 256, 0, None) == MISALIGNED
     assert lib.fp8bs_gemm_grouped(A16, B16, C16, B16, None, o, 2, 256, 256, 0, None) == INVALID
     assert lib.fp8bs_gemm_grouped(A16, B16, C16, B16, C16, None, 2, 256, 256, 0, None) == INVALID
+
+
+def test_gemm_ex_rejects_unknown_flags(lib):
+    assert lib.fp8bs_gemm_ex(A16, B16, C16, B16, C16, 8, 256, 256, 0, 0x2, None) == INVALID
+    assert lib.fp8bs_gemm_ex(None, None, None, None, None, 0, 256, 256, 0, 0x1, None) == OK

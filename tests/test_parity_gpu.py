@@ -182,14 +182,16 @@ def test_gemm_deterministic():
     assert np.array_equal(c1, c2)
 
 
-def pipeline_check(x_bits, b, b_s, fmt, what, per_tile=2):
+def pipeline_check(x_bits, b, b_s, fmt, what, per_tile=2, weights_constant=False):
     """The whole path on the GPU (act_quant then fp8_gemm, as the benchmark runs it); the
     oracle recomputes act_quant on the sampled rows from the same bf16 input, checks those rows
     bit-exactly, and evaluates the GEMM at sampled positions from its own codes."""
     M, K = x_bits.shape
     N = b.shape[0]
-    y, s = fp8bs.act_quant(dev_bf16(x_bits), fmt)
-    c = fp8bs.fp8_gemm(y, s, dev_e4m3(b), dev_f32(b_s), fmt)
+    bt, bst, xt = dev_e4m3(b), dev_f32(b_s), dev_bf16(x_bits)
+    torch.cuda.synchronize()
+    y, s = fp8bs.act_quant(xt, fmt)          # the GEMM may start while this one finishes
+    c = fp8bs.fp8_gemm(y, s, bt, bst, fmt, weights_constant=weights_constant)
     torch.cuda.synchronize()
     mi, ni = tile_samples(M, N, per_tile, seed=M + N)
     rows = np.unique(mi)
@@ -203,10 +205,39 @@ def pipeline_check(x_bits, b, b_s, fmt, what, per_tile=2):
     return assert_gemm_close(got, ref, what)
 
 
+@pytest.mark.parametrize("weights_constant", [False, True])
 @pytest.mark.parametrize("M", synth.DECODE_MS)
-def test_pipeline_decode_full_size(M):
+def test_pipeline_decode_full_size(M, weights_constant):
     b, b_s = synth.weights(synth.INTER, synth.DIM, seed=0, name="decode/B")
-    pipeline_check(synth.decode(M), b, b_s, "fp32", f"decode M={M}", per_tile=4)
+    pipeline_check(synth.decode(M), b, b_s, "fp32", f"decode M={M}", per_tile=4,
+                   weights_constant=weights_constant)
+
+
+def test_back_to_back_layers_share_buffers():
+    """Several act_quant -> GEMM pairs on one stream reusing the same activation and output
+    buffers, as consecutive layers do: each kernel may start while the previous one finishes,
+    and must still see its inputs complete."""
+    K, N, M = synth.DIM, 2048, 32
+    ws = [synth.weights(N, K, seed=40 + i, name="layers/B") for i in range(3)]
+    xs = [synth.activations(M, K, seed=50 + i, name="layers/A") for i in range(3)]
+    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
+    s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+    c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    outs = []
+    dev_w = [(dev_e4m3(b), dev_f32(bs)) for b, bs in ws]
+    dev_x = [dev_bf16(x) for x in xs]
+    torch.cuda.synchronize()
+    st = torch.cuda.current_stream().cuda_stream
+    for i in range(3):
+        fp8bs.fp8bs_act_quant(dev_x[i].data_ptr(), y.data_ptr(), s.data_ptr(), M, K, 0, st)
+        fp8bs.fp8bs_gemm_ex(y.data_ptr(), s.data_ptr(), dev_w[i][0].data_ptr(),
+                            dev_w[i][1].data_ptr(), c.data_ptr(), M, N, K, 0,
+                            fp8bs.GEMM_WEIGHTS_CONSTANT, st)
+        outs.append(c.clone())
+    torch.cuda.synchronize()
+    for i in range(3):
+        a_ref, as_ref = oracle.act_quant(xs[i])
+        assert_gemm_close(host_bf16_f64(outs[i]), oracle.gemm(a_ref, as_ref, *ws[i]), f"layer {i}")
 
 
 @pytest.mark.parametrize("which", ["up", "down"])
