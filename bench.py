@@ -522,6 +522,20 @@ def run_profile(case: str, launches: int, warmup: int):
         y = torch.empty((8192, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
         s = torch.empty((8192, K_DIM // 128), dtype=torch.float32, device="cuda")
         fn = lambda: g.act_quant(x, y, s, 8192, K_DIM)  # noqa: E731
+    elif case == "moe":
+        rows, counts = synth.moe_routing(0)
+        x = g.bf16(synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows])
+        y = torch.empty((8192, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((8192, K_DIM // 128), dtype=torch.float32, device="cuda")
+        g.act_quant(x, y, s, 8192, K_DIM)
+        ws = [synth.weights(synth.MOE_INTER, K_DIM, 0, f"moe/B{e}") for e in range(32)]
+        B = g.e4m3(np.stack([w for w, _ in ws]))
+        S = g.f32(np.stack([sc for _, sc in ws]))
+        c = torch.empty((8192, synth.MOE_INTER), dtype=torch.bfloat16, device="cuda")
+        offs = [int(v) for v in np.r_[0, np.cumsum(counts)]]
+        fn = lambda: g.fp8bs.fp8bs_gemm_grouped(  # noqa: E731
+            y.data_ptr(), s.data_ptr(), B.data_ptr(), S.data_ptr(), c.data_ptr(), offs, 32,
+            synth.MOE_INTER, K_DIM, 0, g.sh)
     elif case == "dequant":
         b, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up")
         W, WS = g.e4m3(b), g.f32(bs)
@@ -583,7 +597,7 @@ def main(argv=None):
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
     ap.add_argument("--profile", metavar="CASE", default=None,
                     help="run one kernel only (decode1..decode64, prefill_up, prefill_down, "
-                         "act_quant, dequant): warmup + steps launches, for ncu")
+                         "act_quant, dequant, moe): warmup + steps launches, for ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be at least 3")
