@@ -43,6 +43,12 @@ DECODE_MS = synth.DECODE_MS
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the decode GEMM,
+# from the ncu captures summarised in profiles/gemm_swapab_decode.md (M=1: 135.21 MB,
+# M=64: 135.60 MB), valid only for the gemm.cu they were taken on (first 16 hex digits of its
+# SHA-256); for any other source the bench reports traffic as null.
+DECODE_TRAFFIC_MB = {"gemm_sha": "3309e353991b32ab", "per_launch_mb": (135.21 + 135.60) / 2}
+
 
 # ----------------------------------------------------------------------------- accounting
 
@@ -66,6 +72,20 @@ def gemm_flops(M, N, K):
 
 def decode_step_bytes():
     return sum(act_quant_bytes(M, K_DIM) + gemm_bytes(M, N_DIM, K_DIM) for M in DECODE_MS)
+
+
+def decode_traffic():
+    """Measured DRAM bytes per decode-GEMM launch (MB), if the kernel source is unchanged."""
+    import hashlib
+    path = os.path.join(ROOT, "fp8_block_scaled_fp8bs_gb300", "csrc", "gemm.cu")
+    try:
+        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    except OSError:
+        return None
+    if sha != DECODE_TRAFFIC_MB["gemm_sha"]:
+        return None
+    return {"value": round(DECODE_TRAFFIC_MB["per_launch_mb"], 2), "unit": "MB per launch",
+            "source": "profiles/gemm_swapab_decode.md"}
 
 
 def load_peaks():
@@ -634,7 +654,7 @@ def main(argv=None):
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
-                "traffic": None,
+                "traffic": decode_traffic(),
                 "per_launch": [{"M": M, "us": round(d * 1e3, 2),
                                 "GB/s": round(gemm_bytes(M, N_DIM, K_DIM) / (d * 1e6), 1)}
                                for M, d in per_m]}
