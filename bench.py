@@ -75,7 +75,7 @@ def decode_step_bytes():
 
 
 def decode_traffic():
-    """Measured DRAM bytes per decode-GEMM launch (MB), if the kernel source is unchanged."""
+    """Measured DRAM bytes per decode-GEMM launch, if the kernel source is unchanged."""
     import hashlib
     path = os.path.join(ROOT, "fp8_block_scaled_fp8bs_gb300", "csrc", "gemm.cu")
     try:
@@ -84,8 +84,7 @@ def decode_traffic():
         return None
     if sha != DECODE_TRAFFIC_MB["gemm_sha"]:
         return None
-    return {"value": round(DECODE_TRAFFIC_MB["per_launch_mb"], 2), "unit": "MB per launch",
-            "source": "profiles/gemm_swapab_decode.md"}
+    return round(DECODE_TRAFFIC_MB["per_launch_mb"] * 1e6)
 
 
 def load_peaks():
@@ -655,6 +654,8 @@ def main(argv=None):
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "traffic": decode_traffic(),
+                "traffic_note": "dram read+write bytes per launch, ncu "
+                                "(profiles/gemm_swapab_decode.md); null if gemm.cu changed",
                 "per_launch": [{"M": M, "us": round(d * 1e3, 2),
                                 "GB/s": round(gemm_bytes(M, N_DIM, K_DIM) / (d * 1e6), 1)}
                                for M, d in per_m]}
