@@ -30,6 +30,7 @@ SCALE_FP32 = 0
 SCALE_UE8M0 = 1
 STATUS = {0: "ok", 1: "invalid argument", 2: "pointer not aligned",
           3: "unsupported device (needs sm_103)", 4: "CUDA error"}
+DEVERR_SCALE_NOT_POW2 = 0x10
 DEVERR_PROBE = 0x100
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -161,11 +161,14 @@ int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b
         if (e != cudaErrorInvalidValue) return status_of(e);
         // K too long to stage the activation scales: fall through to the normal kernel.
     }
-    const int BN = fp8bs::pick_tile_n((M + 127) / 128, N, sms);
+    const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
+    const int BN = block_scaled ? fp8bs::pick_tile_n_bs((M + 127) / 128, N, sms)
+                                : fp8bs::pick_tile_n((M + 127) / 128, N, sms);
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
     const int64_t rows[2] = {0, M};
     fp8bs::GroupTable gt;
     fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), BN);
+    if (block_scaled) return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, st));
     return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
 }
 
@@ -208,12 +211,15 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     int64_t m_tiles_total = 0;
     for (int64_t i = 0; i < groups; ++i)
         m_tiles_total += (row_offsets[i + 1] - row_offsets[i] + 127) / 128;
-    const int BN = fp8bs::pick_tile_n(m_tiles_total, N, sms);
+    const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
+    const int BN = block_scaled ? fp8bs::pick_tile_n_bs(m_tiles_total, N, sms)
+                                : fp8bs::pick_tile_n(m_tiles_total, N, sms);
     fp8bs::GroupTable gt;
     fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, BN);
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
         return FP8BS_ERR_CUDA;
+    if (block_scaled) return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, st));
     return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
 }
 

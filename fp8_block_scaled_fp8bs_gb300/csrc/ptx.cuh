@@ -179,6 +179,44 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with ue8m0 scale factors read from TMEM, one per 32
+// elements of K per row of A and per row of B (kind::mxf8f6f4, scale_vec::1X); one thread issues.
+__device__ __forceinline__ void mma_f8_block_scaled(uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                    uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor for kind::mxf8f6f4 with block scaling: D = fp32, A = B = e4m3, both
+// K-major, ue8m0 scale factors (scale-factor byte selectors left at 0), shape M x N.
+__host__ __device__ constexpr uint32_t idesc_e4m3_block_scaled(uint32_t M, uint32_t N) {
+    return (0u << 7)              // A format: e4m3
+           | (0u << 10)           // B format: e4m3
+           | ((N >> 3) << 17)     // N / 8
+           | (1u << 23)           // scale factor format: ue8m0
+           | ((M >> 4) << 24);    // M / 16
+}
+
+// Write four 32-bit words to TMEM columns col .. col+3 of the warp's 32 lanes (thread t of the
+// warp writes lane lane_base + t).
+__device__ __forceinline__ void tmem_st_4cols(uint32_t taddr, uint32_t w0, uint32_t w1, uint32_t w2,
+                                              uint32_t w3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+                 "r"(w0), "r"(w1), "r"(w2), "r"(w3)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() {
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Arrive (once) on `bar` when every tcgen05 operation issued so far by this thread completes.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile(

@@ -99,8 +99,12 @@ FP8BS_API int fp8bs_weight_dequant(const void* w, const float* s, void* y, int64
  *   b_s  [in]  fp32 [ceil(N/128), K/128], 4-byte aligned (per 128x128 block of b).
  *   c    [out] bf16 [M, N], 16-byte aligned.
  *   M >= 0, N >= 0, K >= 0 with K % 128 == 0.
- *   scale_fmt: FP8BS_SCALE_FP32 or FP8BS_SCALE_UE8M0; a hint about the scale values only
- *   (both are read as fp32).
+ *   scale_fmt: FP8BS_SCALE_FP32: a_s and b_s are any positive finite fp32 values.
+ *              FP8BS_SCALE_UE8M0: the caller promises that every a_s and b_s value is a power
+ *              of two 2^e with -126 <= e <= 127 (the V3.1 ue8m0 scales; act_quant with
+ *              FP8BS_SCALE_UE8M0 produces such a_s). For M > 128 the tensor cores then apply
+ *              the scales themselves (block-scaled MMA with ue8m0 scale factors). A scale that
+ *              breaks the promise sets FP8BS_DEVERR_SCALE_NOT_POW2 and makes C undefined.
  *
  * C[m, n] = sum_kb a_s[m, kb] * b_s[n/128, kb] * sum_{k in block kb} a[m, k] * b[n, k]:
  * each block's partial product is formed on the tensor cores in fp32, scaled and accumulated
@@ -142,7 +146,8 @@ FP8BS_API int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, cons
  *   c           [out] bf16 [T, N], 16-byte aligned: row r of group i is A[r] . B[i]^T.
  *   row_offsets [in]  HOST array of groups+1 non-decreasing row offsets, row_offsets[0] == 0,
  *                     T = row_offsets[groups]; empty groups are allowed.
- *   groups      0 .. 256.  N >= 0, K >= 0 with K % 128 == 0.  scale_fmt as in fp8bs_gemm.
+ *   groups      0 .. 256.  N >= 0, K >= 0 with K % 128 == 0.  scale_fmt as in fp8bs_gemm
+ *               (with FP8BS_SCALE_UE8M0 every group runs on the block-scaled MMA).
  *
  * Results and accuracy are those of fp8bs_gemm on each group's rows.
  */
@@ -166,6 +171,7 @@ FP8BS_API int fp8bs_device_error(unsigned int* out, int clear, void* stream);
 #define FP8BS_DEVERR_MMA_WAIT 0x2u       /* MMA issuer waited too long for data or TMEM */
 #define FP8BS_DEVERR_EPILOGUE_WAIT 0x4u  /* promotion/epilogue waited too long for TMEM */
 #define FP8BS_DEVERR_DRAIN_WAIT 0x8u     /* in-flight copies did not drain after an abort */
+#define FP8BS_DEVERR_SCALE_NOT_POW2 0x10u /* FP8BS_SCALE_UE8M0 GEMM met a scale that is not 2^e */
 #define FP8BS_DEVERR_PROBE 0x100u        /* set by fp8bs_probe_wait_timeout */
 
 /*

@@ -285,17 +285,20 @@ def test_moe_experts_full_size():
         assert_gemm_close(got, ref, f"expert {e} (M_e={hi - lo})")
 
 
-def grouped_check(counts, N, K, seed, what, per_tile=None):
-    """Grouped GEMM of stacked experts against the oracle, group by group."""
+def grouped_check(counts, N, K, seed, what, per_tile=None, fmt="fp32"):
+    """Grouped GEMM of stacked experts against the oracle, group by group. With fmt="ue8m0"
+    every scale is a power of two (act_quant's ue8m0 scales, 2^e weight scales)."""
     counts = np.asarray(counts, dtype=np.int64)
     offs = np.r_[0, np.cumsum(counts)]
     T = int(offs[-1])
     x = synth.activations(max(T, 1), K, seed=seed, name="grpA", outlier_frac=0.01)[:T]
-    a, a_s = oracle.act_quant(x) if T else (np.zeros((0, K), np.uint8), np.zeros((0, K // 128), np.float32))
-    ws = [synth.weights(N, K, seed=seed + 1 + e, name="grpB") for e in range(len(counts))]
+    a, a_s = oracle.act_quant(x, FMTS[fmt]) if T else \
+        (np.zeros((0, K), np.uint8), np.zeros((0, K // 128), np.float32))
+    ws = [synth.weights(N, K, seed=seed + 1 + e, name="grpB", pow2=fmt == "ue8m0")
+          for e in range(len(counts))]
     b = np.stack([w for w, _ in ws])
     b_s = np.stack([s for _, s in ws])
-    c = fp8bs.fp8_gemm_grouped(dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), offs)
+    c = fp8bs.fp8_gemm_grouped(dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), offs, fmt)
     torch.cuda.synchronize()
     c = host_bf16_f64(c)
     for e in range(len(counts)):
@@ -333,6 +336,84 @@ def test_gemm_grouped_k_zero_and_no_rows():
     torch.cuda.synchronize()
     assert torch.count_nonzero(c).item() == 0
     fp8bs.fp8bs_gemm_grouped(0, 0, 0, 0, 0, [0, 0, 0], 2, 16, 128)   # no rows: nothing runs
+
+
+# ------------------------------------------------------------------------------ ue8m0 block-scaled MMA
+# With FP8BS_SCALE_UE8M0 and more than 128 rows the tensor cores apply the power-of-two scales
+# themselves (block-scaled MMA); the oracle is the same fp64 GEMM on the same codes and scales.
+
+def pow2_case(M, N, K, seed):
+    x = synth.activations(M, K, seed=seed, name="bsA", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x, oracle.SCALE_UE8M0)
+    b, b_s = synth.weights(N, K, seed=seed + 1, name="bsB", pow2=True)
+    return a, a_s, b, b_s
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (64, 1536, 1024),                                   # few rows: swapped kernel, ue8m0 scales
+    (129, 256, 512), (200, 640, 1024), (300, 576, 384), (513, 97, 256), (1024, 2048, 256),
+    (2048, 1536, 512), (700, 1000, 256), (1100, 4736, 256), (256, 128, 7168), (384, 200, 2048),
+])
+def test_gemm_ue8m0_block_scaled_full_compare(M, N, K):
+    a, a_s, b, b_s = pow2_case(M, N, K, M + N + K)
+    assert_gemm_close(run_gemm(a, a_s, b, b_s, "ue8m0"), oracle.gemm(a, a_s, b, b_s),
+                      f"ue8m0 {M}x{N}x{K}")
+
+
+def random_codes(rng, rows, cols):
+    c = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x00                        # no NaN codes
+    return c
+
+
+def test_gemm_ue8m0_per_row_and_block_exponents():
+    """Every row of A and every 128-row block of B carries its own exponent in every K block,
+    so a scale factor taken from the wrong row, column block, K block or pipeline stage moves
+    whole output regions out of tolerance."""
+    M, N, K = 384, 384, 1152
+    rng = np.random.default_rng(11)
+    a, b = random_codes(rng, M, K), random_codes(rng, N, K)
+    m = np.arange(M)[:, None]
+    kb = np.arange(K // 128)[None, :]
+    a_s = np.ldexp(1.0, ((m * 7 + kb * 3) % 9) - 4 - 8).astype(np.float32)
+    nb = np.arange(N // 128)[:, None]
+    b_s = np.ldexp(1.0, ((nb * 5 + kb * 2) % 7) - 3 - 8).astype(np.float32)
+    assert_gemm_close(run_gemm(a, a_s, b, b_s, "ue8m0"), oracle.gemm(a, a_s, b, b_s),
+                      "ue8m0 exponent pattern")
+
+
+def test_gemm_ue8m0_extreme_exponents():
+    """Scales at the ends of the ue8m0 range that act_quant and the weights can produce."""
+    M, N, K = 256, 256, 512
+    rng = np.random.default_rng(12)
+    a, b = random_codes(rng, M, K), random_codes(rng, N, K)
+    a_s = np.ldexp(1.0, rng.integers(-22, 0, size=(M, K // 128))).astype(np.float32)
+    b_s = np.ldexp(1.0, rng.integers(-10, 30, size=(N // 128, K // 128))).astype(np.float32)
+    assert_gemm_close(run_gemm(a, a_s, b, b_s, "ue8m0"), oracle.gemm(a, a_s, b, b_s),
+                      "ue8m0 extreme exponents")
+
+
+def test_gemm_ue8m0_reports_a_scale_that_is_not_a_power_of_two():
+    a, a_s, b, b_s = pow2_case(256, 256, 256, 5)
+    b_s = b_s.copy()
+    b_s[1, 1] *= np.float32(1.5)
+    run_gemm(a, a_s, b, b_s, "ue8m0")
+    assert fp8bs.fp8bs_device_error(clear=True) & fp8bs.DEVERR_SCALE_NOT_POW2
+
+
+@pytest.mark.parametrize("counts,N,K", [
+    ([0, 130, 5, 0, 257, 1], 384, 256),
+    ([64] * 8, 576, 512),
+    ([300, 0, 200], 2048, 256),
+])
+def test_gemm_grouped_ue8m0_block_scaled(counts, N, K):
+    grouped_check(counts, N, K, seed=sum(counts) + N + 1, what=f"grouped ue8m0 {counts}",
+                  fmt="ue8m0")
+
+
+def test_gemm_ue8m0_deterministic():
+    a, a_s, b, b_s = pow2_case(512, 1024, 1024, 9)
+    assert np.array_equal(run_gemm(a, a_s, b, b_s, "ue8m0"), run_gemm(a, a_s, b, b_s, "ue8m0"))
 
 
 # ------------------------------------------------------------------------------ bounded waits
