@@ -44,10 +44,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 
 # DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the decode GEMM,
-# from the ncu captures summarised in profiles/gemm_swapab_decode.md (M=1: 135.21 MB,
-# M=64: 135.60 MB), valid only for the gemm.cu they were taken on (first 16 hex digits of its
-# SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"gemm_sha": "3309e353991b32ab", "per_launch_mb": (135.21 + 135.60) / 2}
+# from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
+# valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
+# digits of their SHA-256); for any other source the bench reports traffic as null.
+DECODE_TRAFFIC_MB = {"kernel_sha": None, "per_launch_mb": None}
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -74,15 +74,25 @@ def decode_step_bytes():
     return sum(act_quant_bytes(M, K_DIM) + gemm_bytes(M, N_DIM, K_DIM) for M in DECODE_MS)
 
 
-def decode_traffic():
-    """Measured DRAM bytes per decode-GEMM launch, if the kernel source is unchanged."""
+DECODE_KERNEL_SOURCES = ("gemm_swapab.cu", "gemm_common.cuh", "ptx.cuh", "kernels.h")
+
+
+def decode_kernel_sha():
+    """Hash of the sources the decode GEMM kernel is compiled from."""
     import hashlib
-    path = os.path.join(ROOT, "fp8_block_scaled_fp8bs_gb300", "csrc", "gemm.cu")
+    h = hashlib.sha256()
     try:
-        sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+        for f in DECODE_KERNEL_SOURCES:
+            h.update(open(os.path.join(ROOT, "fp8_block_scaled_fp8bs_gb300", "csrc", f), "rb").read())
     except OSError:
         return None
-    if sha != DECODE_TRAFFIC_MB["gemm_sha"]:
+    return h.hexdigest()[:16]
+
+
+def decode_traffic():
+    """Measured DRAM bytes per decode-GEMM launch, if the kernel's sources are unchanged."""
+    sha = decode_kernel_sha()
+    if sha is None or sha != DECODE_TRAFFIC_MB["kernel_sha"]:
         return None
     return round(DECODE_TRAFFIC_MB["per_launch_mb"] * 1e6)
 
@@ -380,11 +390,15 @@ def secondary(g: Gpu, peaks, reps=10):
         out[name] = {"M": M, "K": K, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
                      "frac_hbm": round(gbs / hbm, 4)}
 
-    # ue8m0 MLA projections
+    # ue8m0 MLA projections (block-scaled MMA: the tensor cores apply the power-of-two scales)
     xa = synth.mla_acts()
     for N in (synth.Q_LORA, synth.KV_LORA_ROPE):
         bc, bs = synth.weights(N, K_DIM, 0, f"mla/B{N}", pow2=True)
         gemm_entry(f"mla_ue8m0_N{N}", 2048, N, K_DIM, 1, xa, bc, bs)
+    # the prefill up-projection shape with ue8m0 scales, on the same block-scaled kernel
+    bc, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up", pow2=True)
+    gemm_entry("prefill_up_ue8m0", 4096, N_DIM, K_DIM, 1, synth.prefill_up(), bc, bs)
+    del bc
 
     # MoE: 32 expert GEMMs back to back on one stream, timed as a group
     rows, counts = synth.moe_routing(0)
@@ -535,6 +549,17 @@ def run_profile(case: str, launches: int, warmup: int):
         c = torch.empty((4096, N), dtype=torch.bfloat16, device="cuda")
         g.act_quant(x, y, s, 4096, K)
         fn = lambda: g.gemm(y, s, B, S, c, 4096, N, K)  # noqa: E731
+    elif case.startswith("mla"):
+        # ue8m0 MLA projection on the block-scaled kernel: mla1536 or mla576
+        N = int(case[len("mla"):] or synth.Q_LORA)
+        b, bs = synth.weights(N, K_DIM, 0, f"mla/B{N}", pow2=True)
+        B, S = g.e4m3(b), g.f32(bs)
+        x = g.bf16(synth.mla_acts())
+        y = torch.empty((2048, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((2048, K_DIM // 128), dtype=torch.float32, device="cuda")
+        c = torch.empty((2048, N), dtype=torch.bfloat16, device="cuda")
+        g.act_quant(x, y, s, 2048, K_DIM, 1)
+        fn = lambda: g.gemm(y, s, B, S, c, 2048, N, K_DIM, 1)  # noqa: E731
     elif case == "act_quant":
         rows, _ = synth.moe_routing(0)
         x = g.bf16(synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows])
@@ -615,7 +640,7 @@ def main(argv=None):
                     "and no CPU baseline")
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
     ap.add_argument("--profile", metavar="CASE", default=None,
-                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, "
+                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, mla1536, mla576, "
                          "act_quant, dequant, moe): warmup + steps launches, for ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
@@ -655,7 +680,7 @@ def main(argv=None):
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "traffic": decode_traffic(),
                 "traffic_note": "dram read+write bytes per launch, ncu "
-                                "(profiles/gemm_swapab_decode.md); null if gemm.cu changed",
+                                "(profiles/gemm_swapab_decode.md); null if the kernel's sources changed",
                 "per_launch": [{"M": M, "us": round(d * 1e3, 2),
                                 "GB/s": round(gemm_bytes(M, N_DIM, K_DIM) / (d * 1e6), 1)}
                                for M, d in per_m]}

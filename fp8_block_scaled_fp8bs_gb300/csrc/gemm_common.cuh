@@ -1,0 +1,192 @@
+// gemm_common.cuh -- pieces shared by the GEMM kernels (gemm_tn.cu, gemm_bs.cu, gemm_swapab.cu):
+// tile constants, the shared-memory ring of TMA stages with its mbarriers, tile decoding for
+// grouped launches, the bf16 row store and the device error word.
+//
+// Every GEMM kernel computes C[M,N] (bf16) = sum_kb a_s[m,kb] * b_s[n/128,kb] * P_kb[m,n],
+// where P_kb is the product of the 128-wide K block kb of A (e4m3 [M,K]) and B (e4m3 [N,K]) --
+// "DeepSeek-V3 Administrator & Developer Guide", §8.5.3 fp8_gemm_kernel -- with the same
+// warp-specialised scheme (one CTA per SM):
+//   TMA producer warp   streams 128-byte-wide K slices of A and B into a ring of shared-memory
+//                       stages (128-byte swizzle), completion counted on mbarriers;
+//   MMA issuer warp     per K block, 4 x tcgen05.mma (K = 32 each) into TMEM, then
+//                       tcgen05.commit to free the stage;
+//   epilogue warps      tcgen05.ld the fp32 accumulator from TMEM, round to bf16 and store.
+// The kernels differ in where the block scales are applied (CUDA-core promotion of each K
+// block's partial in gemm_tn.cu and gemm_swapab.cu; the tensor core itself, from ue8m0 scale
+// factors in TMEM, in gemm_bs.cu) and in the orientation of the MMA.
+//
+// Every wait is bounded (ptx.cuh); a wait that runs out records a bit in the device error
+// word, the CTA stops issuing, drains its in-flight TMA copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <cuda_bf16.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+#include "../../include/fp8bs.h"
+
+namespace fp8bs {
+namespace {
+
+// Each translation unit that includes this header has its own error word (internal linkage);
+// read_device_error in diag.cu combines the words of all of them.
+__device__ unsigned int g_device_error = 0;
+
+constexpr int BM = 128;       // tile rows on the MMA's M side = TMEM lanes
+constexpr int BK = 128;       // K block: one scale block, one 128-byte swizzle row of e4m3
+constexpr int MMA_K = 32;     // K per tcgen05.mma for 8-bit operands
+constexpr int A_TILE = BM * BK;  // bytes of one 128 x 128 e4m3 tile
+
+__device__ __forceinline__ void record_error(unsigned bit) { atomicOr(&g_device_error, bit); }
+
+__host__ __device__ constexpr uint32_t tmem_cols_for(uint32_t used) {
+    uint32_t c = 32;
+    while (c < used) c <<= 1;
+    return c;
+}
+
+__device__ __forceinline__ uint8_t* align_1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Warp-uniform bounded wait: every lane waits, the warp agrees on the outcome.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity) {
+    const bool ok = mbar_wait(bar, parity);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// acc[0..1] += (v0, v1) * (s0, s1) as one packed fp32x2 FMA (round-to-nearest per component).
+__device__ __forceinline__ void fma2_into(float* acc, float v0, float v1, float s0, float s1) {
+    const float2 r = __ffma2_rn(make_float2(v0, v1), make_float2(s0, s1), make_float2(acc[0], acc[1]));
+    acc[0] = r.x;
+    acc[1] = r.y;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// Shared-memory bookkeeping common to both kernels.
+struct Ring {
+    uint64_t* full;    // [stages] TMA bytes landed
+    uint64_t* empty;   // [stages] MMAs reading the stage are done
+    uint64_t* tfull;   // [2] TMEM buffer holds a finished partial
+    uint64_t* tempty;  // [2] TMEM buffer has been read out
+    uint64_t* drain;   // [1] all MMAs issued by the CTA are done
+    uint32_t* tmem_holder;
+};
+
+__device__ __forceinline__ Ring carve_ring(uint8_t* p, int stages) {
+    Ring r;
+    r.full = reinterpret_cast<uint64_t*>(p);
+    r.empty = r.full + stages;
+    r.tfull = r.empty + stages;
+    r.tempty = r.tfull + 2;
+    r.drain = r.tempty + 2;
+    r.tmem_holder = reinterpret_cast<uint32_t*>(r.drain + 1);
+    return r;
+}
+
+constexpr int ring_bytes(int stages) { return (2 * stages + 5) * 8 + 16; }
+
+// full[s] completes on `full_count` arrivals plus the stage's TMA bytes (the producer's
+// arrive.expect_tx is one arrival; the block-scaled kernel adds its scale-factor warps).
+__device__ __forceinline__ void init_ring(const Ring& r, int stages, uint32_t epi_warps,
+                                          uint32_t full_count = 1) {
+    for (int s = 0; s < stages; ++s) {
+        mbar_init(&r.full[s], full_count);
+        mbar_init(&r.empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+        mbar_init(&r.tfull[b], 1);
+        mbar_init(&r.tempty[b], epi_warps);
+    }
+    mbar_init(r.drain, 1);
+    fence_barrier_init();
+}
+
+// After an abort, wait (briefly) for the TMA copies this producer issued but that no consumer
+// saw land, so that no copy is still writing shared memory when the CTA exits.
+__device__ __forceinline__ void drain_tma(const Ring& r, int stages, int64_t issued) {
+    const int64_t first = issued > stages ? issued - stages : 0;
+    for (int64_t i = first; i < issued; ++i) {
+        const int s = static_cast<int>(i % stages);
+        const uint32_t ph = static_cast<uint32_t>((i / stages) & 1);
+        if (!mbar_wait(&r.full[s], ph, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
+    }
+}
+
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Coordinates of one output tile: group, first row (global), first column, end of the group's
+// rows. Tiles are numbered group by group, m tiles fastest within a group.
+struct TileCoord {
+    int g, m0, n0, row_end;
+};
+
+template <int BN>
+__device__ __forceinline__ TileCoord decode_tile(const GroupTable& gt, int tile, int n_tiles) {
+    int grp = 0;
+    while (tile >= gt.tile_off[grp + 1]) ++grp;   // groups without tiles are skipped
+    const int local = tile - gt.tile_off[grp];
+    const int m_tiles = (gt.tile_off[grp + 1] - gt.tile_off[grp]) / n_tiles;
+    TileCoord t;
+    t.g = grp;
+    t.m0 = gt.row_off[grp] + (local % m_tiles) * BM;
+    t.n0 = (local / m_tiles) * BN;
+    t.row_end = gt.row_off[grp + 1];
+    return t;
+}
+
+// Round `CW` fp32 values to bf16 and store the first `valid` of them at `crow` (one row of C):
+// 16-byte stores when the row pitch keeps them aligned (N % 8 == 0), else element stores.
+template <int CW>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* crow, const float* acc, int valid,
+                                               bool vec) {
+    if (vec) {
+#pragma unroll
+        for (int j = 0; j < CW / 8; ++j) {
+            if (8 * j < valid) {
+                uint4 o;
+                o.x = pack_bf16x2(acc[8 * j + 0], acc[8 * j + 1]);
+                o.y = pack_bf16x2(acc[8 * j + 2], acc[8 * j + 3]);
+                o.z = pack_bf16x2(acc[8 * j + 4], acc[8 * j + 5]);
+                o.w = pack_bf16x2(acc[8 * j + 6], acc[8 * j + 7]);
+                *reinterpret_cast<uint4*>(crow + 8 * j) = o;
+            }
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < CW; ++j)
+            if (j < valid) crow[j] = __float2bfloat16_rn(acc[j]);
+    }
+}
+
+constexpr int kSmemLimit = 227 * 1024;
+constexpr int kMaxStages = 8;
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// Read (and, if `clear`, reset) this translation unit's error word; enqueued on `stream`.
+inline cudaError_t read_tu_error(unsigned int* out, bool clear, cudaStream_t stream) {
+    cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_device_error, sizeof(unsigned int), 0,
+                                              cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess || !clear) return e;
+    static const unsigned int zero = 0;
+    return cudaMemcpyToSymbolAsync(g_device_error, &zero, sizeof(unsigned int), 0,
+                                   cudaMemcpyHostToDevice, stream);
+}
+
+}  // namespace
+}  // namespace fp8bs

@@ -80,7 +80,11 @@ cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
 // Diagnostic kernel: one wait on a barrier nothing signals (see fp8bs_probe_wait_timeout).
 cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream);
 
-// The device error word of the GEMM kernels (read/clear).
+// The device error word of the library (read/clear; synchronises `stream`): the OR of the
+// words of the kernel files, each read (and cleared) by its own function below.
 cudaError_t read_device_error(unsigned int* out, bool clear, cudaStream_t stream);
+cudaError_t read_error_tn(unsigned int* out, bool clear, cudaStream_t stream);
+cudaError_t read_error_bs(unsigned int* out, bool clear, cudaStream_t stream);
+cudaError_t read_error_swapab(unsigned int* out, bool clear, cudaStream_t stream);
 
 }  // namespace fp8bs
