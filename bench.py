@@ -180,6 +180,7 @@ class Gpu:
         self.stream = torch.cuda.current_stream()
         self.sh = self.stream.cuda_stream
         self._flush_buf = None
+        self._ws = None
 
     def bf16(self, bits):
         return self.torch.from_numpy(np.ascontiguousarray(bits)).view(self.torch.bfloat16).cuda()
@@ -214,22 +215,43 @@ class Gpu:
         self.fp8bs.fp8bs_gemm_ex(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
                                  c.data_ptr(), M, N, K, fmt, flags, self.sh)
 
+    def gemm_ws(self, a, a_s, b, b_s, c, M, N, K, fmt=0):
+        """fp8bs_gemm_ws with the benchmark's workspace (stream-K where it pays)."""
+        if self._ws is None:
+            self._ws = self.torch.zeros(self.fp8bs.fp8bs_gemm_workspace_size(),
+                                        dtype=self.torch.uint8, device="cuda")
+        self.fp8bs.fp8bs_gemm_ws(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
+                                 c.data_ptr(), M, N, K, fmt, 0, self._ws.data_ptr(),
+                                 self._ws.numel(), self.sh)
+
     def dequant(self, w, s, y, N, K):
         self.fp8bs.fp8bs_weight_dequant(w.data_ptr(), s.data_ptr(), y.data_ptr(), N, K, self.sh)
 
     def time_each(self, fn, reps, flush=True):
-        """Median device time (ms) of fn() over reps launches, L2 flushed before each."""
-        ts = []
+        """Device time (ms) of one fn() launch with a cold L2: `reps` launches back to back,
+        each after an L2 flush, timed as one region between two events, minus a region of the
+        flushes alone. (An event pair around every single launch would add the GPU's launch
+        latency, ~5 us here, to each sample.) Everything is enqueued behind a GPU sleep so that
+        no launch waits on the host."""
+        torch = self.torch
+        e = [self.event() for _ in range(3)]
+        fn()
+        if flush:
+            self.flush_l2()          # allocates the flush buffer outside the timed region
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e6 + reps * 2e5))       # ~1 ms + 0.1 ms per launch at 2 GHz
+        e[0].record()
         for _ in range(reps):
             if flush:
                 self.flush_l2()
-            e0, e1 = self.event(), self.event()
-            e0.record()
             fn()
-            e1.record()
-            e1.synchronize()
-            ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        e[1].record()
+        if flush:
+            for _ in range(reps):
+                self.flush_l2()
+        e[2].record()
+        torch.cuda.synchronize()
+        return (e[0].elapsed_time(e[1]) - e[1].elapsed_time(e[2])) / reps
 
 
 def decode_setup(g: Gpu, seed=0):
@@ -254,19 +276,14 @@ def decode_setup(g: Gpu, seed=0):
 WEIGHTS_CONSTANT = 1   # fp8bs_gemm_ex flag: model weights are not written during the step
 
 
-def decode_step(g: Gpu, state, events=None):
-    """act_quant + fp8_gemm for every M. Without events the kernels run back to back and each
-    may start while the previous one finishes (the GEMM starts its weight stream early); with
-    events, each GEMM launch is bracketed and timed on its own."""
-    for i, st in enumerate(state):
+def decode_step(g: Gpu, state):
+    """act_quant + fp8_gemm for every M, back to back: each kernel may start while the
+    previous one finishes (the GEMM starts its weight stream early)."""
+    for st in state:
         M = st["M"]
         g.act_quant(st["x"], st["y"], st["s"], M, K_DIM)
-        if events is not None:
-            events[i][0].record()
         g.gemm_ex(st["y"], st["s"], st["B"], st["S"], st["c"], M, N_DIM, K_DIM, 0,
                   WEIGHTS_CONSTANT)
-        if events is not None:
-            events[i][1].record()
 
 
 def run_decode(g: Gpu, steps, warmup, rank, world, clocks_path):
@@ -289,17 +306,34 @@ def run_decode(g: Gpu, steps, warmup, rank, world, clocks_path):
         barrier(world)
         time.sleep(0.25)
     ms_total = t0.elapsed_time(t1)
-    # each GEMM launch on its own (events in between keep it from overlapping its neighbours)
-    reps = max(3, min(steps, 200))
-    ev = [[[g.event(), g.event()] for _ in state] for _ in range(reps)]
-    for k in range(reps):
-        decode_step(g, state, ev[k])
-    torch.cuda.synchronize()
+    return ms_total, decode_gemm_launch_ms(g, state, max(3, min(steps, 100))), sampler.summary()
+
+
+def decode_gemm_launch_ms(g: Gpu, state, rounds):
+    """Average duration of one decode-GEMM launch per M: `rounds` x 4 launches back to back,
+    cycling through the four distinct 132 MB weights (so that no launch finds its weight in
+    L2), timed as one region between two events on the launching stream."""
+    torch = g.torch
     per_m = []
-    for i, st in enumerate(state):
-        d = [ev[k][i][0].elapsed_time(ev[k][i][1]) for k in range(reps)]
-        per_m.append((st["M"], statistics.mean(d)))
-    return ms_total, per_m, sampler.summary()
+    for st in state:
+        M = st["M"]
+
+        def launch(w):
+            g.gemm_ex(st["y"], st["s"], w["B"], w["S"], st["c"], M, N_DIM, K_DIM, 0,
+                      WEIGHTS_CONSTANT)
+        for w in state:
+            launch(w)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e6 + rounds * 4e5))
+        t0, t1 = g.event(), g.event()
+        t0.record()
+        for _ in range(rounds):
+            for w in state:
+                launch(w)
+        t1.record()
+        torch.cuda.synchronize()
+        per_m.append((M, t0.elapsed_time(t1) / (rounds * len(state))))
+    return per_m
 
 
 def run_decode_e2e(g: Gpu, steps, warmup, world):
@@ -334,7 +368,7 @@ def run_decode_e2e(g: Gpu, steps, warmup, world):
     return t0.elapsed_time(t1), h2d, d2h
 
 
-def secondary(g: Gpu, peaks, reps=10):
+def secondary(g: Gpu, peaks, reps=20):
     """Other workloads of the path, each kernel timed alone with L2 flushed before every
     launch; reported against its roofline."""
     torch = g.torch
@@ -350,8 +384,8 @@ def secondary(g: Gpu, peaks, reps=10):
         B, S = g.e4m3(b_codes), g.f32(b_s)
         c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
         for _ in range(3):
-            g.gemm(y, s, B, S, c, M, N, K, fmt)
-        ms = g.time_each(lambda: g.gemm(y, s, B, S, c, M, N, K, fmt), reps)
+            g.gemm_ws(y, s, B, S, c, M, N, K, fmt)
+        ms = g.time_each(lambda: g.gemm_ws(y, s, B, S, c, M, N, K, fmt), reps)
         tf = gemm_flops(M, N, K) / ms / 1e9
         gb = gemm_bytes(M, N, K) / ms / 1e6
         bound_ms = max(gemm_flops(M, N, K) / (fp8_peak * 1e9), gemm_bytes(M, N, K) / (hbm * 1e6))
@@ -559,7 +593,7 @@ def run_profile(case: str, launches: int, warmup: int):
         s = torch.empty((2048, K_DIM // 128), dtype=torch.float32, device="cuda")
         c = torch.empty((2048, N), dtype=torch.bfloat16, device="cuda")
         g.act_quant(x, y, s, 2048, K_DIM, 1)
-        fn = lambda: g.gemm(y, s, B, S, c, 2048, N, K_DIM, 1)  # noqa: E731
+        fn = lambda: g.gemm_ws(y, s, B, S, c, 2048, N, K_DIM, 1)  # noqa: E731
     elif case == "act_quant":
         rows, _ = synth.moe_routing(0)
         x = g.bf16(synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows])
@@ -673,8 +707,9 @@ def main(argv=None):
     gemm_bytes_total = sum(gemm_bytes(M, N_DIM, K_DIM) for M in DECODE_MS)
     gemm_ms = sum(d for _, d in per_m)
     achieved = gemm_bytes_total / (gemm_ms * 1e6)
-    roofline = {"kernel": "gemm_swapab_kernel (decode fp8_gemm, all four M, each launch timed "
-                          "on its own)",
+    roofline = {"kernel": "gemm_swapab_kernel (decode fp8_gemm, all four M; per M, 4 x rounds "
+                          "launches back to back over four distinct weights, one event pair "
+                          "around the region)",
                 "bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",

@@ -37,7 +37,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 GEMM_WEIGHTS_CONSTANT = 0x1
 EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_ex",
-           "fp8bs_gemm_grouped",
+           "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_grouped",
            "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
 
 _lock = threading.Lock()
@@ -66,6 +66,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_weight_dequant.argtypes = [vp, vp, vp, i64, i64, vp]
         lib.fp8bs_gemm.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, vp]
         lib.fp8bs_gemm_ex.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint, vp]
+        lib.fp8bs_gemm_ws.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint, vp,
+                                      ctypes.c_size_t, vp]
+        lib.fp8bs_gemm_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
         lib.fp8bs_gemm_grouped.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
                                            i64, i64, i64, i32, vp]
         lib.fp8bs_status_string.argtypes = [i32]
@@ -101,6 +104,18 @@ def fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, stream=0) -> No
 def fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0, stream=0) -> None:
     _check("fp8bs_gemm_ex", load().fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags,
                                                  stream))
+
+
+def fp8bs_gemm_ws(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0, workspace=0,
+                  workspace_bytes=0, stream=0) -> None:
+    _check("fp8bs_gemm_ws", load().fp8bs_gemm_ws(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags,
+                                                 workspace, workspace_bytes, stream))
+
+
+def fp8bs_gemm_workspace_size() -> int:
+    out = ctypes.c_size_t(0)
+    _check("fp8bs_gemm_workspace_size", load().fp8bs_gemm_workspace_size(ctypes.byref(out)))
+    return out.value
 
 
 def fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt=SCALE_FP32,
@@ -170,9 +185,28 @@ def weight_dequant(w, s):
     return y
 
 
-def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False):
+_workspaces = {}
+
+
+def gemm_workspace(device=None, stream=None):
+    """The zero-filled workspace fp8_gemm uses on `device` for calls on `stream` (one per
+    device and stream, so that calls that may overlap never share one), allocated on first use."""
+    import torch
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    key = (dev.index, stream if stream is not None else _stream())
+    ws = _workspaces.get(key)
+    if ws is None:
+        with torch.cuda.device(dev):
+            ws = torch.zeros(fp8bs_gemm_workspace_size(), dtype=torch.uint8, device=dev)
+        _workspaces[key] = ws
+    return ws
+
+
+def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False,
+             workspace="auto"):
     """C[M,N] bf16 = A[M,K] . B[N,K]^T with per-128-K-block scales a_s [M,K/128] and
-    b_s [ceil(N/128), K/128]."""
+    b_s [ceil(N/128), K/128]. workspace: "auto" (a cached one per device and stream), None (no
+    split K loops) or a zero-filled uint8 CUDA tensor of fp8bs_gemm_workspace_size() bytes."""
     import torch
     _require(a, torch.float8_e4m3fn, 2, "a")
     _require(b, torch.float8_e4m3fn, 2, "b")
@@ -184,9 +218,13 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False)
             tuple(b_s.shape) != (-(-N // BLOCK), K // BLOCK):
         raise ValueError("operand or scale shapes do not match")
     c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
-    fp8bs_gemm_ex(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = gemm_workspace(a.device)
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (0, 0)
+    fp8bs_gemm_ws(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
                   M, N, K, _fmt(scale_fmt), GEMM_WEIGHTS_CONSTANT if weights_constant else 0,
-                  _stream())
+                  ws_ptr, ws_bytes, _stream())
     return c
 
 

@@ -72,6 +72,71 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int b
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
 
+// fp8bs_gemm_ex and fp8bs_gemm_ws: checks, then the kernel for the shape (see fp8bs.h).
+int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
+              int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
+              void* workspace, size_t workspace_bytes, void* stream) {
+    if ((flags & ~FP8BS_GEMM_WEIGHTS_CONSTANT) != 0) return FP8BS_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
+    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
+        return FP8BS_ERR_INVALID_ARG;
+    // The kernels index with 32-bit row/column coordinates (TMA coordinates are 32-bit).
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (!c) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(c)) return FP8BS_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (K == 0) {
+        int sms = 0;
+        if (int e = check_device(&sms)) return e;
+        return status_of(cudaMemsetAsync(c, 0, static_cast<size_t>(M * N) * 2, st));
+    }
+    if (!a || !a_s || !b || !b_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(a) || !aligned16(b) || !aligned4(a_s) || !aligned4(b_s))
+        return FP8BS_ERR_MISALIGNED;
+    int sms = 0;
+    if (int e = check_device(&sms)) return e;
+    if (workspace) {
+        if (!aligned16(workspace)) return FP8BS_ERR_MISALIGNED;
+        if (workspace_bytes < fp8bs::bs_stream_k_workspace(sms)) return FP8BS_ERR_INVALID_ARG;
+    }
+
+    GemmArgs g;
+    g.a_s = a_s;
+    g.b_s = b_s;
+    g.c = c;
+    g.M = static_cast<int>(M);
+    g.N = static_cast<int>(N);
+    g.K = static_cast<int>(K);
+    g.weights_constant = (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0;
+
+    CUtensorMap tmA, tmB;
+    if (M <= 128) {
+        // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA.
+        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, MT)) return FP8BS_ERR_CUDA;
+        cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, st);
+        if (e != cudaErrorInvalidValue) return status_of(e);
+        // K too long to stage the activation scales: fall through to the normal kernel.
+    }
+    const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
+    const int64_t m_tiles = (M + 127) / 128;
+    // Stream-K (shared K loops) when a workspace is given and whole tiles would idle SMs.
+    const bool stream_k =
+        block_scaled && workspace && fp8bs::bs_stream_k_pays(m_tiles, N, K / 128, sms);
+    const int BN = stream_k       ? 128
+                   : block_scaled ? fp8bs::pick_tile_n_bs(m_tiles, N, sms)
+                                  : fp8bs::pick_tile_n(m_tiles, N, sms);
+    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
+    const int64_t rows[2] = {0, M};
+    fp8bs::GroupTable gt;
+    fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), BN);
+    if (block_scaled)
+        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms,
+                                               stream_k ? workspace : nullptr, st));
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
+}
+
 }  // namespace
 
 extern "C" {
@@ -122,54 +187,22 @@ int fp8bs_gemm(const void* a, const float* a_s, const void* b, const float* b_s,
 int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
                   int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
                   void* stream) {
-    if ((flags & ~FP8BS_GEMM_WEIGHTS_CONSTANT) != 0) return FP8BS_ERR_INVALID_ARG;
-    if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
-    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
-        return FP8BS_ERR_INVALID_ARG;
-    // The kernels index with 32-bit row/column coordinates (TMA coordinates are 32-bit).
-    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
-    if (M == 0 || N == 0) return FP8BS_OK;
-    if (!c) return FP8BS_ERR_INVALID_ARG;
-    if (!aligned16(c)) return FP8BS_ERR_MISALIGNED;
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (K == 0) {
-        int sms = 0;
-        if (int e = check_device(&sms)) return e;
-        return status_of(cudaMemsetAsync(c, 0, static_cast<size_t>(M * N) * 2, st));
-    }
-    if (!a || !a_s || !b || !b_s) return FP8BS_ERR_INVALID_ARG;
-    if (!aligned16(a) || !aligned16(b) || !aligned4(a_s) || !aligned4(b_s))
-        return FP8BS_ERR_MISALIGNED;
+    return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, nullptr, 0, stream);
+}
+
+int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
+                  int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
+                  void* workspace, size_t workspace_bytes, void* stream) {
+    return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes,
+                     stream);
+}
+
+int fp8bs_gemm_workspace_size(size_t* bytes) {
+    if (!bytes) return FP8BS_ERR_INVALID_ARG;
     int sms = 0;
-    if (int e = check_device(&sms)) return e;
-
-    GemmArgs g;
-    g.a_s = a_s;
-    g.b_s = b_s;
-    g.c = c;
-    g.M = static_cast<int>(M);
-    g.N = static_cast<int>(N);
-    g.K = static_cast<int>(K);
-    g.weights_constant = (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0;
-
-    CUtensorMap tmA, tmB;
-    if (M <= 128) {
-        // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA.
-        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-        if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, MT)) return FP8BS_ERR_CUDA;
-        cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, st);
-        if (e != cudaErrorInvalidValue) return status_of(e);
-        // K too long to stage the activation scales: fall through to the normal kernel.
-    }
-    const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
-    const int BN = block_scaled ? fp8bs::pick_tile_n_bs((M + 127) / 128, N, sms)
-                                : fp8bs::pick_tile_n((M + 127) / 128, N, sms);
-    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
-    const int64_t rows[2] = {0, M};
-    fp8bs::GroupTable gt;
-    fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), BN);
-    if (block_scaled) return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, st));
-    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
+    if (int st = check_device(&sms)) return st;
+    *bytes = fp8bs::bs_stream_k_workspace(sms);
+    return FP8BS_OK;
 }
 
 int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
@@ -219,7 +252,8 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     CUtensorMap tmA, tmB;
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
         return FP8BS_ERR_CUDA;
-    if (block_scaled) return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, st));
+    if (block_scaled)
+        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, nullptr, st));
     return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
 }
 

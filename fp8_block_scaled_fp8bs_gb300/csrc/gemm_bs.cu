@@ -18,13 +18,24 @@
 // B). A stage's full barrier completes when its TMA bytes have landed AND the four scale-factor
 // warps have written its slot; the MMA's commit to the stage's empty barrier frees both.
 //
-// Scale-factor placement. Tiles are BN <= 128 columns wide and start on a multiple of BN, so
-// the tile lies inside one 128-row block of B and its B exponent is one value: every lane,
-// column and byte of the B slot holds it. For A, lane L of the slot's four columns holds
-//   L < 32:  column j = exponent of tile row L + 32 j
-//   L >= 32: every column = exponent of tile row L
-// with the same byte in all four bytes of a word. This serves row m whether the tensor core
-// takes it from lane m column 0, from lane m column m/32, or from lane m%32 column m/32.
+// Scale-factor placement. The tensor core takes the exponent of row m of A from lane m,
+// column m/32 of the A slot, and the exponent of row n of B (for output rows of lane quarter q)
+// from lane 32q + n%32, column n/32 of the B slot -- measured on GB300 by giving every lane,
+// column and byte of the slots a distinct exponent. Lane L writes the exponent of tile row L
+// into all four columns of the A slot. Tiles are BN <= 128 columns wide and start on a multiple
+// of BN, so a tile lies inside one 128-row block of B and its B exponent is one value, written
+// to every lane and column of the B slot. Every byte of a word holds the same exponent.
+//
+// Work schedule. Data-parallel: CTA c computes tiles c, c + gridDim.x, ... whole. Stream-K
+// (when a workspace is given and the tiles alone would leave SMs idle): the tiles x K blocks
+// units are cut into gridDim.x equal contiguous ranges and CTA c works through its range tile
+// by tile, so a tile's K loop may be shared by consecutive CTAs. Only a CTA's first piece can
+// start inside a tile; that CTA writes its fp32 partial to its own workspace slot and counts it
+// in the flag of the tile's owner, the CTA holding the tile's first K blocks (the last piece of
+// its own range). The owner waits for its flag, adds the partials in K order -- a fixed order,
+// so results do not depend on timing -- resets the flag and stores. It only waits on CTAs after it, each of which
+// writes its partial before anything else, and every CTA of the grid is resident (one per
+// SM), so the wait always ends.
 #include "gemm_common.cuh"
 
 namespace fp8bs {
@@ -41,6 +52,7 @@ struct BsCfg {
     static constexpr int STAGE = A_TILE + B_TILE;
     static constexpr int SF_COLS = 8;                 // per stage: A in 0..3, B in 4..7
     static constexpr int SF_COL0 = 2 * BN;            // after the two accumulators
+    static constexpr int PART = BM * BN * 4;          // one fp32 partial tile (stream-K)
 };
 
 template <int BN>
@@ -59,32 +71,112 @@ __device__ __forceinline__ uint32_t ue8m0_code(float v, bool& ok) {
 
 __device__ __forceinline__ uint32_t splat4(uint32_t byte) { return byte * 0x01010101u; }
 
-// Exponents of a_s[row, kb] for the rows this scale-factor lane writes (4 rows in warp 0,
-// the lane's own row elsewhere) and of b_s[nb, kb], raw fp32; kb past the end loads nothing.
-__device__ __forceinline__ void load_sf(float* va, float& vb, const float* const* as_r,
-                                        const float* bs_row, int kb, int num_kb, bool four) {
-    if (kb >= num_kb) return;
-    if (four) {
-#pragma unroll
-        for (int j = 0; j < 4; ++j) va[j] = __ldg(as_r[j] + kb);
-    } else {
-        const float v = __ldg(as_r[0] + kb);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) va[j] = v;
+// Stream-K workspace: `flags` one counter per CTA (partials published for the tile it owns),
+// then `parts`, one 128 x BN fp32 partial per CTA as float4 chunks [cta][chunk][row] (a warp's
+// 32 rows of one chunk are 512 contiguous bytes). The layout depends only on the SM count, so a
+// workspace serves every problem size. Both null in the data-parallel schedule.
+struct StreamK {
+    int* flags;
+    float4* parts;
+};
+
+// A CTA's pieces of work, in order: (tile, first K block, end K block).
+struct Sched {
+    int64_t u, u_end;   // stream-K: unit cursor and end of this CTA's range
+    int tile;           // data-parallel: next tile
+    bool sk;
+};
+
+__device__ __forceinline__ int64_t sk_range_start(int cta, int64_t units) {
+    return static_cast<int64_t>(cta) * units / gridDim.x;
+}
+
+// The CTA whose range holds unit x: the largest c with floor(c * units / grid) <= x.
+__device__ __forceinline__ int sk_owner(int64_t x, int64_t units) {
+    return static_cast<int>(((x + 1) * gridDim.x - 1) / units);
+}
+
+__device__ __forceinline__ Sched sched_begin(bool sk, int num_tiles, int num_kb) {
+    Sched s;
+    s.sk = sk;
+    s.tile = blockIdx.x;
+    const int64_t units = static_cast<int64_t>(num_tiles) * num_kb;
+    s.u = sk ? sk_range_start(blockIdx.x, units) : 0;
+    s.u_end = sk ? sk_range_start(blockIdx.x + 1, units) : 0;
+    return s;
+}
+
+__device__ __forceinline__ bool sched_next(Sched& s, int num_tiles, int num_kb, int& tile,
+                                           int& kb0, int& kb1) {
+    if (!s.sk) {
+        if (s.tile >= num_tiles) return false;
+        tile = s.tile;
+        kb0 = 0;
+        kb1 = num_kb;
+        s.tile += gridDim.x;
+        return true;
     }
-    vb = __ldg(bs_row + kb);
+    if (s.u >= s.u_end) return false;
+    tile = static_cast<int>(s.u / num_kb);
+    kb0 = static_cast<int>(s.u - static_cast<int64_t>(tile) * num_kb);
+    const int64_t left = s.u_end - s.u;
+    kb1 = left < num_kb - kb0 ? kb0 + static_cast<int>(left) : num_kb;
+    s.u += kb1 - kb0;
+    return true;
+}
+
+// Hand a TMEM accumulator back to the MMA issuer once this warp's loads of it have completed.
+__device__ __forceinline__ void release_tmem(uint64_t* tempty, int lane) {
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(tempty);
+}
+
+// The four epilogue warps (128 threads) only.
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+__device__ __forceinline__ void flag_add_release(int* flag, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int flag_load_acquire(const int* flag) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *flag == target.
+__device__ __forceinline__ bool flag_wait(const int* flag, int target) {
+    if (flag_load_acquire(flag) == target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (flag_load_acquire(flag) == target) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 template <int BN>
 __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs g, const __grid_constant__ GroupTable gt, const int stages) {
+                   const GemmArgs g, const __grid_constant__ GroupTable gt, const int stages,
+                   const StreamK sk) {
     using Cfg = BsCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sA = smem;
     uint8_t* sB = smem + stages * A_TILE;
-    const Ring ring = carve_ring(sB + stages * Cfg::B_TILE, stages);
+    const bool stream_k = sk.parts != nullptr;
+    // Stream-K only: the first contributor's partial of the tile this CTA owns, copied in while
+    // the owner's own piece still runs (after the stages, 1024-byte aligned), and the barrier
+    // counting its bytes (after the ring).
+    float4* sPart = reinterpret_cast<float4*>(sB + stages * Cfg::B_TILE);
+    const Ring ring = carve_ring(sB + stages * Cfg::B_TILE + (stream_k ? Cfg::PART : 0), stages);
+    uint64_t* part_bar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ring.full) +
+                                                     ring_bytes(stages));
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -99,6 +191,10 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     grid_launch_dependents();
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS, 1 + Cfg::SF_WARPS);
+        if (stream_k) {
+            mbar_init(part_bar, 1);
+            fence_barrier_init();
+        }
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
@@ -108,16 +204,19 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
 
+    Sched sched = sched_begin(stream_k, num_tiles, num_kb);
+    int tile, kb0, kb1;
+
     if (warp == PRODUCER) {
         if (lane == 0) {
             int stage = 0;
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
                 const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
                 const int b_row = t.g * g.N + t.n0;      // row of the stacked B
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
                         record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                         ok = false;
@@ -141,14 +240,14 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
                 if (!mbar_wait(&ring.tempty[buf], tphase ^ 1)) {
                     record_error(FP8BS_DEVERR_MMA_WAIT);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&ring.full[stage], phase)) {
                         record_error(FP8BS_DEVERR_MMA_WAIT);
                         ok = false;
@@ -163,7 +262,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     for (int j = 0; j < BK / MMA_K; ++j)
                         mma_f8_block_scaled(d_tmem, smem_desc_k_sw128(a_addr + j * MMA_K),
                                             smem_desc_k_sw128(b_addr + j * MMA_K), idesc, sfa,
-                                            sfa + 4, (kb > 0 || j > 0) ? 1u : 0u);
+                                            sfa + 4, (kb > kb0 || j > 0) ? 1u : 0u);
                     mma_commit(&ring.empty[stage]);
                     if (++stage == stages) {
                         stage = 0;
@@ -180,38 +279,40 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
         }
     } else if (warp < Cfg::SF_WARPS) {
-        // Scale-factor writers: warp w owns TMEM lanes 32w .. 32w+31 of every slot.
+        // Scale-factor writers: warp w owns TMEM lanes 32w .. 32w+31 of every slot, i.e. tile
+        // rows 32w .. 32w+31.
         constexpr int P = 8;                      // K blocks of scales in flight per lane
         const int nb_count = (g.N + 127) / 128;
         const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const bool four = (warp == 0);
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true, pow2 = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
             const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
             // Rows past the group's end (clamped into A) are computed but never stored.
-            const float* as_r[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int row = t.m0 + (four ? lane + 32 * j : warp * 32 + lane);
-                as_r[j] = g.a_s + static_cast<int64_t>(min(row, g.M - 1)) * num_kb;
-            }
+            const int row = min(t.m0 + warp * 32 + lane, g.M - 1);
+            const float* as_row = g.a_s + static_cast<int64_t>(row) * num_kb;
             const float* bs_row =
                 g.b_s + (static_cast<int64_t>(t.g) * nb_count + t.n0 / 128) * num_kb;
-            float va[P][4], vb[P];
+            float va[P], vb[P];
 #pragma unroll
-            for (int i = 0; i < P; ++i) load_sf(va[i], vb[i], as_r, bs_row, i, num_kb, four);
-            for (int kb0 = 0; ok && kb0 < num_kb; kb0 += P) {
+            for (int i = 0; i < P; ++i) {
+                if (kb0 + i < kb1) {
+                    va[i] = __ldg(as_row + kb0 + i);
+                    vb[i] = __ldg(bs_row + kb0 + i);
+                }
+            }
+            for (int kbp = kb0; ok && kbp < kb1; kbp += P) {
 #pragma unroll
                 for (int i = 0; i < P; ++i) {
-                    const int kb = kb0 + i;
-                    if (kb >= num_kb) break;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) w[j] = splat4(ue8m0_code(va[i][j], pow2));
+                    const int kb = kbp + i;
+                    if (kb >= kb1) break;
+                    const uint32_t wa = splat4(ue8m0_code(va[i], pow2));
                     const uint32_t wb = splat4(ue8m0_code(vb[i], pow2));
-                    load_sf(va[i], vb[i], as_r, bs_row, kb + P, num_kb, four);
+                    if (kb + P < kb1) {                 // the scales of kb + P, in flight
+                        va[i] = __ldg(as_row + kb + P);
+                        vb[i] = __ldg(bs_row + kb + P);
+                    }
                     if (!warp_wait(&ring.empty[stage], phase ^ 1)) {
                         if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                         ok = false;
@@ -220,7 +321,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     tc_fence_after();
                     const uint32_t taddr = tmem_base + lane_base +
                                            static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
-                    tmem_st_4cols(taddr, w[0], w[1], w[2], w[3]);
+                    tmem_st_4cols(taddr, wa, wa, wa, wa);
                     tmem_st_4cols(taddr + 4, wb, wb, wb, wb);
                     tmem_wait_st();
                     tc_fence_before();
@@ -238,10 +339,46 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
         // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31, i.e. tile rows of the same numbers.
         const int quarter = warp & 3;
         const int row_in_tile = quarter * 32 + lane;
+        const int epi_thread = row_in_tile;        // 0 .. 127
+        const int64_t units = static_cast<int64_t>(num_tiles) * num_kb;
         int buf = 0;
-        uint32_t tphase = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        uint32_t tphase = 0, part_phase = 0;
+        bool ok = true;
+        while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
             const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
+            const bool owner = kb0 == 0 && kb1 < num_kb;
+            int parts = 0;
+            bool got = true;
+            if (owner) {
+                // The tile continues in the next CTAs, each of which starts with its piece of
+                // it. While this CTA's own piece is still on the tensor cores, thread 0 waits
+                // for their partials and copies the first into shared memory; the outcome
+                // reaches the other epilogue threads through the word after the TMEM address.
+                const int64_t tile_end = static_cast<int64_t>(tile + 1) * num_kb;
+                for (int j = blockIdx.x + 1; j < static_cast<int>(gridDim.x) &&
+                                             sk_range_start(j, units) < tile_end; ++j)
+                    ++parts;
+                volatile uint32_t* outcome = ring.tmem_holder + 1;
+                if (epi_thread == 0) {
+                    got = flag_wait(sk.flags + blockIdx.x, parts);
+                    if (got) {
+                        sk.flags[blockIdx.x] = 0;        // ready for the next call
+                        fence_proxy_async_global();
+                        const float4* src = sk.parts + static_cast<int64_t>(blockIdx.x + 1) *
+                                                           (BN / 4) * BM;
+                        constexpr uint32_t kBytes = BM * BN * sizeof(float);
+                        mbar_arrive_expect_tx(part_bar, kBytes);
+                        for (int q = 0; q < 4; ++q)
+                            bulk_load(sPart + q * (kBytes / 64), src + q * (kBytes / 64),
+                                      kBytes / 4, part_bar);
+                    } else {
+                        record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                    }
+                    *outcome = got ? 1u : 0u;
+                }
+                epilogue_bar();
+                got = *outcome != 0;
+            }
             if (!warp_wait(&ring.tfull[buf], tphase)) {
                 if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
                 break;
@@ -249,23 +386,83 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * BN);
-            float acc[BN];
+            const int row = t.m0 + row_in_tile;
+            const bool store = row < t.row_end;
+            __nv_bfloat16* crow =
+                static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(row) * g.N + t.n0;
+            const int valid = min(BN, g.N - t.n0);
+            const bool vec = (g.N & 7) == 0;
+
+            if (kb0 == 0 && kb1 == num_kb) {
+                // A whole tile: the accumulator into registers, the buffer back, then store.
+                float acc[BN];
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
+                for (int c = 0; c < BN / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
-            // The accumulator is in registers: hand the buffer back before storing.
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
+                release_tmem(&ring.tempty[buf], lane);
+                if (store) store_row_bf16<BN>(crow, acc, valid, vec);
+            } else if (kb0 > 0) {
+                // A piece that does not start its tile: publish the partial in this CTA's slot,
+                // 32 columns at a time, and count it in the flag of the tile's owner.
+                float4* slot = sk.parts + static_cast<int64_t>(blockIdx.x) * (BN / 4) * BM;
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld_32cols(taddr + 32 * c, v);
+                    tmem_wait_ld_32(v);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q)
+                        __stcg(slot + (8 * c + q) * BM + row_in_tile,
+                               make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
+                }
+                release_tmem(&ring.tempty[buf], lane);
+                epilogue_bar();
+                if (epi_thread == 0) {
+                    __threadfence();
+                    flag_add_release(sk.flags + sk_owner(static_cast<int64_t>(tile) * num_kb, units), 1);
+                }
+            } else {
+                // The tile's first piece: per 32 columns, add the partials of the pieces that
+                // continue it in K order (the first from shared memory) and store.
+                const bool have = got && mbar_wait(part_bar, part_phase);
+                part_phase ^= 1;
+                if (got && !have && lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+#pragma unroll
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld_32cols(taddr + 32 * c, v);
+                    tmem_wait_ld_32(v);
+                    if (have) {
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const float4 p = sPart[(8 * c + q) * BM + row_in_tile];
+                            v[4 * q] += p.x;
+                            v[4 * q + 1] += p.y;
+                            v[4 * q + 2] += p.z;
+                            v[4 * q + 3] += p.w;
+                        }
+#pragma unroll 1
+                        for (int j = 2; j <= parts; ++j) {
+                            const float4* slot =
+                                sk.parts + static_cast<int64_t>(blockIdx.x + j) * (BN / 4) * BM;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 p = __ldcg(slot + (8 * c + q) * BM + row_in_tile);
+                                v[4 * q] += p.x;
+                                v[4 * q + 1] += p.y;
+                                v[4 * q + 2] += p.z;
+                                v[4 * q + 3] += p.w;
+                            }
+                        }
+                    }
+                    if (store && have) store_row_bf16<32>(crow + 32 * c, v, valid - 32 * c, vec);
+                }
+                release_tmem(&ring.tempty[buf], lane);
+                if (!have) ok = false;
+            }
             buf ^= 1;
             if (buf == 0) tphase ^= 1;
-            const int row = t.m0 + row_in_tile;
-            if (row < t.row_end) {
-                __nv_bfloat16* crow =
-                    static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(row) * g.N + t.n0;
-                store_row_bf16<BN>(crow, acc, min(BN, g.N - t.n0), (g.N & 7) == 0);
-            }
         }
     }
 
@@ -275,21 +472,37 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     if (warp == ISSUER) tmem_dealloc(tmem_base, tmem_cols);
 }
 
+size_t bs_flag_bytes(int num_sms) {
+    return (static_cast<size_t>(num_sms) * sizeof(int) + 255) & ~size_t(255);
+}
+
 template <int BN>
 cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                      const GroupTable& gt, int num_sms, cudaStream_t stream) {
+                      const GroupTable& gt, int num_sms, void* workspace, cudaStream_t stream) {
     using Cfg = BsCfg<BN>;
     int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
-    if (stages > kMaxStages) stages = kMaxStages;
     static_assert(bs_tmem_cols<BN>(kMaxStages) <= 512, "TMEM holds 512 columns");
-    const int smem = 1024 + stages * Cfg::STAGE + ring_bytes(stages);
-    cudaError_t e = set_smem(gemm_bs_kernel<BN>, smem);
+    // Stream-K keeps one partial tile (and its barrier) in shared memory, at two stages' cost.
+    const int part_bytes = workspace ? Cfg::PART + 16 : 0;
+    if (workspace) stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages) - part_bytes) / Cfg::STAGE;
+    if (stages > kMaxStages) stages = kMaxStages;
+    const int smem = 1024 + stages * Cfg::STAGE + part_bytes + ring_bytes(stages);
+    cudaError_t e = set_smem(gemm_bs_kernel<BN>, kSmemLimit);
     if (e != cudaSuccess) return e;
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
-    const int grid = tiles < num_sms ? tiles : num_sms;
+    StreamK sk = {nullptr, nullptr};
+    int grid = tiles < num_sms ? tiles : num_sms;
+    if (workspace) {
+        // Every CTA gets a nonempty range of units (there are at least as many as CTAs).
+        const int64_t units = static_cast<int64_t>(tiles) * (g.K / BK);
+        grid = units < num_sms ? static_cast<int>(units) : num_sms;
+        sk.flags = static_cast<int*>(workspace);
+        sk.parts = reinterpret_cast<float4*>(static_cast<char*>(workspace) +
+                                             bs_flag_bytes(num_sms));
+    }
     return launch_pdl(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, tmA, tmB, g, gt,
-                      stages);
+                      stages, sk);
 }
 
 }  // namespace
@@ -298,11 +511,29 @@ int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
     return m_tiles_total * ((N + 127) / 128) * 5 >= num_sms * 4 ? 128 : 64;
 }
 
+// Stream-K pays when whole tiles would leave SMs idle for a large part of the run: compare
+// the K blocks the busiest SM works through (plus about four K blocks' worth for writing and
+// adding a partial) with the data-parallel schedule's, which runs ceil(tiles / SMs) whole tiles.
+bool bs_stream_k_pays(int64_t m_tiles_total, int64_t N, int64_t num_kb, int num_sms) {
+    if (num_kb < 2) return false;
+    const int bn_dp = pick_tile_n_bs(m_tiles_total, N, num_sms);
+    const int64_t tiles_dp = m_tiles_total * ((N + bn_dp - 1) / bn_dp);
+    const int64_t cost_dp = (tiles_dp + num_sms - 1) / num_sms * num_kb;
+    const int64_t units = m_tiles_total * ((N + 127) / 128) * num_kb;
+    const int64_t cost_sk = (units + num_sms - 1) / num_sms + 4;
+    return cost_sk * 10 < cost_dp * 9;
+}
+
+size_t bs_stream_k_workspace(int num_sms) {
+    return bs_flag_bytes(num_sms) + static_cast<size_t>(num_sms) * BM * 128 * sizeof(float);
+}
+
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           const GroupTable& gt, int BN, int num_sms, cudaStream_t stream) {
+                           const GroupTable& gt, int BN, int num_sms, void* workspace,
+                           cudaStream_t stream) {
     switch (BN) {
-        case 64: return launch_bs<64>(tmA, tmB, g, gt, num_sms, stream);
-        case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, stream);
+        case 64: return launch_bs<64>(tmA, tmB, g, gt, num_sms, workspace, stream);
+        case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, workspace, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -68,9 +68,15 @@ cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 // Block-scaled orientation, for scales that are all powers of two (FP8BS_SCALE_UE8M0): the
 // tensor core applies a_s and b_s as ue8m0 exponents per K block; tiles of 128 rows x BN
 // (64 or 128) columns, same maps and group table as launch_gemm_tn.
+// With a workspace (stream-K schedule, BN = 128 only) consecutive CTAs may share a tile's K
+// loop; the workspace holds bs_stream_k_workspace(num_sms) bytes (the same for every problem),
+// starts zero-filled and is left zero-filled by every call that completes.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms);
+bool bs_stream_k_pays(int64_t m_tiles_total, int64_t N, int64_t num_kb, int num_sms);
+size_t bs_stream_k_workspace(int num_sms);
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           const GroupTable& gt, int BN, int num_sms, cudaStream_t stream);
+                           const GroupTable& gt, int BN, int num_sms, void* workspace,
+                           cudaStream_t stream);
 
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
 // on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K].

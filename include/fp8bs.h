@@ -26,6 +26,7 @@
 #ifndef FP8BS_H
 #define FP8BS_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -131,6 +132,37 @@ FP8BS_API int fp8bs_gemm(const void* a, const float* a_s, const void* b, const f
 FP8BS_API int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b_s,
                             void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
                             unsigned int flags, void* stream);
+
+/*
+ * fp8bs_gemm_ws -- fp8bs_gemm_ex with a device workspace, which lets the library share the K
+ * loop of an output tile between SMs (stream-K) when whole tiles would leave SMs idle. Used
+ * for FP8BS_SCALE_UE8M0 with M > 128 (the block-scaled MMA) when the tiles do not fill the
+ * SMs evenly, e.g. the MLA projections M=2048, K=7168, N=1536 or 576; otherwise the call runs
+ * as fp8bs_gemm_ex. The partial sums of a shared tile are added in K order, so results do not
+ * depend on timing. ("DeepSeek-V3 Administrator & Developer Guide", §8.5.3, computed as in
+ * fp8bs_gemm; the pages' kernel has no split of K.)
+ *
+ *   workspace        device memory of at least fp8bs_gemm_workspace_size bytes, 16-byte
+ *                    aligned, owned by the caller. It must hold zeros before its first use;
+ *                    every call that completes without a device error leaves it that way (after
+ *                    a device error, fill it with zeros again). Calls that may run at the same
+ *                    time (on different streams) need different workspaces. NULL: no splitting.
+ *   workspace_bytes  its size in bytes; a non-NULL workspace smaller than
+ *                    fp8bs_gemm_workspace_size returns FP8BS_ERR_INVALID_ARG.
+ *   other arguments  as in fp8bs_gemm_ex.
+ */
+FP8BS_API int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, const float* b_s,
+                            void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                            unsigned int flags, void* workspace, size_t workspace_bytes,
+                            void* stream);
+
+/*
+ * fp8bs_gemm_workspace_size -- bytes of workspace fp8bs_gemm_ws uses on the current device: the
+ * same for every problem size (one 128 x 128 fp32 partial and one counter per SM, about 10 MB
+ * on 152 SMs).
+ *   bytes [out] host pointer receiving the size.
+ */
+FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
 
 /*
  * fp8bs_gemm_grouped -- several independent block-scaled GEMMs in one launch, one per group of

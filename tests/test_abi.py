@@ -138,3 +138,25 @@ def test_gemm_grouped_rejects_misaligned_and_null(lib):
 def test_gemm_ex_rejects_unknown_flags(lib):
     assert lib.fp8bs_gemm_ex(A16, B16, C16, B16, C16, 8, 256, 256, 0, 0x2, None) == INVALID
     assert lib.fp8bs_gemm_ex(None, None, None, None, None, 0, 256, 256, 0, 0x1, None) == OK
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, B16, C16, 8, 256, 200, 0, 0), INVALID),      # K % 128
+    ((A16, B16, C16, B16, C16, 8, 256, 256, 0, 0x2), INVALID),    # unknown flag
+    ((A16, B16, C16, B16, C16, -1, 256, 256, 0, 0), INVALID),
+    ((A16 + 8, B16, C16, B16, C16, 8, 256, 256, 0, 0), MISALIGNED),
+    ((None, None, None, None, None, 0, 256, 256, 1, 0), OK),
+])
+def test_gemm_ws_argument_checks(lib, args, expect):
+    """fp8bs_gemm_ws checks its arguments as fp8bs_gemm_ex does, with or without a workspace."""
+    for ws, nbytes in ((None, 0), (C16, 1 << 24)):
+        assert lib.fp8bs_gemm_ws(*args, ws, nbytes, None) == expect
+
+
+def test_gemm_workspace_size_without_a_gpu(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    out = ctypes.c_size_t(0)
+    assert lib.fp8bs_gemm_workspace_size(ctypes.byref(out)) in (CUDA, UNSUPPORTED)
+    assert lib.fp8bs_gemm_workspace_size(None) == INVALID

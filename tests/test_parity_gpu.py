@@ -411,6 +411,54 @@ def test_gemm_grouped_ue8m0_block_scaled(counts, N, K):
                   fmt="ue8m0")
 
 
+def run_gemm_ws(a_codes, a_s, b_codes, b_s, ws, fmt="ue8m0"):
+    c = fp8bs.fp8_gemm(dev_e4m3(a_codes), dev_f32(a_s), dev_e4m3(b_codes), dev_f32(b_s), fmt,
+                       workspace=ws)
+    torch.cuda.synchronize()
+    return host_bf16_f64(c)
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (256, 256, 1024),     # 4 tiles x 8 K blocks on 32 CTAs: every tile shared by 8 CTAs
+    (129, 200, 2048),     # ragged rows and columns
+    (300, 576, 2048),     # N tail inside the last 128-column tile
+    (1024, 1536, 4096),   # 96 tiles over all SMs, pieces of uneven length
+    (640, 384, 7168),
+])
+def test_gemm_ue8m0_stream_k_against_oracle(M, N, K):
+    """With a workspace the block-scaled GEMM shares tiles' K loops between CTAs; every output
+    element must still match the oracle, and repeated calls on the same workspace agree bit
+    for bit (the partials are added in a fixed order, and the workspace's counters return to
+    zero after each call)."""
+    a, a_s, b, b_s = pow2_case(M, N, K, M * 3 + N + K)
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
+    ref = oracle.gemm(a, a_s, b, b_s)
+    c1 = run_gemm_ws(a, a_s, b, b_s, ws)
+    assert_gemm_close(c1, ref, f"stream-K {M}x{N}x{K}")
+    c2 = run_gemm_ws(a, a_s, b, b_s, ws)
+    assert np.array_equal(c1, c2)
+    assert_gemm_close(run_gemm_ws(a, a_s, b, b_s, None), ref, f"no workspace {M}x{N}x{K}")
+
+
+def test_gemm_ue8m0_stream_k_workspace_reused_across_shapes():
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
+    for M, N, K in [(256, 256, 1024), (640, 384, 7168), (129, 200, 2048), (256, 256, 1024)]:
+        a, a_s, b, b_s = pow2_case(M, N, K, M + N)
+        assert_gemm_close(run_gemm_ws(a, a_s, b, b_s, ws), oracle.gemm(a, a_s, b, b_s),
+                          f"reused workspace {M}x{N}x{K}")
+
+
+def test_gemm_ws_rejects_a_short_workspace():
+    a, a_s, b, b_s = pow2_case(256, 256, 256, 3)
+    need = fp8bs.fp8bs_gemm_workspace_size()
+    ws = torch.zeros(need, dtype=torch.uint8, device="cuda")
+    c = torch.empty((256, 256), dtype=torch.bfloat16, device="cuda")
+    A, AS, B, BS = dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s)
+    with pytest.raises(fp8bs.Fp8bsError):
+        fp8bs.fp8bs_gemm_ws(A.data_ptr(), AS.data_ptr(), B.data_ptr(), BS.data_ptr(), c.data_ptr(),
+                            256, 256, 256, 1, 0, ws.data_ptr(), need - 1)
+
+
 def test_gemm_ue8m0_deterministic():
     a, a_s, b, b_s = pow2_case(512, 1024, 1024, 9)
     assert np.array_equal(run_gemm(a, a_s, b, b_s, "ue8m0"), run_gemm(a, a_s, b, b_s, "ue8m0"))
