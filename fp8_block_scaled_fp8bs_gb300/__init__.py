@@ -37,7 +37,8 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 GEMM_WEIGHTS_CONSTANT = 0x1
 EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_ex",
-           "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_grouped",
+           "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_noalloc",
+           "fp8bs_gemm_grouped",
            "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
 
 _lock = threading.Lock()
@@ -69,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_gemm_ws.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint, vp,
                                       ctypes.c_size_t, vp]
         lib.fp8bs_gemm_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+        lib.fp8bs_gemm_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint,
+                                           vp]
         lib.fp8bs_gemm_grouped.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
                                            i64, i64, i64, i32, vp]
         lib.fp8bs_status_string.argtypes = [i32]
@@ -110,6 +113,12 @@ def fp8bs_gemm_ws(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0, wor
                   workspace_bytes=0, stream=0) -> None:
     _check("fp8bs_gemm_ws", load().fp8bs_gemm_ws(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags,
                                                  workspace, workspace_bytes, stream))
+
+
+def fp8bs_gemm_noalloc(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0,
+                       stream=0) -> None:
+    _check("fp8bs_gemm_noalloc", load().fp8bs_gemm_noalloc(a, a_s, b, b_s, c, M, N, K,
+                                                           scale_fmt, flags, stream))
 
 
 def fp8bs_gemm_workspace_size() -> int:

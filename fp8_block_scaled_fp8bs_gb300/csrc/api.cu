@@ -197,6 +197,19 @@ int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, const float* b
                      stream);
 }
 
+int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b, const float* b_s,
+                       void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                       unsigned int flags, void* stream) {
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    void* ws = nullptr;
+    size_t bytes = 0;
+    const cudaError_t e = fp8bs::bs_static_workspace(sms, &ws, &bytes);
+    if (e == cudaErrorInvalidValue) return FP8BS_ERR_UNSUPPORTED_DEVICE;
+    if (e != cudaSuccess) return FP8BS_ERR_CUDA;
+    return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, ws, bytes, stream);
+}
+
 int fp8bs_gemm_workspace_size(size_t* bytes) {
     if (!bytes) return FP8BS_ERR_INVALID_ARG;
     int sms = 0;

@@ -36,6 +36,8 @@
 // so results do not depend on timing -- resets the flag and stores. It only waits on CTAs after it, each of which
 // writes its partial before anything else, and every CTA of the grid is resident (one per
 // SM), so the wait always ends.
+#include <atomic>
+
 #include "gemm_common.cuh"
 
 namespace fp8bs {
@@ -536,6 +538,34 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
         case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, workspace, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+// A stream-K workspace that needs no allocation: a file-scope device array, zero at module
+// load (every call that completes leaves its counters at zero again), big enough for devices
+// with up to kStaticWsSms SMs. Its address is looked up once per device.
+constexpr int kStaticWsSms = 160;
+constexpr size_t kStaticWsBytes = 256 * ((kStaticWsSms * sizeof(int) + 255) / 256) +
+                                  static_cast<size_t>(kStaticWsSms) * BM * 128 * sizeof(float);
+static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+
+cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes) {
+    constexpr int kMaxDevices = 64;
+    static std::atomic<void*> addr[kMaxDevices];
+    if (num_sms > kStaticWsSms || bs_stream_k_workspace(num_sms) > kStaticWsBytes)
+        return cudaErrorInvalidValue;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    void* p = addr[dev].load(std::memory_order_acquire);
+    if (!p) {
+        e = cudaGetSymbolAddress(&p, g_static_ws);
+        if (e != cudaSuccess) return e;
+        addr[dev].store(p, std::memory_order_release);
+    }
+    *ws = p;
+    *bytes = kStaticWsBytes;
+    return cudaSuccess;
 }
 
 cudaError_t read_error_bs(unsigned int* out, bool clear, cudaStream_t stream) {

@@ -77,6 +77,9 @@ size_t bs_stream_k_workspace(int num_sms);
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
                            const GroupTable& gt, int BN, int num_sms, void* workspace,
                            cudaStream_t stream);
+// The library's static stream-K workspace on the current device (no allocation); fails with
+// cudaErrorInvalidValue on a device with more SMs than it covers.
+cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes);
 
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
 // on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K].

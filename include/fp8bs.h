@@ -165,6 +165,22 @@ FP8BS_API int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, cons
 FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
 
 /*
+ * fp8bs_gemm_noalloc -- fp8bs_gemm_ws on a workspace that the library keeps in a static device
+ * array (about 10.5 MB per device, reserved when the library's device code is loaded): no
+ * memory is allocated by the caller or by the library at any time. The pages have no
+ * counterpart of this entry point: their fp8_gemm neither splits K nor uses scratch memory.
+ *
+ *   Arguments, results and accuracy as in fp8bs_gemm_ws.
+ *   Calls on one device share the one workspace: they must not run at the same time (issue
+ *   them on one stream, or order them).
+ *   A device with more than 160 SMs (more than the static workspace covers) returns
+ *   FP8BS_ERR_UNSUPPORTED_DEVICE without launching anything.
+ */
+FP8BS_API int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b, const float* b_s,
+                                 void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                                 unsigned int flags, void* stream);
+
+/*
  * fp8bs_gemm_grouped -- several independent block-scaled GEMMs in one launch, one per group of
  * rows of A: the MoE expert loop of "DeepSeek-V3 Administrator & Developer Guide", §6.4 MoE
  * expert routing (each local expert runs its Linear on the tokens routed to it), with every
