@@ -72,6 +72,48 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int b
 
 int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
 
+// Stream-K plans (see StreamKArgs in kernels.h). Whole tiles for all but the last one to two
+// waves, the rest shared; used when the busiest SM's K blocks (plus the hand-over of a partial)
+// drop clearly below the data-parallel schedule's ceil(tiles / SMs) whole tiles.
+fp8bs::StreamKArgs no_stream_k() { return fp8bs::StreamKArgs{nullptr, 0}; }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// The kernels count shared units (tiles x K blocks) in 32 bits.
+bool units_fit(int64_t tiles, int64_t num_kb) { return tiles * num_kb < INT32_MAX; }
+
+int dp_tiles_before_sharing(int64_t tiles, int sms) {
+    return tiles < 2 * sms ? 0 : static_cast<int>((tiles / sms - 1) * sms);
+}
+
+// fp32 scales (promotion kernel): the owner adds the other pieces' partials before its own
+// piece, which needs every CTA's range to span at least one tile (>= SMs tiles shared).
+fp8bs::StreamKArgs plan_stream_k_tn(int64_t tiles, int64_t num_kb, int sms, void* workspace) {
+    if (!workspace || tiles < sms || num_kb < 2 || !units_fit(tiles, num_kb)) return no_stream_k();
+    const int dp = dp_tiles_before_sharing(tiles, sms);
+    const int64_t cost_dp = ceil_div(tiles, sms) * num_kb;
+    const int64_t cost_sk = dp / sms * num_kb + ceil_div((tiles - dp) * num_kb, sms) + 2;
+    if (cost_sk * 100 >= cost_dp * 97) return no_stream_k();
+    return fp8bs::StreamKArgs{workspace, dp};
+}
+
+// ue8m0 scales (block-scaled kernel, 128-column tiles when shared). Measured: with ranges
+// shorter than a tile (fewer tiles than SMs) the hand-over of partials at the end costs more
+// than the balance gains (MLA N = 576: 24.0 us shared against 22.4 us whole), so tiles are only
+// shared when there are at least as many as SMs.
+fp8bs::StreamKArgs plan_stream_k_bs(int64_t m_tiles, int64_t N, int64_t num_kb, int sms,
+                                    void* workspace) {
+    if (!workspace || num_kb < 2) return no_stream_k();
+    const int bn_dp = fp8bs::pick_tile_n_bs(m_tiles, N, sms);
+    const int64_t cost_dp = ceil_div(m_tiles * ceil_div(N, bn_dp), sms) * num_kb;
+    const int64_t tiles = m_tiles * ceil_div(N, 128);
+    if (tiles < sms || !units_fit(tiles, num_kb)) return no_stream_k();
+    const int dp = dp_tiles_before_sharing(tiles, sms);
+    const int64_t cost_sk = dp / sms * num_kb + ceil_div((tiles - dp) * num_kb, sms) + 4;
+    if (cost_sk * 10 >= cost_dp * 9) return no_stream_k();
+    return fp8bs::StreamKArgs{workspace, dp};
+}
+
 // fp8bs_gemm_ex and fp8bs_gemm_ws: checks, then the kernel for the shape (see fp8bs.h).
 int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
               int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
@@ -98,7 +140,7 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
     if (int e = check_device(&sms)) return e;
     if (workspace) {
         if (!aligned16(workspace)) return FP8BS_ERR_MISALIGNED;
-        if (workspace_bytes < fp8bs::bs_stream_k_workspace(sms)) return FP8BS_ERR_INVALID_ARG;
+        if (workspace_bytes < fp8bs::stream_k_workspace(sms)) return FP8BS_ERR_INVALID_ARG;
     }
 
     GemmArgs g;
@@ -121,20 +163,21 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
     }
     const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
     const int64_t m_tiles = (M + 127) / 128;
-    // Stream-K (shared K loops) when a workspace is given and whole tiles would idle SMs.
-    const bool stream_k =
-        block_scaled && workspace && fp8bs::bs_stream_k_pays(m_tiles, N, K / 128, sms);
-    const int BN = stream_k       ? 128
-                   : block_scaled ? fp8bs::pick_tile_n_bs(m_tiles, N, sms)
-                                  : fp8bs::pick_tile_n(m_tiles, N, sms);
+    fp8bs::StreamKArgs ska;
+    int BN;
+    if (block_scaled) {
+        ska = plan_stream_k_bs(m_tiles, N, K / 128, sms, workspace);
+        BN = ska.workspace ? 128 : fp8bs::pick_tile_n_bs(m_tiles, N, sms);
+    } else {
+        BN = fp8bs::pick_tile_n(m_tiles, N, sms);
+        ska = plan_stream_k_tn(m_tiles * ceil_div(N, BN), K / 128, sms, workspace);
+    }
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
     const int64_t rows[2] = {0, M};
     fp8bs::GroupTable gt;
     fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), BN);
-    if (block_scaled)
-        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms,
-                                               stream_k ? workspace : nullptr, st));
-    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
+    if (block_scaled) return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, ska, st));
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, ska, st));
 }
 
 }  // namespace
@@ -214,7 +257,7 @@ int fp8bs_gemm_workspace_size(size_t* bytes) {
     if (!bytes) return FP8BS_ERR_INVALID_ARG;
     int sms = 0;
     if (int st = check_device(&sms)) return st;
-    *bytes = fp8bs::bs_stream_k_workspace(sms);
+    *bytes = fp8bs::stream_k_workspace(sms);
     return FP8BS_OK;
 }
 
@@ -266,8 +309,8 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
         return FP8BS_ERR_CUDA;
     if (block_scaled)
-        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, nullptr, st));
-    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, st));
+        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, no_stream_k(), st));
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, no_stream_k(), st));
 }
 
 int fp8bs_device_error(unsigned int* out, int clear, void* stream) {

@@ -73,92 +73,11 @@ __device__ __forceinline__ uint32_t ue8m0_code(float v, bool& ok) {
 
 __device__ __forceinline__ uint32_t splat4(uint32_t byte) { return byte * 0x01010101u; }
 
-// Stream-K workspace: `flags` one counter per CTA (partials published for the tile it owns),
-// then `parts`, one 128 x BN fp32 partial per CTA as float4 chunks [cta][chunk][row] (a warp's
-// 32 rows of one chunk are 512 contiguous bytes). The layout depends only on the SM count, so a
-// workspace serves every problem size. Both null in the data-parallel schedule.
-struct StreamK {
-    int* flags;
-    float4* parts;
-};
-
-// A CTA's pieces of work, in order: (tile, first K block, end K block).
-struct Sched {
-    int64_t u, u_end;   // stream-K: unit cursor and end of this CTA's range
-    int tile;           // data-parallel: next tile
-    bool sk;
-};
-
-__device__ __forceinline__ int64_t sk_range_start(int cta, int64_t units) {
-    return static_cast<int64_t>(cta) * units / gridDim.x;
-}
-
-// The CTA whose range holds unit x: the largest c with floor(c * units / grid) <= x.
-__device__ __forceinline__ int sk_owner(int64_t x, int64_t units) {
-    return static_cast<int>(((x + 1) * gridDim.x - 1) / units);
-}
-
-__device__ __forceinline__ Sched sched_begin(bool sk, int num_tiles, int num_kb) {
-    Sched s;
-    s.sk = sk;
-    s.tile = blockIdx.x;
-    const int64_t units = static_cast<int64_t>(num_tiles) * num_kb;
-    s.u = sk ? sk_range_start(blockIdx.x, units) : 0;
-    s.u_end = sk ? sk_range_start(blockIdx.x + 1, units) : 0;
-    return s;
-}
-
-__device__ __forceinline__ bool sched_next(Sched& s, int num_tiles, int num_kb, int& tile,
-                                           int& kb0, int& kb1) {
-    if (!s.sk) {
-        if (s.tile >= num_tiles) return false;
-        tile = s.tile;
-        kb0 = 0;
-        kb1 = num_kb;
-        s.tile += gridDim.x;
-        return true;
-    }
-    if (s.u >= s.u_end) return false;
-    tile = static_cast<int>(s.u / num_kb);
-    kb0 = static_cast<int>(s.u - static_cast<int64_t>(tile) * num_kb);
-    const int64_t left = s.u_end - s.u;
-    kb1 = left < num_kb - kb0 ? kb0 + static_cast<int>(left) : num_kb;
-    s.u += kb1 - kb0;
-    return true;
-}
-
 // Hand a TMEM accumulator back to the MMA issuer once this warp's loads of it have completed.
 __device__ __forceinline__ void release_tmem(uint64_t* tempty, int lane) {
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(tempty);
-}
-
-// The four epilogue warps (128 threads) only.
-__device__ __forceinline__ void epilogue_bar() {
-    asm volatile("bar.sync 1, 128;" ::: "memory");
-}
-
-__device__ __forceinline__ void flag_add_release(int* flag, int v) {
-    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ int flag_load_acquire(const int* flag) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    return v;
-}
-
-// Wait (bounded) until *flag == target.
-__device__ __forceinline__ bool flag_wait(const int* flag, int target) {
-    if (flag_load_acquire(flag) == target) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (true) {
-#pragma unroll 1
-        for (int i = 0; i < 16; ++i)
-            if (flag_load_acquire(flag) == target) return true;
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    }
 }
 
 template <int BN>
@@ -206,7 +125,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
 
-    Sched sched = sched_begin(stream_k, num_tiles, num_kb);
+    Sched sched = sched_begin(sk, num_tiles, num_kb);
     int tile, kb0, kb1;
 
     if (warp == PRODUCER) {
@@ -215,7 +134,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
+            while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
                 const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
                 const int b_row = t.g * g.N + t.n0;      // row of the stacked B
                 for (int kb = kb0; kb < kb1; ++kb) {
@@ -242,7 +161,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
             bool ok = true;
-            while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
+            while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
                 if (!mbar_wait(&ring.tempty[buf], tphase ^ 1)) {
                     record_error(FP8BS_DEVERR_MMA_WAIT);
                     break;
@@ -289,7 +208,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true, pow2 = true;
-        while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
+        while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
             const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
             // Rows past the group's end (clamped into A) are computed but never stored.
             const int row = min(t.m0 + warp * 32 + lane, g.M - 1);
@@ -342,11 +261,10 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
         const int quarter = warp & 3;
         const int row_in_tile = quarter * 32 + lane;
         const int epi_thread = row_in_tile;        // 0 .. 127
-        const int64_t units = static_cast<int64_t>(num_tiles) * num_kb;
         int buf = 0;
         uint32_t tphase = 0, part_phase = 0;
         bool ok = true;
-        while (ok && sched_next(sched, num_tiles, num_kb, tile, kb0, kb1)) {
+        while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
             const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
             const bool owner = kb0 == 0 && kb1 < num_kb;
             int parts = 0;
@@ -356,10 +274,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                 // it. While this CTA's own piece is still on the tensor cores, thread 0 waits
                 // for their partials and copies the first into shared memory; the outcome
                 // reaches the other epilogue threads through the word after the TMEM address.
-                const int64_t tile_end = static_cast<int64_t>(tile + 1) * num_kb;
-                for (int j = blockIdx.x + 1; j < static_cast<int>(gridDim.x) &&
-                                             sk_range_start(j, units) < tile_end; ++j)
-                    ++parts;
+                parts = sk_contributors(sk, tile, num_tiles, num_kb);
                 volatile uint32_t* outcome = ring.tmem_holder + 1;
                 if (epi_thread == 0) {
                     got = flag_wait(sk.flags + blockIdx.x, parts);
@@ -378,7 +293,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     }
                     *outcome = got ? 1u : 0u;
                 }
-                epilogue_bar();
+                epilogue_bar<128>();
                 got = *outcome != 0;
             }
             if (!warp_wait(&ring.tfull[buf], tphase)) {
@@ -419,10 +334,10 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]));
                 }
                 release_tmem(&ring.tempty[buf], lane);
-                epilogue_bar();
+                epilogue_bar<128>();
                 if (epi_thread == 0) {
                     __threadfence();
-                    flag_add_release(sk.flags + sk_owner(static_cast<int64_t>(tile) * num_kb, units), 1);
+                    flag_add_release(sk.flags + sk_tile_owner(sk, tile, num_tiles, num_kb), 1);
                 }
             } else {
                 // The tile's first piece: per 32 columns, add the partials of the pieces that
@@ -474,35 +389,25 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     if (warp == ISSUER) tmem_dealloc(tmem_base, tmem_cols);
 }
 
-size_t bs_flag_bytes(int num_sms) {
-    return (static_cast<size_t>(num_sms) * sizeof(int) + 255) & ~size_t(255);
-}
-
 template <int BN>
 cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                      const GroupTable& gt, int num_sms, void* workspace, cudaStream_t stream) {
+                      const GroupTable& gt, int num_sms, const StreamKArgs& ska,
+                      cudaStream_t stream) {
     using Cfg = BsCfg<BN>;
     int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
     static_assert(bs_tmem_cols<BN>(kMaxStages) <= 512, "TMEM holds 512 columns");
     // Stream-K keeps one partial tile (and its barrier) in shared memory, at two stages' cost.
-    const int part_bytes = workspace ? Cfg::PART + 16 : 0;
-    if (workspace) stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages) - part_bytes) / Cfg::STAGE;
+    const int part_bytes = ska.workspace ? Cfg::PART + 16 : 0;
+    if (ska.workspace)
+        stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages) - part_bytes) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
     const int smem = 1024 + stages * Cfg::STAGE + part_bytes + ring_bytes(stages);
     cudaError_t e = set_smem(gemm_bs_kernel<BN>, kSmemLimit);
     if (e != cudaSuccess) return e;
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
-    StreamK sk = {nullptr, nullptr};
-    int grid = tiles < num_sms ? tiles : num_sms;
-    if (workspace) {
-        // Every CTA gets a nonempty range of units (there are at least as many as CTAs).
-        const int64_t units = static_cast<int64_t>(tiles) * (g.K / BK);
-        grid = units < num_sms ? static_cast<int>(units) : num_sms;
-        sk.flags = static_cast<int*>(workspace);
-        sk.parts = reinterpret_cast<float4*>(static_cast<char*>(workspace) +
-                                             bs_flag_bytes(num_sms));
-    }
+    StreamK sk = {nullptr, nullptr, 0};
+    const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
     return launch_pdl(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, tmA, tmB, g, gt,
                       stages, sk);
 }
@@ -513,29 +418,12 @@ int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
     return m_tiles_total * ((N + 127) / 128) * 5 >= num_sms * 4 ? 128 : 64;
 }
 
-// Stream-K pays when whole tiles would leave SMs idle for a large part of the run: compare
-// the K blocks the busiest SM works through (plus about four K blocks' worth for writing and
-// adding a partial) with the data-parallel schedule's, which runs ceil(tiles / SMs) whole tiles.
-bool bs_stream_k_pays(int64_t m_tiles_total, int64_t N, int64_t num_kb, int num_sms) {
-    if (num_kb < 2) return false;
-    const int bn_dp = pick_tile_n_bs(m_tiles_total, N, num_sms);
-    const int64_t tiles_dp = m_tiles_total * ((N + bn_dp - 1) / bn_dp);
-    const int64_t cost_dp = (tiles_dp + num_sms - 1) / num_sms * num_kb;
-    const int64_t units = m_tiles_total * ((N + 127) / 128) * num_kb;
-    const int64_t cost_sk = (units + num_sms - 1) / num_sms + 4;
-    return cost_sk * 10 < cost_dp * 9;
-}
-
-size_t bs_stream_k_workspace(int num_sms) {
-    return bs_flag_bytes(num_sms) + static_cast<size_t>(num_sms) * BM * 128 * sizeof(float);
-}
-
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           const GroupTable& gt, int BN, int num_sms, void* workspace,
+                           const GroupTable& gt, int BN, int num_sms, const StreamKArgs& ska,
                            cudaStream_t stream) {
     switch (BN) {
-        case 64: return launch_bs<64>(tmA, tmB, g, gt, num_sms, workspace, stream);
-        case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, workspace, stream);
+        case 64: return launch_bs<64>(tmA, tmB, g, gt, num_sms, ska, stream);
+        case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, ska, stream);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -544,14 +432,13 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 // load (every call that completes leaves its counters at zero again), big enough for devices
 // with up to kStaticWsSms SMs. Its address is looked up once per device.
 constexpr int kStaticWsSms = 160;
-constexpr size_t kStaticWsBytes = 256 * ((kStaticWsSms * sizeof(int) + 255) / 256) +
-                                  static_cast<size_t>(kStaticWsSms) * BM * 128 * sizeof(float);
+constexpr size_t kStaticWsBytes = stream_k_workspace(kStaticWsSms);
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
 
 cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes) {
     constexpr int kMaxDevices = 64;
     static std::atomic<void*> addr[kMaxDevices];
-    if (num_sms > kStaticWsSms || bs_stream_k_workspace(num_sms) > kStaticWsBytes)
+    if (num_sms > kStaticWsSms || stream_k_workspace(num_sms) > kStaticWsBytes)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);

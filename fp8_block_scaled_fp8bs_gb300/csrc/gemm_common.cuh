@@ -178,6 +178,158 @@ cudaError_t set_smem(K kernel, int bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
 }
 
+// ------------------------------------------------------------------ work schedule (stream-K)
+//
+// A CTA works through pieces (tile, first K block, end K block). Data-parallel tiles come
+// first: CTA c takes tiles c, c + gridDim.x, ... below `dp_tiles`, each whole. The remaining
+// tiles x K blocks "units" are cut into gridDim.x equal contiguous ranges, one per CTA, which
+// each CTA works through tile by tile, so a tile's K loop may be shared by consecutive CTAs.
+// Only a CTA's first shared piece can start inside a tile. That CTA writes its fp32 partial to
+// its own workspace slot and counts it in the flag of the tile's owner, the CTA holding the
+// tile's first K blocks (the last piece of its own range), which adds the partials in a fixed
+// order -- results do not depend on timing -- resets its flag and stores the tile. The owner
+// only waits on CTAs after it, each of which writes its partial before its other pieces, and
+// every CTA of the grid is resident (one per SM), so the wait always ends.
+struct StreamK {
+    int* flags;       // [gridDim.x] partials published for the tile each CTA owns
+    float4* parts;    // [gridDim.x][BN/4][128]: a CTA's partial, float4 of columns x rows
+    int dp_tiles;     // tiles computed whole before the shared ones (a multiple of gridDim.x)
+};
+
+struct Sched {
+    int tile;           // next data-parallel tile
+    int dp_tiles;
+    int u, u_end;       // shared units (fewer than 2^31): cursor and end of this CTA's range
+};
+
+// Start of CTA `cta`'s range of the `units` shared units.
+__device__ __forceinline__ int64_t sk_range_start(int cta, int64_t units) {
+    return static_cast<int64_t>(cta) * units / gridDim.x;
+}
+
+// The CTA whose range holds shared unit x: the largest c with floor(c * units / grid) <= x.
+__device__ __forceinline__ int sk_owner(int64_t x, int64_t units) {
+    return static_cast<int>(((x + 1) * gridDim.x - 1) / units);
+}
+
+__device__ __forceinline__ int64_t sk_units(const StreamK& sk, int num_tiles, int num_kb) {
+    return sk.parts ? static_cast<int64_t>(num_tiles - sk.dp_tiles) * num_kb : 0;
+}
+
+__device__ __forceinline__ Sched sched_begin(const StreamK& sk, int num_tiles, int num_kb) {
+    Sched s;
+    s.tile = blockIdx.x;
+    s.dp_tiles = sk.parts ? sk.dp_tiles : num_tiles;
+    const int64_t units = sk_units(sk, num_tiles, num_kb);
+    s.u = sk.parts ? static_cast<int>(sk_range_start(blockIdx.x, units)) : 0;
+    s.u_end = sk.parts ? static_cast<int>(sk_range_start(blockIdx.x + 1, units)) : 0;
+    return s;
+}
+
+__device__ __forceinline__ bool sched_next(Sched& s, int num_kb, int& tile, int& kb0, int& kb1) {
+    if (s.tile < s.dp_tiles) {
+        tile = s.tile;
+        kb0 = 0;
+        kb1 = num_kb;
+        s.tile += gridDim.x;
+        return true;
+    }
+    if (s.u >= s.u_end) return false;
+    const int rel = s.u / num_kb;
+    tile = s.dp_tiles + rel;
+    kb0 = s.u - rel * num_kb;
+    const int left = s.u_end - s.u;
+    kb1 = left < num_kb - kb0 ? kb0 + left : num_kb;
+    s.u += kb1 - kb0;
+    return true;
+}
+
+// Piece p of this CTA's sequence (the same sequence as sched_next), computed from p alone.
+__device__ __forceinline__ bool piece_at(const StreamK& sk, int p, int num_tiles, int num_kb,
+                                         int& tile, int& kb0, int& kb1) {
+    const int dp_tiles = sk.parts ? sk.dp_tiles : num_tiles;
+    const int n_dp = blockIdx.x < dp_tiles ? (dp_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+    if (p < n_dp) {
+        tile = blockIdx.x + p * gridDim.x;
+        kb0 = 0;
+        kb1 = num_kb;
+        return true;
+    }
+    if (!sk.parts) return false;
+    const int64_t units = sk_units(sk, num_tiles, num_kb);
+    const int u0 = static_cast<int>(sk_range_start(blockIdx.x, units));
+    const int u_end = static_cast<int>(sk_range_start(blockIdx.x + 1, units));
+    const int q = p - n_dp;
+    const int rel = u0 / num_kb + q;
+    const int start = q == 0 ? u0 : rel * num_kb;
+    if (start >= u_end) return false;
+    tile = dp_tiles + rel;
+    kb0 = start - rel * num_kb;
+    kb1 = min(num_kb, u_end - rel * num_kb);
+    return true;
+}
+
+// Number of CTAs after this one whose ranges start inside shared tile `tile` (this CTA owns
+// it: its range holds the tile's first K block).
+__device__ __forceinline__ int sk_contributors(const StreamK& sk, int tile, int num_tiles,
+                                               int num_kb) {
+    const int64_t units = sk_units(sk, num_tiles, num_kb);
+    const int64_t tile_end = static_cast<int64_t>(tile - sk.dp_tiles + 1) * num_kb;
+    int n = 0;
+    for (int j = blockIdx.x + 1; j < static_cast<int>(gridDim.x) &&
+                                 sk_range_start(j, units) < tile_end; ++j)
+        ++n;
+    return n;
+}
+
+// The owner of shared tile `tile`.
+__device__ __forceinline__ int sk_tile_owner(const StreamK& sk, int tile, int num_tiles,
+                                             int num_kb) {
+    return sk_owner(static_cast<int64_t>(tile - sk.dp_tiles) * num_kb,
+                    sk_units(sk, num_tiles, num_kb));
+}
+
+__device__ __forceinline__ void flag_add_release(int* flag, int v) {
+    asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(flag), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int flag_load_acquire(const int* flag) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    return v;
+}
+
+// Wait (bounded) until *flag == target.
+__device__ __forceinline__ bool flag_wait(const int* flag, int target) {
+    if (flag_load_acquire(flag) == target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 16; ++i)
+            if (flag_load_acquire(flag) == target) return true;
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+
+// Named barrier 1 among `threads` threads (the epilogue warps of a kernel).
+template <int threads>
+__device__ __forceinline__ void epilogue_bar() {
+    asm volatile("bar.sync 1, %0;" ::"n"(threads) : "memory");
+}
+
+// Host: grid size and kernel parameter for a stream-K plan (see StreamKArgs in kernels.h).
+inline int stream_k_grid(const StreamKArgs& ska, int tiles, int num_kb, int num_sms,
+                         StreamK* sk) {
+    if (!ska.workspace) return tiles < num_sms ? tiles : num_sms;
+    const int64_t units = static_cast<int64_t>(tiles - ska.dp_tiles) * num_kb;
+    const int grid = ska.dp_tiles > 0 || units >= num_sms ? num_sms : static_cast<int>(units);
+    sk->flags = static_cast<int*>(ska.workspace);
+    sk->parts = reinterpret_cast<float4*>(static_cast<char*>(ska.workspace) +
+                                          stream_k_flag_bytes(num_sms));
+    sk->dp_tiles = ska.dp_tiles;
+    return grid;
+}
+
 // Read (and, if `clear`, reset) this translation unit's error word; enqueued on `stream`.
 inline cudaError_t read_tu_error(unsigned int* out, bool clear, cudaStream_t stream) {
     cudaError_t e = cudaMemcpyFromSymbolAsync(out, g_device_error, sizeof(unsigned int), 0,

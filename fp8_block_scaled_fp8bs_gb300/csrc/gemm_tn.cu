@@ -14,22 +14,6 @@ namespace fp8bs {
 
 namespace {
 
-// Scales of four consecutive K blocks starting at block k (k a multiple of 4): one 16-byte
-// load when the row is 16-byte aligned and holds whole groups of four, else scalar loads.
-__device__ __forceinline__ float4 load_scales4(const float* row, int k, int n, bool vec) {
-    if (vec && k + 4 <= n) return __ldg(reinterpret_cast<const float4*>(row + k));
-    float4 r;
-    r.x = k < n ? __ldg(row + k) : 0.0f;
-    r.y = k + 1 < n ? __ldg(row + k + 1) : 0.0f;
-    r.z = k + 2 < n ? __ldg(row + k + 2) : 0.0f;
-    r.w = k + 3 < n ? __ldg(row + k + 3) : 0.0f;
-    return r;
-}
-
-__device__ __forceinline__ float pick4(const float4& v, int j) {
-    return j == 0 ? v.x : j == 1 ? v.y : j == 2 ? v.z : v.w;
-}
-
 // Tile = 128 rows of A x BN columns of B (BN = 64, 128 or 256). Warp layout (whole
 // warpgroups, so that register budgets can be moved between them):
 //   warps 0 .. 7     promotion/epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 and the
@@ -49,7 +33,14 @@ struct TnCfg {
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * BN);
-    static constexpr bool SPLIT_REGS = (BN == 256);
+    static constexpr int NCH = CW / 32;                       // 32-column TMEM chunks per thread
+    // Up to two chunks fit in registers next to the accumulator: they are loaded together
+    // and the buffer is handed back after one TMEM round trip. With three or four the chunks
+    // are loaded one after another, each while the previous one is folded in.
+    static constexpr bool LOAD_ALL = NCH <= 2;
+    // With BN = 192 a thread's 96 columns may span two 128-row blocks of B (at a chunk edge).
+    static constexpr bool TWO_B = (BN % 128) != 0 && CW > 64;
+    static constexpr bool SPLIT_REGS = (BN >= 192);
     static constexpr uint32_t kCtlRegs = 40;
     static constexpr uint32_t kEpiRegs = 232;
     static_assert(!SPLIT_REGS || 4 * 32 * kCtlRegs + 8 * 32 * kEpiRegs <= 384 * 168,
@@ -59,7 +50,8 @@ struct TnCfg {
 template <int BN>
 __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     gemm_tn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmArgs g, const __grid_constant__ GroupTable gt, const int stages) {
+                   const GemmArgs g, const __grid_constant__ GroupTable gt, const int stages,
+                   const StreamK sk) {
     using Cfg = TnCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -88,6 +80,9 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
 
+    Sched sched = sched_begin(sk, num_tiles, num_kb);
+    int tile, kb0, kb1;
+
     if (warp >= Cfg::EPI_WARPS) {
         if constexpr (Cfg::SPLIT_REGS) regs_dec<Cfg::kCtlRegs>();
         if (warp == PRODUCER && lane == 0) {
@@ -95,10 +90,10 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
             uint32_t phase = 0;
             int64_t issued = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
                 const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
                 const int b_row = t.g * g.N + t.n0;      // row of the stacked B
-                for (int kb = 0; kb < num_kb; ++kb) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
                         record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                         ok = false;
@@ -120,8 +115,8 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                for (int kb = 0; kb < num_kb; ++kb) {
+            while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
+                for (int kb = kb0; kb < kb1; ++kb) {
                     if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
                         !mbar_wait(&ring.full[stage], phase)) {
                         record_error(FP8BS_DEVERR_MMA_WAIT);
@@ -157,36 +152,102 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
         const int col0 = (warp >> 2) * Cfg::CW;
         const int row_in_tile = quarter * 32 + lane;
         const int nb_count = (g.N + 127) / 128;
-        const bool vec_scales = (num_kb % 4 == 0) &&
-                                ((reinterpret_cast<uintptr_t>(g.a_s) & 15u) == 0) &&
-                                ((reinterpret_cast<uintptr_t>(g.b_s) & 15u) == 0);
+        constexpr int EPI_THREADS = 32 * Cfg::EPI_WARPS;
         int buf = 0;
         uint32_t tphase = 0;
+        // Pieces are recomputed from their index (piece_at), so that only the index and the K
+        // end stay live through the K loop: these warps are at their register limit.
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        for (int p = 0; ok; ++p) {
+            int tile, kb0, kb1;
+            if (!piece_at(sk, p, num_tiles, num_kb, tile, kb0, kb1)) break;
             const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
             const int n0 = t.n0;
             const int row = t.m0 + row_in_tile;
             const int nb = min((n0 + col0) / 128, nb_count - 1);
+            const int nb2 = min((n0 + col0 + Cfg::CW - 1) / 128, nb_count - 1);
             const float* as_row = g.a_s + static_cast<int64_t>(min(row, g.M - 1)) * num_kb;
             const float* bs_row =
                 g.b_s + (static_cast<int64_t>(t.g) * nb_count + nb) * num_kb;
+            const float* bs_row2 =
+                g.b_s + (static_cast<int64_t>(t.g) * nb_count + nb2) * num_kb;
+            // This thread's float4s of a partial tile in a stream-K slot: columns col0 .. col0+CW-1
+            // of row row_in_tile, at [col / 4][row].
+            const int part_base = (col0 / 4) * BM + row_in_tile;
             float acc[Cfg::CW];
 #pragma unroll
             for (int i = 0; i < Cfg::CW; ++i) acc[i] = 0.0f;
-            // Scales in groups of four K blocks, the next group in flight.
-            float4 a_cur = load_scales4(as_row, 0, num_kb, vec_scales);
-            float4 b_cur = load_scales4(bs_row, 0, num_kb, vec_scales);
-            float4 a_nxt = load_scales4(as_row, 4, num_kb, vec_scales);
-            float4 b_nxt = load_scales4(bs_row, 4, num_kb, vec_scales);
-            for (int kb = 0; kb < num_kb; ++kb) {
-                const int j = kb & 3;
-                const float sc = pick4(a_cur, j) * pick4(b_cur, j);
-                if (j == 3) {
-                    a_cur = a_nxt;
-                    b_cur = b_nxt;
-                    a_nxt = load_scales4(as_row, kb + 5, num_kb, vec_scales);
-                    b_nxt = load_scales4(bs_row, kb + 5, num_kb, vec_scales);
+            if (kb0 == 0 && kb1 < num_kb) {
+                // This CTA owns a shared tile: the pieces after its own are computed first by
+                // the next CTAs (their ranges are at least a tile long, so they are done by
+                // now); start from the sum of their partials.
+                const int parts = sk_contributors(sk, tile, num_tiles, num_kb);
+                volatile uint32_t* outcome = ring.tmem_holder + 1;
+                if (threadIdx.x == 0) {
+                    const bool got = flag_wait(sk.flags + blockIdx.x, parts);
+                    if (got) {
+                        sk.flags[blockIdx.x] = 0;        // ready for the next call
+                    } else {
+                        record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                    }
+                    *outcome = got ? 1u : 0u;
+                }
+                epilogue_bar<EPI_THREADS>();
+                if (*outcome == 0) {
+                    ok = false;
+                    break;
+                }
+                // The first partial goes straight into the (zero) accumulator; any further ones
+                // (a tile shared by three or more CTAs) are added 8 float4 at a time.
+                const float4* slot1 = sk.parts + static_cast<int64_t>(blockIdx.x + 1) * (BN / 4) * BM;
+#pragma unroll
+                for (int i = 0; i < Cfg::CW / 4; ++i) {
+                    const float4 p = __ldcg(slot1 + part_base + i * BM);
+                    acc[4 * i] = p.x;
+                    acc[4 * i + 1] = p.y;
+                    acc[4 * i + 2] = p.z;
+                    acc[4 * i + 3] = p.w;
+                }
+#pragma unroll 1
+                for (int j = 2; j <= parts; ++j) {
+                    const float4* slot = sk.parts + static_cast<int64_t>(blockIdx.x + j) * (BN / 4) * BM;
+#pragma unroll
+                    for (int i0 = 0; i0 < Cfg::CW / 4; i0 += 8) {
+                        float4 p[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) p[i] = __ldcg(slot + part_base + (i0 + i) * BM);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            acc[4 * (i0 + i)] += p[i].x;
+                            acc[4 * (i0 + i) + 1] += p[i].y;
+                            acc[4 * (i0 + i) + 2] += p[i].z;
+                            acc[4 * (i0 + i) + 3] += p[i].w;
+                        }
+                        asm volatile("" ::: "memory");   // keep the next chunk's loads here
+                    }
+                }
+            }
+            // Scales of K blocks kb and kb+1 in registers, kb+2 requested as kb is consumed (the
+            // scale arrays stay in L2; two blocks of MMA time hide the load).
+            float sa0 = 0.f, sa1 = 0.f, sb0 = 0.f, sb1 = 0.f, sbb0 = 0.f, sbb1 = 0.f;
+            sa0 = __ldg(as_row + kb0);
+            sb0 = __ldg(bs_row + kb0);
+            if constexpr (Cfg::TWO_B) sbb0 = __ldg(bs_row2 + kb0);
+            if (kb0 + 1 < kb1) {
+                sa1 = __ldg(as_row + kb0 + 1);
+                sb1 = __ldg(bs_row + kb0 + 1);
+                if constexpr (Cfg::TWO_B) sbb1 = __ldg(bs_row2 + kb0 + 1);
+            }
+            for (int kb = kb0; kb < kb1; ++kb) {
+                const float sc = sa0 * sb0;
+                const float sc2 = Cfg::TWO_B ? sa0 * sbb0 : sc;
+                sa0 = sa1;
+                sb0 = sb1;
+                sbb0 = sbb1;
+                if (kb + 2 < kb1) {
+                    sa1 = __ldg(as_row + kb + 2);
+                    sb1 = __ldg(bs_row + kb + 2);
+                    if constexpr (Cfg::TWO_B) sbb1 = __ldg(bs_row2 + kb + 2);
                 }
                 if (!warp_wait(&ring.tfull[buf], tphase)) {
                     if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
@@ -196,35 +257,73 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                 tc_fence_after();
                 const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                        static_cast<uint32_t>(buf * BN + col0);
-                // Four chunks of 32 columns: the load of chunk c+1 is in flight while chunk c is
-                // folded in; the buffer is handed back as soon as the last chunk has landed.
-                float va[32], vb[32];
-                tmem_ld_32cols(taddr, va);
-                tmem_wait_ld_32(va);
+                if constexpr (Cfg::LOAD_ALL) {
+                    // All chunks in flight at once; the buffer goes back after one round trip.
+                    float v[Cfg::CW];
 #pragma unroll
-                for (int c = 0; c < Cfg::CW / 32; ++c) {
-                    float* cur = (c & 1) ? vb : va;
-                    float* nxt = (c & 1) ? va : vb;
-                    if (c + 1 < Cfg::CW / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
-                    if (c + 1 == Cfg::CW / 32) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&ring.tempty[buf]);
-                    }
-                    // Packed fp32x2 FMAs (round-to-nearest per component): half the issue slots.
+                    for (int c = 0; c < Cfg::NCH; ++c) tmem_ld_32cols(taddr + 32 * c, v + 32 * c);
 #pragma unroll
-                    for (int i = 0; i < 32; i += 2) {
-                        const float2 r = __ffma2_rn(make_float2(cur[i], cur[i + 1]), make_float2(sc, sc),
-                                                    make_float2(acc[c * 32 + i], acc[c * 32 + i + 1]));
-                        acc[c * 32 + i] = r.x;
-                        acc[c * 32 + i + 1] = r.y;
+                    for (int c = 0; c < Cfg::NCH; ++c) tmem_wait_ld_32(v + 32 * c);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+#pragma unroll
+                    for (int c = 0; c < Cfg::NCH; ++c) {
+                        // the chunk's 128-row block of B: the thread's first, or the next one
+                        const float s_c =
+                            Cfg::TWO_B && min((n0 + col0 + 32 * c) / 128, nb_count - 1) != nb
+                                ? sc2
+                                : sc;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            fma2_into(acc + 32 * c + i, v[32 * c + i], v[32 * c + i + 1], s_c, s_c);
                     }
-                    if (c + 1 < Cfg::CW / 32) tmem_wait_ld_32(nxt);
+                } else {
+                    // Chunks of 32 columns: the load of chunk c+1 is in flight while chunk c is
+                    // folded in; the buffer is handed back as soon as the last chunk has landed.
+                    float va[32], vb[32];
+                    tmem_ld_32cols(taddr, va);
+                    tmem_wait_ld_32(va);
+#pragma unroll
+                    for (int c = 0; c < Cfg::NCH; ++c) {
+                        float* cur = (c & 1) ? vb : va;
+                        float* nxt = (c & 1) ? va : vb;
+                        if (c + 1 < Cfg::NCH) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+                        if (c + 1 == Cfg::NCH) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                        }
+                        const float s_c =
+                            Cfg::TWO_B && min((n0 + col0 + 32 * c) / 128, nb_count - 1) != nb
+                                ? sc2
+                                : sc;
+                        // Packed fp32x2 FMAs (round-to-nearest per component).
+#pragma unroll
+                        for (int i = 0; i < 32; i += 2)
+                            fma2_into(acc + 32 * c + i, cur[i], cur[i + 1], s_c, s_c);
+                        if (c + 1 < Cfg::NCH) tmem_wait_ld_32(nxt);
+                    }
                 }
                 buf ^= 1;
                 if (buf == 0) tphase ^= 1;
             }
             if (!ok) break;
+            if (kb0 > 0) {
+                // A piece that does not start its tile: publish the partial in this CTA's slot
+                // and count it in the flag of the tile's owner.
+                float4* slot = sk.parts + static_cast<int64_t>(blockIdx.x) * (BN / 4) * BM;
+#pragma unroll
+                for (int i = 0; i < Cfg::CW / 4; ++i)
+                    __stcg(slot + part_base + i * BM,
+                           make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2], acc[4 * i + 3]));
+                epilogue_bar<EPI_THREADS>();
+                if (threadIdx.x == 0) {
+                    __threadfence();
+                    flag_add_release(sk.flags + sk_tile_owner(sk, tile, num_tiles, num_kb), 1);
+                }
+                continue;
+            }
             if (row < t.row_end) {
                 __nv_bfloat16* crow = static_cast<__nv_bfloat16*>(g.c) +
                                       static_cast<int64_t>(row) * g.N + n0 + col0;
@@ -258,7 +357,8 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
 
 template <int BN>
 cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                      const GroupTable& gt, int num_sms, cudaStream_t stream) {
+                      const GroupTable& gt, int num_sms, const StreamKArgs& ska,
+                      cudaStream_t stream) {
     using Cfg = TnCfg<BN>;
     int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
@@ -267,17 +367,30 @@ cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     if (e != cudaSuccess) return e;
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
-    const int grid = tiles < num_sms ? tiles : num_sms;
+    StreamK sk = {nullptr, nullptr, 0};
+    const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
     return launch_pdl(gemm_tn_kernel<BN>, grid, Cfg::THREADS, smem, stream, tmA, tmB, g, gt,
-                      stages);
+                      stages, sk);
 }
 
 }  // namespace
 
+// Relative time of one K block of a 128 x BN tile, measured on GB300 at prefill shapes (745,
+// 960 and 1050 clk for BN = 128, 192 and 256); BN = 64 from the N = 64 MMA rate.
 int pick_tile_n(int64_t m_tiles_total, int64_t N, int num_sms) {
-    if (m_tiles_total * ((N + 255) / 256) >= num_sms) return 256;
-    if (m_tiles_total * ((N + 127) / 128) * 5 >= num_sms * 4) return 128;
-    return 64;
+    static const int kWidth[4] = {256, 192, 128, 64};
+    static const int kCost[4] = {141, 129, 100, 80};
+    int best = 256;
+    int64_t best_cost = INT64_MAX;
+    for (int i = 0; i < 4; ++i) {
+        const int64_t tiles = m_tiles_total * ((N + kWidth[i] - 1) / kWidth[i]);
+        const int64_t cost = (tiles + num_sms - 1) / num_sms * kCost[i];
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = kWidth[i];
+        }
+    }
+    return best;
 }
 
 void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N, int bn) {
@@ -293,11 +406,13 @@ void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N,
 }
 
 cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           const GroupTable& gt, int BN, int num_sms, cudaStream_t stream) {
+                           const GroupTable& gt, int BN, int num_sms, const StreamKArgs& ska,
+                           cudaStream_t stream) {
     switch (BN) {
-        case 64: return launch_tn<64>(tmA, tmB, g, gt, num_sms, stream);
-        case 128: return launch_tn<128>(tmA, tmB, g, gt, num_sms, stream);
-        case 256: return launch_tn<256>(tmA, tmB, g, gt, num_sms, stream);
+        case 64: return launch_tn<64>(tmA, tmB, g, gt, num_sms, ska, stream);
+        case 128: return launch_tn<128>(tmA, tmB, g, gt, num_sms, ska, stream);
+        case 192: return launch_tn<192>(tmA, tmB, g, gt, num_sms, ska, stream);
+        case 256: return launch_tn<256>(tmA, tmB, g, gt, num_sms, ska, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -56,26 +56,42 @@ struct GroupTable {
 // Tiles of 128 rows and `bn` columns for the given group row offsets (host-side helper).
 void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N, int bn);
 
-// Tile width for the normal orientation: the widest of 256, 128, 64 columns whose tile count
-// still keeps the SMs busy (wider tiles re-read A less often; narrower ones fill more SMs).
+// Stream-K schedule of the normal-orientation kernels: a workspace (null: every tile computed
+// whole by one CTA) and the number of tiles computed whole before the rest are shared (a
+// multiple of the grid, which is then the SM count; 0 shares every tile). See gemm_common.cuh.
+struct StreamKArgs {
+    void* workspace;
+    int dp_tiles;
+};
+
+// Workspace layout: one int counter per SM (rounded up to 256 bytes), then one 128 x 256 fp32
+// partial tile per SM -- the same for every problem size. It starts zero-filled and every call
+// that completes leaves the counters at zero.
+constexpr size_t stream_k_flag_bytes(int num_sms) {
+    return (static_cast<size_t>(num_sms) * sizeof(int) + 255) / 256 * 256;
+}
+constexpr size_t stream_k_workspace(int num_sms) {
+    return stream_k_flag_bytes(num_sms) + static_cast<size_t>(num_sms) * 128 * 256 * sizeof(float);
+}
+
+// Tile width for the normal orientation with fp32 scales: the one of 256, 192, 128 and 64
+// columns that minimises rounds of tiles x measured time per tile.
 int pick_tile_n(int64_t m_tiles_total, int64_t N, int num_sms);
 
-// Normal orientation: 128-row tiles of A on the MMA's M side, BN columns of B on its N side.
-// tmA: box {128, 128} over A [rows, K]; tmB: box {128, BN} over B [groups*N, K].
+// Normal orientation: 128-row tiles of A on the MMA's M side, BN (64, 128, 192 or 256)
+// columns of B on its N side. tmA: box {128, 128} over A [rows, K]; tmB: box {128, BN} over B
+// [groups*N, K].
 cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           const GroupTable& gt, int BN, int num_sms, cudaStream_t stream);
+                           const GroupTable& gt, int BN, int num_sms, const StreamKArgs& ska,
+                           cudaStream_t stream);
 
 // Block-scaled orientation, for scales that are all powers of two (FP8BS_SCALE_UE8M0): the
 // tensor core applies a_s and b_s as ue8m0 exponents per K block; tiles of 128 rows x BN
-// (64 or 128) columns, same maps and group table as launch_gemm_tn.
-// With a workspace (stream-K schedule, BN = 128 only) consecutive CTAs may share a tile's K
-// loop; the workspace holds bs_stream_k_workspace(num_sms) bytes (the same for every problem),
-// starts zero-filled and is left zero-filled by every call that completes.
+// (64 or 128; 128 when K loops are shared) columns, same maps and group table as
+// launch_gemm_tn.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms);
-bool bs_stream_k_pays(int64_t m_tiles_total, int64_t N, int64_t num_kb, int num_sms);
-size_t bs_stream_k_workspace(int num_sms);
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
-                           const GroupTable& gt, int BN, int num_sms, void* workspace,
+                           const GroupTable& gt, int BN, int num_sms, const StreamKArgs& ska,
                            cudaStream_t stream);
 // The library's static stream-K workspace on the current device (no allocation); fails with
 // cudaErrorInvalidValue on a device with more SMs than it covers.

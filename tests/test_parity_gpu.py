@@ -151,15 +151,37 @@ def test_gemm_tiny_config():
     (100, 130, 256), (128, 2048, 512),                  # swapped-orientation kernel
     (129, 256, 512), (200, 640, 1024), (300, 576, 384), (256, 2304, 256), (513, 97, 256),
     (1200, 4608, 256), (1100, 4736, 256), (1024, 4800, 384), (768, 5120, 1280),
-    (1024, 2048, 256), (2048, 1536, 512), (700, 1000, 256),
-                                                        # normal kernel: 64/128/256-wide tiles,
-                                                        # several tiles, ragged tails
+    (1024, 2048, 256), (2048, 1536, 512), (700, 1000, 256), (2048, 1300, 256),
+                                                        # normal kernel: 64/128/192/256-wide
+                                                        # tiles (192: a thread's columns may
+                                                        # span two blocks of b_s), several
+                                                        # tiles, ragged tails
 ])
 def test_gemm_shapes_full_compare(M, N, K):
     x = synth.activations(M, K, seed=M + N + K, name="pgA", outlier_frac=0.01)
     a, a_s = oracle.act_quant(x)
     b, b_s = synth.weights(N, K, seed=M * N + K, name="pgB")
     assert_gemm_close(run_gemm(a, a_s, b, b_s), oracle.gemm(a, a_s, b, b_s), f"{M}x{N}x{K}")
+
+
+def test_gemm_fp32_stream_k_against_oracle():
+    """fp32 scales with a workspace: 180 tiles of 128 x 192 on the SMs share their K loops
+    (each owner starts from the next CTA's partial); every element matches the oracle, and two
+    calls agree bit for bit."""
+    M, N, K = 2560, 2304, 1024
+    x = synth.activations(M, K, seed=21, name="skA", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x)
+    b, b_s = synth.weights(N, K, seed=22, name="skB")
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
+    args = (dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), "fp32")
+    c1 = fp8bs.fp8_gemm(*args, workspace=ws)
+    c2 = fp8bs.fp8_gemm(*args, workspace=ws)
+    c0 = fp8bs.fp8_gemm(*args, workspace=None)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    ref = oracle.gemm(a, a_s, b, b_s)
+    assert_gemm_close(host_bf16_f64(c1), ref, "fp32 stream-K")
+    assert_gemm_close(host_bf16_f64(c0), ref, "fp32 no workspace")
 
 
 def test_gemm_k_zero_writes_zeros():
@@ -418,31 +440,47 @@ def run_gemm_ws(a_codes, a_s, b_codes, b_s, ws, fmt="ue8m0"):
     return host_bf16_f64(c)
 
 
-@pytest.mark.parametrize("M,N,K", [
-    (256, 256, 1024),     # 4 tiles x 8 K blocks on 32 CTAs: every tile shared by 8 CTAs
-    (129, 200, 2048),     # ragged rows and columns
-    (300, 576, 2048),     # N tail inside the last 128-column tile
-    (1024, 1536, 4096),   # 96 tiles over all SMs, pieces of uneven length
-    (640, 384, 7168),
+@pytest.mark.parametrize("M,N,K,full", [
+    (1100, 2500, 2048, True),    # 180 tiles, ragged rows and columns, each shared by two CTAs
+    (1024, 2560, 2048, True),    # 160 tiles
+    (256, 256, 1024, True),      # 4 tiles: too few to share, computed whole
+    (2048, 1536, 7168, False),   # the MLA q projection, 192 tiles of 56 K blocks
 ])
-def test_gemm_ue8m0_stream_k_against_oracle(M, N, K):
+def test_gemm_ue8m0_stream_k_against_oracle(M, N, K, full):
     """With a workspace the block-scaled GEMM shares tiles' K loops between CTAs; every output
-    element must still match the oracle, and repeated calls on the same workspace agree bit
-    for bit (the partials are added in a fixed order, and the workspace's counters return to
-    zero after each call)."""
+    element (or a sample hitting every tile) must still match the oracle, and repeated calls on
+    the same workspace agree bit for bit (the partials are added in a fixed order, and the
+    workspace's counters return to zero after each call)."""
     a, a_s, b, b_s = pow2_case(M, N, K, M * 3 + N + K)
     ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
-    ref = oracle.gemm(a, a_s, b, b_s)
     c1 = run_gemm_ws(a, a_s, b, b_s, ws)
-    assert_gemm_close(c1, ref, f"stream-K {M}x{N}x{K}")
     c2 = run_gemm_ws(a, a_s, b, b_s, ws)
+    c0 = run_gemm_ws(a, a_s, b, b_s, None)
     assert np.array_equal(c1, c2)
-    assert_gemm_close(run_gemm_ws(a, a_s, b, b_s, None), ref, f"no workspace {M}x{N}x{K}")
+    if full:
+        ref = oracle.gemm(a, a_s, b, b_s)
+        assert_gemm_close(c1, ref, f"stream-K {M}x{N}x{K}")
+        assert_gemm_close(c0, ref, f"no workspace {M}x{N}x{K}")
+    else:
+        mi, ni = tile_samples(M, N, 1, seed=M + N)
+        ref = oracle.gemm_at(a, a_s, b, b_s, mi, ni)
+        assert_gemm_close(c1[mi, ni], ref, f"stream-K {M}x{N}x{K}")
+        assert_gemm_close(c0[mi, ni], ref, f"no workspace {M}x{N}x{K}")
+
+
+def test_gemm_ue8m0_stream_k_after_whole_tiles():
+    """320 tiles: the first 152 are computed whole, the last 168 share their K loops."""
+    M, N, K = 2560, 2048, 2048
+    a, a_s, b, b_s = pow2_case(M, N, K, 23)
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
+    c = run_gemm_ws(a, a_s, b, b_s, ws)
+    mi, ni = tile_samples(M, N, 2, seed=5)
+    assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni), "ue8m0 hybrid stream-K")
 
 
 def test_gemm_ue8m0_stream_k_workspace_reused_across_shapes():
     ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
-    for M, N, K in [(256, 256, 1024), (640, 384, 7168), (129, 200, 2048), (256, 256, 1024)]:
+    for M, N, K in [(1024, 2560, 2048), (1100, 2500, 2048), (256, 256, 1024), (1024, 2560, 2048)]:
         a, a_s, b, b_s = pow2_case(M, N, K, M + N)
         assert_gemm_close(run_gemm_ws(a, a_s, b, b_s, ws), oracle.gemm(a, a_s, b, b_s),
                           f"reused workspace {M}x{N}x{K}")
