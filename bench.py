@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "7aa55542a73567f8", "per_launch_mb": (135.04 + 135.47) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "025ccecfd3326f7c", "per_launch_mb": (134.97 + 135.12) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -582,7 +582,7 @@ def run_profile(case: str, launches: int, warmup: int):
         s = torch.empty((4096, K // 128), dtype=torch.float32, device="cuda")
         c = torch.empty((4096, N), dtype=torch.bfloat16, device="cuda")
         g.act_quant(x, y, s, 4096, K)
-        fn = lambda: g.gemm(y, s, B, S, c, 4096, N, K)  # noqa: E731
+        fn = lambda: g.gemm_ws(y, s, B, S, c, 4096, N, K)  # noqa: E731
     elif case.startswith("mla"):
         # ue8m0 MLA projection on the block-scaled kernel: mla1536 or mla576
         N = int(case[len("mla"):] or synth.Q_LORA)

@@ -279,31 +279,38 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                             fma2_into(acc + 32 * c + i, v[32 * c + i], v[32 * c + i + 1], s_c, s_c);
                     }
                 } else {
-                    // Chunks of 32 columns: the load of chunk c+1 is in flight while chunk c is
-                    // folded in; the buffer is handed back as soon as the last chunk has landed.
-                    float va[32], vb[32];
-                    tmem_ld_32cols(taddr, va);
-                    tmem_wait_ld_32(va);
-#pragma unroll
-                    for (int c = 0; c < Cfg::NCH; ++c) {
-                        float* cur = (c & 1) ? vb : va;
-                        float* nxt = (c & 1) ? va : vb;
-                        if (c + 1 < Cfg::NCH) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
-                        if (c + 1 == Cfg::NCH) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
-                        }
-                        const float s_c =
-                            Cfg::TWO_B && min((n0 + col0 + 32 * c) / 128, nb_count - 1) != nb
-                                ? sc2
-                                : sc;
-                        // Packed fp32x2 FMAs (round-to-nearest per component).
+                    // Three or four chunks through two 32-column register buffers: chunks 0 and
+                    // 1 are loaded together; chunk 0 is folded in while chunk 2 loads into its
+                    // registers, chunk 1 while chunk 3 loads; the buffer goes back once the last
+                    // chunk has landed, after two round trips, and the rest is folded in after.
+                    static_assert(Cfg::NCH == 3 || Cfg::NCH == 4, "two register buffers");
+                    auto scale_of = [&](int c) {
+                        return Cfg::TWO_B && min((n0 + col0 + 32 * c) / 128, nb_count - 1) != nb
+                                   ? sc2
+                                   : sc;
+                    };
+                    auto fold = [&](int c, const float* v) {
+                        const float s_c = scale_of(c);
 #pragma unroll
                         for (int i = 0; i < 32; i += 2)
-                            fma2_into(acc + 32 * c + i, cur[i], cur[i + 1], s_c, s_c);
-                        if (c + 1 < Cfg::NCH) tmem_wait_ld_32(nxt);
-                    }
+                            fma2_into(acc + 32 * c + i, v[i], v[i + 1], s_c, s_c);
+                    };
+                    float va[32], vb[32];
+                    tmem_ld_32cols(taddr, va);
+                    tmem_ld_32cols(taddr + 32, vb);
+                    tmem_wait_ld_32(va);
+                    tmem_wait_ld_32(vb);
+                    fold(0, va);
+                    tmem_ld_32cols(taddr + 64, va);
+                    fold(1, vb);
+                    if constexpr (Cfg::NCH == 4) tmem_ld_32cols(taddr + 96, vb);
+                    tmem_wait_ld_32(va);
+                    if constexpr (Cfg::NCH == 4) tmem_wait_ld_32(vb);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                    fold(2, va);
+                    if constexpr (Cfg::NCH == 4) fold(3, vb);
                 }
                 buf ^= 1;
                 if (buf == 0) tphase ^= 1;
