@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "025ccecfd3326f7c", "per_launch_mb": (134.97 + 135.12) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "a4b0791a5177531a", "per_launch_mb": (135.02 + 135.41) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -74,7 +74,8 @@ def decode_step_bytes():
     return sum(act_quant_bytes(M, K_DIM) + gemm_bytes(M, N_DIM, K_DIM) for M in DECODE_MS)
 
 
-DECODE_KERNEL_SOURCES = ("gemm_swapab.cu", "gemm_common.cuh", "ptx.cuh", "kernels.h")
+DECODE_KERNEL_SOURCES = ("gemm_swapab.cu", "gemm_common.cuh", "quant_math.cuh", "ptx.cuh",
+                         "kernels.h")
 
 
 def decode_kernel_sha():
@@ -215,11 +216,22 @@ class Gpu:
         self.fp8bs.fp8bs_gemm_ex(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
                                  c.data_ptr(), M, N, K, fmt, flags, self.sh)
 
-    def gemm_ws(self, a, a_s, b, b_s, c, M, N, K, fmt=0):
-        """fp8bs_gemm_ws with the benchmark's workspace (stream-K where it pays)."""
+    def workspace(self):
         if self._ws is None:
             self._ws = self.torch.zeros(self.fp8bs.fp8bs_gemm_workspace_size(),
                                         dtype=self.torch.uint8, device="cuda")
+        return self._ws
+
+    def act_quant_gemm(self, x, y, s, b, b_s, c, M, N, K, fmt=0, flags=0):
+        """act_quant + fp8_gemm through fp8bs_act_quant_gemm (one launch at decode sizes)."""
+        ws = self.workspace()
+        self.fp8bs.fp8bs_act_quant_gemm(x.data_ptr(), y.data_ptr(), s.data_ptr(), b.data_ptr(),
+                                        b_s.data_ptr(), c.data_ptr(), M, N, K, fmt, flags,
+                                        ws.data_ptr(), ws.numel(), self.sh)
+
+    def gemm_ws(self, a, a_s, b, b_s, c, M, N, K, fmt=0):
+        """fp8bs_gemm_ws with the benchmark's workspace (stream-K where it pays)."""
+        self.workspace()
         self.fp8bs.fp8bs_gemm_ws(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
                                  c.data_ptr(), M, N, K, fmt, 0, self._ws.data_ptr(),
                                  self._ws.numel(), self.sh)
@@ -277,13 +289,12 @@ WEIGHTS_CONSTANT = 1   # fp8bs_gemm_ex flag: model weights are not written durin
 
 
 def decode_step(g: Gpu, state):
-    """act_quant + fp8_gemm for every M, back to back: each kernel may start while the
-    previous one finishes (the GEMM starts its weight stream early)."""
+    """act_quant + fp8_gemm for every M, back to back, through fp8bs_act_quant_gemm (two
+    kernels per M): each kernel may start while the previous one finishes (the GEMM starts its
+    weight stream early)."""
     for st in state:
-        M = st["M"]
-        g.act_quant(st["x"], st["y"], st["s"], M, K_DIM)
-        g.gemm_ex(st["y"], st["s"], st["B"], st["S"], st["c"], M, N_DIM, K_DIM, 0,
-                  WEIGHTS_CONSTANT)
+        g.act_quant_gemm(st["x"], st["y"], st["s"], st["B"], st["S"], st["c"], st["M"], N_DIM,
+                         K_DIM, 0, WEIGHTS_CONSTANT)
 
 
 def run_decode(g: Gpu, steps, warmup, rank, world, clocks_path):
@@ -347,9 +358,8 @@ def run_decode_e2e(g: Gpu, steps, warmup, world):
     def step():
         for i, st in enumerate(state):
             st["x"].copy_(hx[i], non_blocking=True)
-            g.act_quant(st["x"], st["y"], st["s"], st["M"], K_DIM)
-            g.gemm_ex(st["y"], st["s"], st["B"], st["S"], st["c"], st["M"], N_DIM, K_DIM, 0,
-                      WEIGHTS_CONSTANT)
+            g.act_quant_gemm(st["x"], st["y"], st["s"], st["B"], st["S"], st["c"], st["M"],
+                             N_DIM, K_DIM, 0, WEIGHTS_CONSTANT)
             hc[i].copy_(st["c"], non_blocking=True)
 
     for _ in range(warmup):
@@ -571,7 +581,8 @@ def run_profile(case: str, launches: int, warmup: int):
         s = torch.empty((M, K_DIM // 128), dtype=torch.float32, device="cuda")
         c = torch.empty((M, N_DIM), dtype=torch.bfloat16, device="cuda")
         g.act_quant(x, y, s, M, K_DIM)
-        fn = lambda: g.gemm(y, s, B, S, c, M, N_DIM, K_DIM)  # noqa: E731
+        fn = lambda: g.gemm_ex(y, s, B, S, c, M, N_DIM, K_DIM, 0,  # noqa: E731
+                               WEIGHTS_CONSTANT)
     elif case in ("prefill_up", "prefill_down"):
         up = case == "prefill_up"
         N, K = (N_DIM, K_DIM) if up else (K_DIM, N_DIM)

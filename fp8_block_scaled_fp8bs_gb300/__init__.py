@@ -36,8 +36,10 @@ DEVERR_PROBE = 0x100
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 GEMM_WEIGHTS_CONSTANT = 0x1
+GEMM_QUANT_IN_KERNEL = 0x2
 EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_ex",
            "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_noalloc",
+           "fp8bs_act_quant_gemm",
            "fp8bs_gemm_grouped",
            "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
 
@@ -70,6 +72,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_gemm_ws.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint, vp,
                                       ctypes.c_size_t, vp]
         lib.fp8bs_gemm_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+        lib.fp8bs_act_quant_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
+                                             ctypes.c_uint, vp, ctypes.c_size_t, vp]
         lib.fp8bs_gemm_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint,
                                            vp]
         lib.fp8bs_gemm_grouped.argtypes = [vp, vp, vp, vp, vp, ctypes.POINTER(ctypes.c_int64),
@@ -119,6 +123,12 @@ def fp8bs_gemm_noalloc(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0
                        stream=0) -> None:
     _check("fp8bs_gemm_noalloc", load().fp8bs_gemm_noalloc(a, a_s, b, b_s, c, M, N, K,
                                                            scale_fmt, flags, stream))
+
+
+def fp8bs_act_quant_gemm(x, y, s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0,
+                         workspace=0, workspace_bytes=0, stream=0) -> None:
+    _check("fp8bs_act_quant_gemm", load().fp8bs_act_quant_gemm(
+        x, y, s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes, stream))
 
 
 def fp8bs_gemm_workspace_size() -> int:
@@ -235,6 +245,34 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False,
                   M, N, K, _fmt(scale_fmt), GEMM_WEIGHTS_CONSTANT if weights_constant else 0,
                   ws_ptr, ws_bytes, _stream())
     return c
+
+
+def act_quant_gemm(x, b, b_s, scale_fmt="fp32", weights_constant=False, workspace="auto",
+                   quant_in_kernel=False):
+    """linear() on the FP8 path: x bf16 [M,K] -> (c bf16 [M,N], y e4m3 [M,K], s fp32
+    [M,K/128]): act_quant then the GEMM (quant_in_kernel: one kernel, M <= 64); see fp8_gemm
+    for `workspace`."""
+    import torch
+    _require(x, torch.bfloat16, 2, "x")
+    _require(b, torch.float8_e4m3fn, 2, "b")
+    _require(b_s, torch.float32, 2, "b_s")
+    M, K = x.shape
+    N = b.shape[0]
+    if b.shape[1] != K or tuple(b_s.shape) != (-(-N // BLOCK), K // BLOCK):
+        raise ValueError("operand or scale shapes do not match")
+    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
+    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=x.device)
+    c = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    if isinstance(workspace, str) and workspace == "auto":
+        workspace = gemm_workspace(x.device)
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
+        if workspace is not None else (0, 0)
+    flags = (GEMM_WEIGHTS_CONSTANT if weights_constant else 0) | \
+        (GEMM_QUANT_IN_KERNEL if quant_in_kernel else 0)
+    fp8bs_act_quant_gemm(x.data_ptr(), y.data_ptr(), s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
+                         c.data_ptr(), M, N, K, _fmt(scale_fmt), flags, ws_ptr, ws_bytes,
+                         _stream())
+    return c, y, s
 
 
 def fp8_gemm_grouped(a, a_s, b, b_s, row_offsets, scale_fmt="fp32", out=None):

@@ -70,6 +70,21 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same over a row-major bf16 matrix [rows, K], box {128 elements, box_rows}, no swizzle
+// (the decode GEMM quantises these rows itself).
+bool make_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
 
 // Stream-K plans (see StreamKArgs in kernels.h). Whole tiles for all but the last one to two
@@ -157,7 +172,7 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
         // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA.
         const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
         if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, MT)) return FP8BS_ERR_CUDA;
-        cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, st);
+        cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, fp8bs::FusedQuant{}, st);
         if (e != cudaErrorInvalidValue) return status_of(e);
         // K too long to stage the activation scales: fall through to the normal kernel.
     }
@@ -237,6 +252,65 @@ int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, const float* b
                   int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
                   void* workspace, size_t workspace_bytes, void* stream) {
     return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes,
+                     stream);
+}
+
+int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b, const float* b_s,
+                         void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                         unsigned int flags, void* workspace, size_t workspace_bytes,
+                         void* stream) {
+    if ((flags & ~(FP8BS_GEMM_WEIGHTS_CONSTANT | FP8BS_GEMM_QUANT_IN_KERNEL)) != 0)
+        return FP8BS_ERR_INVALID_ARG;
+    const bool in_kernel = (flags & FP8BS_GEMM_QUANT_IN_KERNEL) != 0;
+    flags &= ~FP8BS_GEMM_QUANT_IN_KERNEL;
+    if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
+    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
+        return FP8BS_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (!c) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(c)) return FP8BS_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int sms = 0;
+    if (K == 0) {
+        if (int e = check_device(&sms)) return e;
+        return status_of(cudaMemsetAsync(c, 0, static_cast<size_t>(M * N) * 2, st));
+    }
+    if (!x || !y || !s || !b || !b_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(y) || !aligned4(s) || !aligned16(b) || !aligned4(b_s))
+        return FP8BS_ERR_MISALIGNED;
+    if (int e = check_device(&sms)) return e;
+    if (workspace) {
+        if (!aligned16(workspace)) return FP8BS_ERR_MISALIGNED;
+        if (workspace_bytes < fp8bs::stream_k_workspace(sms)) return FP8BS_ERR_INVALID_ARG;
+    }
+    const bool ue8m0 = scale_fmt == FP8BS_SCALE_UE8M0;
+    if (in_kernel && M <= 64) {
+        // One launch: the decode GEMM quantises the rows of each K block it reads.
+        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+        GemmArgs g;
+        g.a_s = s;
+        g.b_s = b_s;
+        g.c = c;
+        g.M = static_cast<int>(M);
+        g.N = static_cast<int>(N);
+        g.K = static_cast<int>(K);
+        g.weights_constant = (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0;
+        fp8bs::FusedQuant fq;
+        fq.x = static_cast<const uint4*>(x);
+        fq.y = static_cast<uint4*>(y);
+        fq.s = s;
+        fq.ue8m0 = ue8m0 ? 1 : 0;
+        CUtensorMap tmA, tmB;
+        if (!make_map(&tmB, b, N, K, 128) || !make_map_bf16(&tmA, x, M, K, MT))
+            return FP8BS_ERR_CUDA;
+        const cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, fq, st);
+        if (e != cudaErrorInvalidValue) return status_of(e);
+        // K too long to stage the scales: two launches below.
+    }
+    // Two launches: act_quant, then the GEMM on its output.
+    if (int st2 = status_of(fp8bs::launch_act_quant(x, y, s, M, K, ue8m0, sms, st))) return st2;
+    return gemm_impl(y, s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes,
                      stream);
 }
 

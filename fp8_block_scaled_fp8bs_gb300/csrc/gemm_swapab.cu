@@ -1,38 +1,76 @@
 // gemm_swapab.cu -- FP8 GEMM with fp32 block scales for few rows of A (decode, M <= 128):
 // 128 rows of B take the MMA's M side and the MT (16, 32, 64 or 128) rows of A its N side, so
 // the weight stream fills the tensor core's 128 lanes and every SM streams its own 128-row
-// weight slab. The activation scales are staged in shared memory transposed, [kb][m]; the
-// promotion warps fold each K block's TMEM partial into fp32 registers as in gemm_tn.cu.
+// weight slab. The promotion warps fold each K block's TMEM partial into fp32 registers with
+// the combined scale a_s[m, kb] * b_s[slab, kb], as in gemm_tn.cu.
+//
+// Two ways in for the activations:
+//   quantised (fp8bs_gemm): TMA brings e4m3 rows of A; their scales are staged in shared memory
+//       transposed to [kb][m] before the main loop.
+//   bf16 (fp8bs_act_quant_gemm, FUSED): TMA brings each K block's bf16 rows of x, and four
+//       quantiser warps turn them into the e4m3 tile the MMA reads (128-byte swizzle) and the
+//       block's scales, with act_quant's arithmetic ("DeepSeek-V3 Administrator & Developer
+//       Guide", §8.5.1) -- every CTA quantises the rows it needs, so no kernel and no grid-wide
+//       synchronisation stands between the previous layer and this GEMM; the CTAs of the first
+//       weight slab also write y and s.
 #include "gemm_common.cuh"
+#include "quant_math.cuh"
 
 namespace fp8bs {
 
 namespace {
 
-template <int MT>
+template <int MT, bool FUSED>
 struct SwapCfg {
     static constexpr int EPI_WARPS = 4;
-    static constexpr int THREADS = 64 + 32 * EPI_WARPS;
-    static constexpr int X_TILE = MT * BK;          // activation rows per stage
-    static constexpr int STAGE = A_TILE + X_TILE;   // weight slab + activation rows
+    static constexpr int Q_WARPS = FUSED ? 4 : 0;   // quantiser warps, after the promotion warps
+    static constexpr int Q_WARP0 = 2 + EPI_WARPS;
+    static constexpr int THREADS = 64 + 32 * (EPI_WARPS + Q_WARPS);
+    static constexpr int X_TILE = MT * BK;          // e4m3 activation rows per stage
+    static constexpr int XB_TILE = FUSED ? MT * BK * 2 : 0;   // bf16 rows per stage (FUSED)
+    static constexpr int STAGE = A_TILE + X_TILE + XB_TILE;
+    static constexpr int TX_BYTES = A_TILE + (FUSED ? XB_TILE : X_TILE);  // bytes TMA brings
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * MT);
 };
 
-template <int MT>
-__global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
+// Shared-memory bytes after the stages: transposed scales [num_kb][MT], then (quantised input)
+// the raw a_s rows [MT][num_kb] or (FUSED) a ready count per K block, the b_s row, and (FUSED)
+// one "quantised" barrier per stage.
+template <int MT, bool FUSED>
+__host__ __device__ constexpr int swap_scale_bytes(int num_kb) {
+    return num_kb * MT * 4 + (FUSED ? num_kb * 4 : num_kb * MT * 4) + ((num_kb + 3) & ~3) * 4 +
+           16;
+}
+
+// Bounded spin until *p == target (a shared-memory count written by other warps).
+__device__ __forceinline__ bool spin_until_equal(const int* p, int target) {
+    const volatile int* v = p;
+    if (*v == target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (*v != target)
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+template <int MT, bool FUSED>
+__global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const GemmArgs g,
-                       const int stages) {
-    using Cfg = SwapCfg<MT>;
+                       const int stages, const FusedQuant fq) {
+    using Cfg = SwapCfg<MT, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sW = smem;                                   // [stages][128 x 128] weights
-    uint8_t* sX = smem + stages * A_TILE;                 // [stages][MT x 128] activations
+    uint8_t* sX = smem + stages * A_TILE;                 // [stages][MT x 128] e4m3 activations
+    uint8_t* sXb = sX + stages * Cfg::X_TILE;             // [stages][MT x 128] bf16 (FUSED)
     const int num_kb = g.K / BK;
-    float* sAs = reinterpret_cast<float*>(sX + stages * Cfg::X_TILE);  // [num_kb][MT]
-    float* sRaw = sAs + num_kb * MT;             // a_s rows m0 .. m0+MT-1 as stored: [MT][num_kb]
-    float* sBs = sRaw + num_kb * MT;             // b_s row of this slab: [num_kb]
-    const Ring ring = carve_ring(reinterpret_cast<uint8_t*>(sBs + ((num_kb + 3) & ~3)), stages);
+    float* sAs = reinterpret_cast<float*>(sXb + stages * Cfg::XB_TILE);  // [num_kb][MT]
+    float* sRaw = sAs + num_kb * MT;   // a_s rows m0 .. m0+MT-1 as stored: [MT][num_kb]
+    int* sReady = reinterpret_cast<int*>(sRaw);          // FUSED: [num_kb] quantiser warps done
+    float* sBs = sRaw + (FUSED ? num_kb : num_kb * MT);  // b_s row of this slab: [num_kb]
+    uint8_t* ring_mem = reinterpret_cast<uint8_t*>(sBs + ((num_kb + 3) & ~3));
+    const Ring ring = carve_ring(ring_mem, stages);
+    uint64_t* qfull = reinterpret_cast<uint64_t*>(ring_mem + ring_bytes(stages));  // FUSED
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -53,23 +91,32 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
+        if constexpr (FUSED) {
+            for (int s = 0; s < stages; ++s) mbar_init(&qfull[s], Cfg::Q_WARPS);
+            fence_barrier_init();
+        }
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         // Weights the caller declared constant need not wait for the kernels before this one:
         // the ring starts filling while they finish.
         if (g.weights_constant) {
             for (int kb = 0; kb < prefill; ++kb) {
-                mbar_arrive_expect_tx(&ring.full[kb], Cfg::STAGE);
+                mbar_arrive_expect_tx(&ring.full[kb], Cfg::TX_BYTES);
                 tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
             }
         }
     }
+    if constexpr (FUSED) {
+        for (int i = threadIdx.x; i < num_kb; i += Cfg::THREADS) sReady[i] = 0;
+    }
     grid_dependency_wait();
     grid_launch_dependents();
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
         const int t = threadIdx.x - 64;
-        for (int i = t; i < scale_rows * num_kb; i += 32 * Cfg::EPI_WARPS)
-            cp_async_4(sRaw + i, as_rows + i);
+        if constexpr (!FUSED) {
+            for (int i = t; i < scale_rows * num_kb; i += 32 * Cfg::EPI_WARPS)
+                cp_async_4(sRaw + i, as_rows + i);
+        }
         for (int i = t; i < num_kb; i += 32 * Cfg::EPI_WARPS) cp_async_4(sBs + i, bs_row + i);
         cp_async_commit();
     }
@@ -78,14 +125,17 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
+    // Activations on the first stages: e4m3 rows of A, or (FUSED) bf16 rows of x.
+    uint8_t* const sAct = FUSED ? sXb : sX;
+    constexpr int ACT_TILE = FUSED ? Cfg::XB_TILE : Cfg::X_TILE;
     if (threadIdx.x == 0) {
         // fill the whole ring at once
         for (int kb = 0; kb < prefill; ++kb) {
             if (!g.weights_constant) {
-                mbar_arrive_expect_tx(&ring.full[kb], Cfg::STAGE);
+                mbar_arrive_expect_tx(&ring.full[kb], Cfg::TX_BYTES);
                 tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
             }
-            tma_load_2d_hint(sX + kb * Cfg::X_TILE, &tmA, &ring.full[kb], kb * BK, m0, keep);
+            tma_load_2d_hint(sAct + kb * ACT_TILE, &tmA, &ring.full[kb], kb * BK, m0, keep);
         }
     }
 
@@ -101,9 +151,9 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(&ring.full[stage], Cfg::STAGE);
+                mbar_arrive_expect_tx(&ring.full[stage], Cfg::TX_BYTES);
                 tma_load_2d_hint(sW + stage * A_TILE, &tmB, &ring.full[stage], kb * BK, n0, stream);
-                tma_load_2d_hint(sX + stage * Cfg::X_TILE, &tmA, &ring.full[stage], kb * BK, m0,
+                tma_load_2d_hint(sAct + stage * ACT_TILE, &tmA, &ring.full[stage], kb * BK, m0,
                                  keep);
                 ++issued;
                 if (++stage == stages) {
@@ -120,7 +170,8 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
             uint32_t phase = 0, tphase = 0;
             for (int kb = 0; kb < num_kb; ++kb) {
                 if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
-                    !mbar_wait(&ring.full[stage], phase)) {
+                    !mbar_wait(&ring.full[stage], phase) ||
+                    (FUSED && !mbar_wait(&qfull[stage], phase))) {
                     record_error(FP8BS_DEVERR_MMA_WAIT);
                     break;
                 }
@@ -144,20 +195,93 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
             mma_commit(ring.drain);
             if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
         }
+    } else if (FUSED && warp >= Cfg::Q_WARP0) {
+        // Quantiser warps: per K block, 8 lanes per row of MT: lane l of a group takes elements
+        // 16 (l % 8) .. +15 of its row, i.e. one 16-byte chunk of the row's 128 e4m3 codes,
+        // stored at chunk (l % 8) ^ (row % 8) of the row (128-byte swizzle, 8-row atoms of 1024
+        // bytes: the layout TMA would have written).
+        const int qw = warp - Cfg::Q_WARP0;
+        const int sub = lane >> 3;                        // row within the warp's four
+        const int chunk = lane & 7;
+        const bool writer = blockIdx.x == 0;              // first slab: also write y and s
+        const int rows = min(MT, g.M - m0);               // rows of x; the rest stay zero
+        constexpr int PASSES = MT / 16;
+        // Rows past M are zero codes in every stage (written once, never overwritten).
+        for (int i = threadIdx.x - Cfg::Q_WARP0 * 32; i < stages * MT * 8; i += Cfg::Q_WARPS * 32) {
+            const int st = i / (MT * 8), row = (i / 8) % MT, ch = i % 8;
+            if (row >= rows)
+                *reinterpret_cast<uint4*>(sX + st * Cfg::X_TILE + (row >> 3) * 1024 +
+                                          (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) =
+                    make_uint4(0, 0, 0, 0);
+        }
+        int stage = 0;
+        uint32_t phase = 0;
+        for (int kb = 0; kb < num_kb; ++kb) {
+            if (!warp_wait(&ring.full[stage], phase)) {
+                if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                break;
+            }
+            const uint8_t* xb = sXb + stage * Cfg::XB_TILE;
+            uint8_t* xq = sX + stage * Cfg::X_TILE;
+            // This warp's rows pass * 16 + qw * 4 + sub: all passes with a row of x are issued
+            // together (independent chains), passes of padding only are skipped (warp-uniform).
+            uint32_t w[PASSES][8];
+#pragma unroll
+            for (int pass = 0; pass < PASSES; ++pass) {
+                const int row = pass * 16 + qw * 4 + sub;
+                if (pass * 16 + qw * 4 < rows) {
+                    const uint4 v0 = *reinterpret_cast<const uint4*>(xb + row * 256 + chunk * 32);
+                    const uint4 v1 =
+                        *reinterpret_cast<const uint4*>(xb + row * 256 + chunk * 32 + 16);
+                    w[pass][0] = v0.x; w[pass][1] = v0.y; w[pass][2] = v0.z; w[pass][3] = v0.w;
+                    w[pass][4] = v1.x; w[pass][5] = v1.y; w[pass][6] = v1.z; w[pass][7] = v1.w;
+                }
+            }
+#pragma unroll
+            for (int pass = 0; pass < PASSES; ++pass) {
+                if (pass * 16 + qw * 4 >= rows) continue;
+                const int row = pass * 16 + qw * 4 + sub;
+                uint32_t out[4];
+                const float sc = fq.ue8m0 ? quant_block16<true>(w[pass], out)
+                                          : quant_block16<false>(w[pass], out);
+                const uint4 q = make_uint4(out[0], out[1], out[2], out[3]);
+                *reinterpret_cast<uint4*>(xq + (row >> 3) * 1024 + (row & 7) * 128 +
+                                          ((chunk ^ (row & 7)) << 4)) = q;
+                if (chunk == 0) sAs[kb * MT + row] = sc;
+                if (writer && row < rows) {
+                    const int64_t grow = m0 + row;
+                    fq.y[(grow * g.K + kb * BK + chunk * 16) >> 4] = q;
+                    if (chunk == 0) fq.s[grow * num_kb + kb] = sc;
+                }
+            }
+            // The tile is read next by the tensor core (async proxy), the scales by the
+            // promotion warps.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&qfull[stage]);
+                atomicAdd(&sReady[kb], 1);
+            }
+            if (++stage == stages) {
+                stage = 0;
+                phase ^= 1;
+            }
+        }
     } else {
-        // Combined scales a_s[m, kb] * b_s[slab, kb] of this CTA's MT rows, transposed to
-        // [kb][m] (zero past row M). Only the promotion warps need them, so the producer and
-        // the MMA issuer start streaming while they are staged; reads are coalesced along kb.
-        // Combined scales sAs[kb][m] = a_s[m0+m, kb] * b_s[slab, kb] (zero past row M), from the
-        // rows copied at kernel start.
+        // Promotion warps.
         cp_async_wait_all();
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
-        const int valid = scale_rows * num_kb;
-        for (int i = threadIdx.x - 64; i < MT * num_kb; i += 32 * Cfg::EPI_WARPS) {
-            const int j = i / num_kb, kb = i - j * num_kb;
-            sAs[kb * MT + j] = i < valid ? sRaw[i] * sBs[kb] : 0.0f;
+        if constexpr (!FUSED) {
+            // Combined scales sAs[kb][m] = a_s[m0+m, kb] * b_s[slab, kb] (zero past row M), from
+            // the rows copied at kernel start, transposed so that reads are coalesced along kb.
+            const int valid = scale_rows * num_kb;
+            for (int i = threadIdx.x - 64; i < MT * num_kb; i += 32 * Cfg::EPI_WARPS) {
+                const int j = i / num_kb, kb = i - j * num_kb;
+                sAs[kb * MT + j] = i < valid ? sRaw[i] * sBs[kb] : 0.0f;
+            }
+            asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         }
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         const int quarter = warp & 3;
         const int n = n0 + quarter * 32 + lane;      // output column owned by this thread
         float acc[MT];
@@ -172,10 +296,32 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
                 ok = false;
                 break;
             }
+            // FUSED: this block's a_s (written by the quantiser warps, long before the MMA that
+            // just finished could run) times b_s; otherwise the staged products.
+            float sb = 1.0f;
+            if constexpr (FUSED) {
+                if (!spin_until_equal(&sReady[kb], Cfg::Q_WARPS)) {
+                    if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                    ok = false;
+                    break;
+                }
+                __threadfence_block();
+                sb = sBs[kb];
+            }
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * MT);
             const float* as_kb = sAs + kb * MT;
+            auto scales4 = [&](int i) {
+                float4 a4 = *reinterpret_cast<const float4*>(as_kb + i);
+                if constexpr (FUSED) {   // rows past M: zero, as when staged
+                    a4.x = m0 + i < g.M ? a4.x * sb : 0.0f;
+                    a4.y = m0 + i + 1 < g.M ? a4.y * sb : 0.0f;
+                    a4.z = m0 + i + 2 < g.M ? a4.z * sb : 0.0f;
+                    a4.w = m0 + i + 3 < g.M ? a4.w * sb : 0.0f;
+                }
+                return a4;
+            };
             if constexpr (MT >= 32) {
                 // Chunks of 32 columns, the next load in flight while one is folded in.
                 constexpr int NCH = MT / 32;
@@ -194,7 +340,7 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
                     }
 #pragma unroll
                     for (int i = 0; i < 32; i += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4*>(as_kb + c * 32 + i);
+                        const float4 a4 = scales4(c * 32 + i);
                         fma2_into(acc + c * 32 + i, cur[i + 0], cur[i + 1], a4.x, a4.y);
                         fma2_into(acc + c * 32 + i + 2, cur[i + 2], cur[i + 3], a4.z, a4.w);
                     }
@@ -209,7 +355,7 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
                 if (lane == 0) mbar_arrive(&ring.tempty[buf]);
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
-                    const float4 a4 = *reinterpret_cast<const float4*>(as_kb + i);
+                    const float4 a4 = scales4(i);
                     fma2_into(acc + i, v[i + 0], v[i + 1], a4.x, a4.y);
                     fma2_into(acc + i + 2, v[i + 2], v[i + 3], a4.z, a4.w);
                 }
@@ -231,34 +377,43 @@ __global__ void __launch_bounds__(SwapCfg<MT>::THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int MT>
+template <int MT, bool FUSED>
 cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const GemmArgs& g,
-                        cudaStream_t stream) {
-    using Cfg = SwapCfg<MT>;
+                        const FusedQuant& fq, cudaStream_t stream) {
+    using Cfg = SwapCfg<MT, FUSED>;
     const int num_kb = g.K / BK;
-    // scale staging: transposed [num_kb][MT], raw rows [MT][num_kb], b_s row, one barrier
-    const int scale_bytes = 2 * num_kb * MT * 4 + ((num_kb + 3) & ~3) * 4 + 16;
-    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages);
+    const int scale_bytes = swap_scale_bytes<MT, FUSED>(num_kb);
+    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages) + (FUSED ? 8 * kMaxStages : 0);
     int stages = (kSmemLimit - fixed) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return cudaErrorInvalidValue;   // K too large for the scale staging
-    const int smem = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages);
-    cudaError_t e = set_smem(gemm_swapab_kernel<MT>, smem);
+    const int smem = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages) +
+                     (FUSED ? 8 * stages : 0);
+    cudaError_t e = set_smem(gemm_swapab_kernel<MT, FUSED>, smem);
     if (e != cudaSuccess) return e;
     const dim3 grid((g.N + BM - 1) / BM, (g.M + MT - 1) / MT);
-    return launch_pdl(gemm_swapab_kernel<MT>, grid, Cfg::THREADS, smem, stream, tmB, tmA, g,
-                      stages);
+    return launch_pdl(gemm_swapab_kernel<MT, FUSED>, grid, Cfg::THREADS, smem, stream, tmB, tmA,
+                      g, stages, fq);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
-                               const GemmArgs& g, int MT, cudaStream_t stream) {
+                               const GemmArgs& g, int MT, const FusedQuant& fq,
+                               cudaStream_t stream) {
+    if (fq.x) {
+        switch (MT) {
+            case 16: return launch_swap<16, true>(tmB, tmA, g, fq, stream);
+            case 32: return launch_swap<32, true>(tmB, tmA, g, fq, stream);
+            case 64: return launch_swap<64, true>(tmB, tmA, g, fq, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (MT) {
-        case 16: return launch_swap<16>(tmB, tmA, g, stream);
-        case 32: return launch_swap<32>(tmB, tmA, g, stream);
-        case 64: return launch_swap<64>(tmB, tmA, g, stream);
-        case 128: return launch_swap<128>(tmB, tmA, g, stream);
+        case 16: return launch_swap<16, false>(tmB, tmA, g, fq, stream);
+        case 32: return launch_swap<32, false>(tmB, tmA, g, fq, stream);
+        case 64: return launch_swap<64, false>(tmB, tmA, g, fq, stream);
+        case 128: return launch_swap<128, false>(tmB, tmA, g, fq, stream);
         default: return cudaErrorInvalidValue;
     }
 }

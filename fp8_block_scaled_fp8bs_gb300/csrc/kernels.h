@@ -97,10 +97,22 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 // cudaErrorInvalidValue on a device with more SMs than it covers.
 cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes);
 
+// Activations quantised inside the decode GEMM launch (MT <= 64): x bf16 [M, K] -> y e4m3,
+// s fp32 (as act_quant writes them); every CTA quantises the rows of each K block it reads,
+// those of the first weight slab also write y and s. x == nullptr: plain GEMM.
+struct FusedQuant {
+    const uint4* x;
+    uint4* y;
+    float* s;
+    int ue8m0;
+};
+
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
-// on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K].
+// on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K] (with
+// FusedQuant: a bf16 map over x, box {128, MT}, no swizzle).
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
-                               const GemmArgs& g, int MT, cudaStream_t stream);
+                               const GemmArgs& g, int MT, const FusedQuant& fq,
+                               cudaStream_t stream);
 
 // Diagnostic kernel: one wait on a barrier nothing signals (see fp8bs_probe_wait_timeout).
 cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream);

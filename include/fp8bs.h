@@ -129,6 +129,8 @@ FP8BS_API int fp8bs_gemm(const void* a, const float* a_s, const void* b, const f
  * it could have written (all inputs, or all but b and b_s with the flag above).
  */
 #define FP8BS_GEMM_WEIGHTS_CONSTANT 0x1u
+/* fp8bs_act_quant_gemm only: quantise the activations inside the GEMM kernel (M <= 64). */
+#define FP8BS_GEMM_QUANT_IN_KERNEL 0x2u
 FP8BS_API int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b_s,
                             void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
                             unsigned int flags, void* stream);
@@ -163,6 +165,32 @@ FP8BS_API int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, cons
  *   bytes [out] host pointer receiving the size.
  */
 FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
+
+/*
+ * fp8bs_act_quant_gemm -- act_quant followed by the block-scaled GEMM on its output, the two
+ * steps of linear() on the FP8 path ("DeepSeek-V3 Administrator & Developer Guide", §6.3
+ * item 3: act_quant, then fp8_gemm; §8.5.1 and §8.5.3), as one call. By default two kernels
+ * run back to back (the GEMM starts while act_quant finishes and, with
+ * FP8BS_GEMM_WEIGHTS_CONSTANT, streams its weights meanwhile). With
+ * FP8BS_GEMM_QUANT_IN_KERNEL and M <= 64 one kernel does both: each CTA of the GEMM quantises
+ * the rows of every K block it reads, as act_quant would, and the CTAs of the first 128
+ * columns also write y and s. On GB300 at decode sizes this single kernel measured slower than
+ * the two (the quantisation sits on every K block's critical path), so it is not the default.
+ *
+ *   x      [in]  bf16 [M, K], 16-byte aligned.
+ *   y      [out] e4m3 [M, K], 16-byte aligned: the quantised activations, as fp8bs_act_quant.
+ *   s      [out] fp32 [M, K/128], 4-byte aligned: their scales, as fp8bs_act_quant.
+ *   b, b_s, c, M, N, K, scale_fmt, flags  as in fp8bs_gemm_ex (a = y, a_s = s); scale_fmt
+ *          also selects act_quant's scale format.
+ *   workspace, workspace_bytes  as in fp8bs_gemm_ws, for the GEMM of the two-launch case
+ *          (NULL: no split K loops).
+ *
+ * y, s and c are bit for bit those of fp8bs_act_quant then fp8bs_gemm_ws on the same stream.
+ */
+FP8BS_API int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b,
+                                   const float* b_s, void* c, int64_t M, int64_t N, int64_t K,
+                                   int scale_fmt, unsigned int flags, void* workspace,
+                                   size_t workspace_bytes, void* stream);
 
 /*
  * fp8bs_gemm_noalloc -- fp8bs_gemm_ws on a workspace that the library keeps in a static device

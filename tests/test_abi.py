@@ -137,6 +137,7 @@ def test_gemm_grouped_rejects_misaligned_and_null(lib):
 
 def test_gemm_ex_rejects_unknown_flags(lib):
     assert lib.fp8bs_gemm_ex(A16, B16, C16, B16, C16, 8, 256, 256, 0, 0x2, None) == INVALID
+    # FP8BS_GEMM_QUANT_IN_KERNEL (0x2) belongs to fp8bs_act_quant_gemm only
     assert lib.fp8bs_gemm_ex(None, None, None, None, None, 0, 256, 256, 0, 0x1, None) == OK
 
 
@@ -160,3 +161,16 @@ def test_gemm_workspace_size_without_a_gpu(lib):
     out = ctypes.c_size_t(0)
     assert lib.fp8bs_gemm_workspace_size(ctypes.byref(out)) in (CUDA, UNSUPPORTED)
     assert lib.fp8bs_gemm_workspace_size(None) == INVALID
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, B16, C16, C16, 8, 256, 200, 0, 0), INVALID),    # K % 128
+    ((A16, B16, C16, B16, C16, C16, 8, 256, 256, 2, 0), INVALID),    # bad scale_fmt
+    ((A16, B16, C16, B16, C16, C16, 8, 256, 256, 0, 0x4), INVALID),  # unknown flag
+    ((A16 + 8, B16, C16, B16, C16, C16, 8, 256, 256, 0, 0), MISALIGNED),
+    ((A16, B16 + 4, C16, B16, C16, C16, 8, 256, 256, 0, 0), MISALIGNED),
+    ((A16, None, C16, B16, C16, C16, 8, 256, 256, 0, 0), INVALID),
+    ((None, None, None, None, None, None, 0, 256, 256, 0, 0), OK),
+])
+def test_act_quant_gemm_argument_checks(lib, args, expect):
+    assert lib.fp8bs_act_quant_gemm(*args, None, 0, None) == expect

@@ -502,6 +502,56 @@ def test_gemm_ue8m0_deterministic():
     assert np.array_equal(run_gemm(a, a_s, b, b_s, "ue8m0"), run_gemm(a, a_s, b, b_s, "ue8m0"))
 
 
+# ------------------------------------------------------------------------------ act_quant + GEMM
+# fp8bs_act_quant_gemm: act_quant then the GEMM in one call, or (FP8BS_GEMM_QUANT_IN_KERNEL,
+# M <= 64) one kernel that quantises the activations itself; y, s and C must equal those of the
+# two separate calls bit for bit.
+
+def separate_act_quant_gemm(xt, bt, bst, fmt, ws):
+    y, s = fp8bs.act_quant(xt, fmt)
+    c = fp8bs.fp8_gemm(y, s, bt, bst, fmt, workspace=ws)
+    return c, y, s
+
+
+@pytest.mark.parametrize("fmt", ["fp32", "ue8m0"])
+@pytest.mark.parametrize("M,N,K", [
+    (1, 18432, 7168), (8, 2048, 7168), (32, 576, 1024), (64, 18432, 7168), (3, 20480, 256),
+    (17, 1000, 18432),     # M <= 64: the one-kernel form applies; N tail, long K
+    (100, 1536, 2048), (128, 4096, 512),   # two launches whatever the flag (swapped)
+    (300, 1024, 512),      # two launches, normal orientation
+])
+def test_act_quant_gemm_matches_separate_calls(fmt, M, N, K):
+    x = synth.activations(M, K, seed=M + N + K, name="aqgA", outlier_frac=0.01)
+    b, b_s = synth.weights(N, K, seed=N + K, name="aqgB", pow2=fmt == "ue8m0")
+    xt, bt, bst = dev_bf16(x), dev_e4m3(b), dev_f32(b_s)
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
+    c0, y0, s0 = separate_act_quant_gemm(xt, bt, bst, fmt, ws)
+    for in_kernel in (False, True, True):                 # default, then the one-kernel form
+        c1, y1, s1 = fp8bs.act_quant_gemm(xt, bt, bst, fmt, weights_constant=True, workspace=ws,
+                                          quant_in_kernel=in_kernel)
+        torch.cuda.synchronize()
+        assert torch.equal(y1.view(torch.uint8), y0.view(torch.uint8))
+        assert torch.equal(s1.view(torch.int32), s0.view(torch.int32))
+        assert torch.equal(c1.view(torch.int16), c0.view(torch.int16))
+    # and against the oracle on the codes it produced itself
+    a_ref, as_ref = oracle.act_quant(x, FMTS[fmt])
+    assert_quant_equal(host_codes(y1), s1.cpu().numpy(), a_ref, as_ref, f"aqg {M}x{K}")
+    mi, ni = tile_samples(M, N, 2, seed=K)
+    ref = oracle.gemm_at(a_ref, as_ref, b, b_s, mi, ni)
+    assert_gemm_close(host_bf16_f64(c1)[mi, ni], ref, f"aqg {M}x{N}x{K}")
+
+
+def test_act_quant_gemm_without_workspace():
+    x = synth.activations(16, 1024, seed=4, name="aqgA")
+    b, b_s = synth.weights(512, 1024, seed=5, name="aqgB")
+    xt, bt, bst = dev_bf16(x), dev_e4m3(b), dev_f32(b_s)
+    c0, y0, s0 = separate_act_quant_gemm(xt, bt, bst, "fp32", None)
+    c1, y1, s1 = fp8bs.act_quant_gemm(xt, bt, bst, "fp32", workspace=None)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c0.view(torch.int16))
+    assert torch.equal(y1.view(torch.uint8), y0.view(torch.uint8))
+
+
 # ------------------------------------------------------------------------------ bounded waits
 
 def test_bounded_wait_reports_instead_of_hanging():
