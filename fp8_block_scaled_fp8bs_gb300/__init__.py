@@ -39,7 +39,7 @@ GEMM_WEIGHTS_CONSTANT = 0x1
 GEMM_QUANT_IN_KERNEL = 0x2
 EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_ex",
            "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_noalloc",
-           "fp8bs_act_quant_gemm",
+           "fp8bs_act_quant_gemm", "fp8bs_linear_bf16",
            "fp8bs_gemm_grouped",
            "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
 
@@ -72,6 +72,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_gemm_ws.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint, vp,
                                       ctypes.c_size_t, vp]
         lib.fp8bs_gemm_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
+        lib.fp8bs_linear_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_uint, vp]
         lib.fp8bs_act_quant_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                              ctypes.c_uint, vp, ctypes.c_size_t, vp]
         lib.fp8bs_gemm_noalloc.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint,
@@ -129,6 +130,10 @@ def fp8bs_act_quant_gemm(x, y, s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flag
                          workspace=0, workspace_bytes=0, stream=0) -> None:
     _check("fp8bs_act_quant_gemm", load().fp8bs_act_quant_gemm(
         x, y, s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes, stream))
+
+
+def fp8bs_linear_bf16(x, w, w_s, y, M, N, K, flags=0, stream=0) -> None:
+    _check("fp8bs_linear_bf16", load().fp8bs_linear_bf16(x, w, w_s, y, M, N, K, flags, stream))
 
 
 def fp8bs_gemm_workspace_size() -> int:
@@ -273,6 +278,22 @@ def act_quant_gemm(x, b, b_s, scale_fmt="fp32", weights_constant=False, workspac
                          c.data_ptr(), M, N, K, _fmt(scale_fmt), flags, ws_ptr, ws_bytes,
                          _stream())
     return c, y, s
+
+
+def linear_bf16(x, w, w_s, weights_constant=False, out=None):
+    """bf16 path of linear(): x bf16 [M,K] . bf16(dequant(w, w_s))^T -> y bf16 [M,N]."""
+    import torch
+    _require(x, torch.bfloat16, 2, "x")
+    _require(w, torch.float8_e4m3fn, 2, "w")
+    _require(w_s, torch.float32, 2, "w_s")
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K or tuple(w_s.shape) != (-(-N // BLOCK), -(-K // BLOCK)):
+        raise ValueError("operand or scale shapes do not match")
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    fp8bs_linear_bf16(x.data_ptr(), w.data_ptr(), w_s.data_ptr(), y.data_ptr(), M, N, K,
+                      GEMM_WEIGHTS_CONSTANT if weights_constant else 0, _stream())
+    return y
 
 
 def fp8_gemm_grouped(a, a_s, b, b_s, row_offsets, scale_fmt="fp32", out=None):

@@ -70,6 +70,22 @@ bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int b
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Over a row-major bf16 matrix [rows, K], box {64 elements (128 bytes), box_rows}, 128-byte
+// swizzle: the K-major layout of a bf16 MMA operand, one 64-wide half of a K block per box.
+bool make_map_bf16_sw128(CUtensorMap* map, const void* base, int64_t rows, int64_t K,
+                         int box_rows) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // The same over a row-major bf16 matrix [rows, K], box {128 elements, box_rows}, no swizzle
 // (the decode GEMM quantises these rows itself).
 bool make_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
@@ -312,6 +328,33 @@ int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b, const 
     if (int st2 = status_of(fp8bs::launch_act_quant(x, y, s, M, K, ue8m0, sms, st))) return st2;
     return gemm_impl(y, s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes,
                      stream);
+}
+
+int fp8bs_linear_bf16(const void* x, const void* w, const float* w_s, void* y, int64_t M,
+                      int64_t N, int64_t K, unsigned int flags, void* stream) {
+    if ((flags & ~FP8BS_GEMM_WEIGHTS_CONSTANT) != 0) return FP8BS_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return FP8BS_OK;
+    if (!y) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(y)) return FP8BS_ERR_MISALIGNED;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int sms = 0;
+    if (K == 0) {
+        if (int e = check_device(&sms)) return e;
+        return status_of(cudaMemsetAsync(y, 0, static_cast<size_t>(M * N) * 2, st));
+    }
+    if (!x || !w || !w_s) return FP8BS_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(w) || !aligned4(w_s)) return FP8BS_ERR_MISALIGNED;
+    if (int e = check_device(&sms)) return e;
+    if (M > 64) return FP8BS_ERR_INVALID_ARG;
+    const int MT = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    CUtensorMap tmW, tmX;
+    if (!make_map(&tmW, w, N, K, 128) || !make_map_bf16_sw128(&tmX, x, M, K, MT))
+        return FP8BS_ERR_CUDA;
+    return status_of(fp8bs::launch_linear_bf16_swap(
+        tmW, tmX, w_s, y, static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), MT,
+        (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0, st));
 }
 
 int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b, const float* b_s,

@@ -24,13 +24,14 @@ cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream) {
 }
 
 cudaError_t read_device_error(unsigned int* out, bool clear, cudaStream_t stream) {
-    unsigned int words[4] = {0, 0, 0, 0};
+    unsigned int words[5] = {0, 0, 0, 0, 0};
     cudaError_t e = read_tu_error(&words[0], clear, stream);
     if (e == cudaSuccess) e = read_error_tn(&words[1], clear, stream);
     if (e == cudaSuccess) e = read_error_bs(&words[2], clear, stream);
     if (e == cudaSuccess) e = read_error_swapab(&words[3], clear, stream);
+    if (e == cudaSuccess) e = read_error_linear(&words[4], clear, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    *out = words[0] | words[1] | words[2] | words[3];
+    *out = words[0] | words[1] | words[2] | words[3] | words[4];
     return e;
 }
 

@@ -114,6 +114,13 @@ cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
                                const GemmArgs& g, int MT, const FusedQuant& fq,
                                cudaStream_t stream);
 
+// bf16 path, decode orientation (M <= 64, MT = 16, 32 or 64): y bf16 [M, N] = x . W'^T with W'
+// the bf16 dequantisation of the e4m3 weight (128 x 128 block scales w_s). tmW: box {128, 128}
+// over W [N, K] (128-byte swizzle); tmX: bf16 map over x [M, K], box {64, MT}, 128-byte swizzle.
+cudaError_t launch_linear_bf16_swap(const CUtensorMap& tmW, const CUtensorMap& tmX,
+                                    const float* w_s, void* y, int M, int N, int K, int MT,
+                                    int weights_constant, cudaStream_t stream);
+
 // Diagnostic kernel: one wait on a barrier nothing signals (see fp8bs_probe_wait_timeout).
 cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream);
 
@@ -123,5 +130,6 @@ cudaError_t read_device_error(unsigned int* out, bool clear, cudaStream_t stream
 cudaError_t read_error_tn(unsigned int* out, bool clear, cudaStream_t stream);
 cudaError_t read_error_bs(unsigned int* out, bool clear, cudaStream_t stream);
 cudaError_t read_error_swapab(unsigned int* out, bool clear, cudaStream_t stream);
+cudaError_t read_error_linear(unsigned int* out, bool clear, cudaStream_t stream);
 
 }  // namespace fp8bs

@@ -179,6 +179,17 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
+// D[tmem] (+)= A * B^T for bf16 operands (kind::f16, K = 16 per instruction); one thread issues.
+__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                         uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with ue8m0 scale factors read from TMEM, one per 32
 // elements of K per row of A and per row of B (kind::mxf8f6f4, scale_vec::1X); one thread issues.
 __device__ __forceinline__ void mma_f8_block_scaled(uint32_t d_tmem, uint64_t a_desc,
@@ -211,6 +222,32 @@ __device__ __forceinline__ void tmem_st_4cols(uint32_t taddr, uint32_t w0, uint3
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
                  "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                  : "memory");
+}
+
+// Write 32 consecutive 32-bit TMEM columns of the warp's 32 lanes (thread t: lane base + t).
+__device__ __forceinline__ void tmem_st_32cols(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]),
+        "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]),
+        "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B^T for bf16 operands (kind::f16, K = 16): A from TMEM, lane = row,
+// each 32-bit column two consecutive K elements; B from shared memory. One thread issues.
+__device__ __forceinline__ void mma_bf16_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() {
@@ -319,6 +356,15 @@ __host__ __device__ constexpr uint32_t idesc_e4m3_f32(uint32_t M, uint32_t N) {
            | (0u << 10)           // B format: e4m3
            | (0u << 15)           // A K-major
            | (0u << 16)           // B K-major
+           | ((N >> 3) << 17)     // N / 8
+           | ((M >> 4) << 24);    // M / 16
+}
+
+// Instruction descriptor for kind::f16: D = fp32, A = B = bf16, both K-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(uint32_t M, uint32_t N) {
+    return (1u << 4)              // D format: f32
+           | (1u << 7)            // A format: bf16
+           | (1u << 10)           // B format: bf16
            | ((N >> 3) << 17)     // N / 8
            | ((M >> 4) << 24);    // M / 16
 }

@@ -193,6 +193,27 @@ FP8BS_API int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void*
                                    size_t workspace_bytes, void* stream);
 
 /*
+ * fp8bs_linear_bf16 -- the bf16 path of linear() with an FP8 weight: y = x . W'^T, where W' is
+ * the bf16 weight fp8bs_weight_dequant would produce from w and w_s ("DeepSeek-V3
+ * Administrator & Developer Guide", §6.3: with gemm_impl = "bf16", weight_dequant (§8.5.2)
+ * then a bf16 GEMM). W' is formed tile by tile in shared memory, never in HBM; products are
+ * accumulated in fp32 on the tensor cores and y is rounded once to bf16.
+ *
+ *   x    [in]  bf16 [M, K], 16-byte aligned.
+ *   w    [in]  e4m3 [N, K], 16-byte aligned.
+ *   w_s  [in]  fp32 [ceil(N/128), K/128], 4-byte aligned.
+ *   y    [out] bf16 [M, N], 16-byte aligned.
+ *   M >= 0, N >= 0, K >= 0 with K % 128 == 0.
+ *   flags: 0 or FP8BS_GEMM_WEIGHTS_CONSTANT (as in fp8bs_gemm_ex).
+ *
+ * Accuracy: |y - y_exact| <= 2^-7 |y_exact| + 1e-3 rms(y_exact) elementwise, y_exact the
+ * product of x with W' in exact arithmetic.
+ */
+FP8BS_API int fp8bs_linear_bf16(const void* x, const void* w, const float* w_s, void* y,
+                                int64_t M, int64_t N, int64_t K, unsigned int flags,
+                                void* stream);
+
+/*
  * fp8bs_gemm_noalloc -- fp8bs_gemm_ws on a workspace that the library keeps in a static device
  * array (about 10.5 MB per device, reserved when the library's device code is loaded): no
  * memory is allocated by the caller or by the library at any time. The pages have no

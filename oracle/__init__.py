@@ -190,3 +190,20 @@ def gemm_at(a, a_s, b, b_s, mi, ni) -> np.ndarray:
                            _ptr(mi, ctypes.c_int64), _ptr(ni, ctypes.c_int64), mi.size,
                            _ptr(out, ctypes.c_double), M, N, K)
     return out
+
+
+def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:
+    """bf16 bit patterns (uint16) -> their values as float64 (exact)."""
+    b = np.ascontiguousarray(bits, dtype=np.uint16)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def linear_bf16(x: np.ndarray, w: np.ndarray, w_s: np.ndarray) -> np.ndarray:
+    """The bf16 path of linear() ("DeepSeek-V3 Administrator & Developer Guide", §6.3,
+    gemm_impl = "bf16"): the weight dequantised to bf16 as weight_dequant does (§8.5.2), then
+    x . W'^T. x: uint16 [M,K] bf16 bits, w: uint8 [N,K] codes, w_s: float32 scales ->
+    float64 [M,N], the exact product (binary64 matmul of bf16 values: every product is exact
+    and K <= 2^16 sums of them stay within binary64's 53 bits to well below the tolerance)."""
+    wd = bf16_bits_to_f64(weight_dequant(w, w_s))
+    xd = bf16_bits_to_f64(x)
+    return xd @ wd.T

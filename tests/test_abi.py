@@ -174,3 +174,15 @@ def test_gemm_workspace_size_without_a_gpu(lib):
 ])
 def test_act_quant_gemm_argument_checks(lib, args, expect):
     assert lib.fp8bs_act_quant_gemm(*args, None, 0, None) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, C16, 8, 256, 200, 0), INVALID),      # K % 128
+    ((A16, B16, C16, C16, 8, 256, 256, 0x2), INVALID),    # unknown flag
+    ((A16 + 2, B16, C16, C16, 8, 256, 256, 0), MISALIGNED),
+    ((A16, B16, C16 + 2, C16, 8, 256, 256, 0), MISALIGNED),
+    ((A16, None, C16, C16, 8, 256, 256, 0), INVALID),
+    ((None, None, None, None, 0, 256, 256, 0), OK),
+])
+def test_linear_bf16_argument_checks(lib, args, expect):
+    assert lib.fp8bs_linear_bf16(*args, None) == expect

@@ -273,3 +273,43 @@ def test_gemm_at_agrees_with_full_gemm():
     mi = np.array([0, 19, 7, 13], np.int64)
     ni = np.array([0, 129, 128, 64], np.int64)
     assert np.array_equal(oracle.gemm_at(a, a_s, b, b_s, mi, ni), c[mi, ni])
+
+
+# ------------------------------------------------------------------------------ bf16 path
+
+def test_linear_bf16_identity_rows_select_dequantised_weights():
+    """x = rows of the identity: y[i, n] = W'[n, i], the bf16 weight_dequant output (pins the
+    transposition, the scale indexing and the dequantisation in one go)."""
+    K, N = 256, 300
+    w, w_s = synth.weights(N, K, seed=31, name="linpin")
+    eye = np.zeros((K, K), dtype=np.float32)
+    np.fill_diagonal(eye, 1.0)
+    x = synth.to_bf16_bits(eye)
+    y = oracle.linear_bf16(x, w, w_s)
+    wd = oracle.bf16_bits_to_f64(oracle.weight_dequant(w, w_s))
+    assert np.array_equal(y, wd.T)
+
+
+def test_linear_bf16_matches_block_scaled_gemm_when_both_are_exact():
+    """With power-of-two weight scales the bf16 weight is exact (code x 2^e fits bf16), and x
+    chosen on the e4m3 grid equals its own act_quant codes at scale 1: then the bf16 path and
+    the block-scaled GEMM compute the same sum."""
+    M, N, K = 7, 260, 384
+    rng = np.random.default_rng(32)
+    codes = rng.integers(0, 256, size=(M, K), dtype=np.uint8)
+    codes[(codes & 0x7F) == 0x7F] = 0
+    xv = np.array([oracle.e4m3_decode(int(c)) for c in codes.ravel()]).reshape(M, K)
+    x = synth.to_bf16_bits(xv.astype(np.float32))            # e4m3 values are exact in bf16
+    w, w_s = synth.weights(N, K, seed=33, name="linpin", pow2=True)
+    a_s = np.ones((M, K // 128), dtype=np.float32)
+    np.testing.assert_allclose(oracle.linear_bf16(x, w, w_s), oracle.gemm(codes, a_s, w, w_s),
+                               rtol=1e-13, atol=0)
+
+
+def test_linear_bf16_single_block_closed_form():
+    """All-ones x against a weight of code 0x38 (1.0) with scale 2^-3: y = K / 8 exactly."""
+    M, N, K = 3, 128, 512
+    x = synth.to_bf16_bits(np.ones((M, K), dtype=np.float32))
+    w = np.full((N, K), 0x38, dtype=np.uint8)
+    w_s = np.full((1, K // 128), 0.125, dtype=np.float32)
+    assert np.all(oracle.linear_bf16(x, w, w_s) == K / 8)

@@ -552,6 +552,58 @@ def test_act_quant_gemm_without_workspace():
     assert torch.equal(y1.view(torch.uint8), y0.view(torch.uint8))
 
 
+# ------------------------------------------------------------------------------ bf16 path
+# fp8bs_linear_bf16: x . bf16(dequant(W))^T with the weight dequantised tile by tile in shared
+# memory; the oracle dequantises with weight_dequant's arithmetic and multiplies in binary64.
+
+@pytest.mark.parametrize("M,N,K", [
+    (1, 256, 128), (5, 576, 512), (16, 1000, 1024), (17, 384, 256), (40, 2048, 2048),
+    (64, 1536, 7168),
+])
+def test_linear_bf16_against_oracle(M, N, K):
+    x = synth.activations(M, K, seed=M + N, name="linA", outlier_frac=0.01)
+    w, w_s = synth.weights(N, K, seed=N + K, name="linB")
+    y = fp8bs.linear_bf16(dev_bf16(x), dev_e4m3(w), dev_f32(w_s))
+    torch.cuda.synchronize()
+    assert_gemm_close(host_bf16_f64(y), oracle.linear_bf16(x, w, w_s), f"bf16 path {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M", synth.DECODE_MS)
+def test_linear_bf16_decode_full_size(M):
+    w, w_s = synth.weights(synth.INTER, synth.DIM, seed=0, name="decode/B")
+    x = synth.decode(M)
+    y = fp8bs.linear_bf16(dev_bf16(x), dev_e4m3(w), dev_f32(w_s), weights_constant=True)
+    torch.cuda.synchronize()
+    assert_gemm_close(host_bf16_f64(y), oracle.linear_bf16(x, w, w_s), f"bf16 path decode M={M}")
+
+
+def test_linear_bf16_large_block_scales():
+    """Block scales of 2^8 and above take the conversion path of the dequantisers (the integer
+    decode would overflow); small and large scales mixed in one weight."""
+    M, N, K = 8, 384, 768
+    x = synth.activations(M, K, seed=6, name="linA")
+    w, w_s = synth.weights(N, K, seed=7, name="linB")
+    w_s = w_s.copy()
+    w_s[::2, ::2] = np.float32(300.0)
+    w_s[1, 1] = np.float32(2.0 ** 20)
+    y = fp8bs.linear_bf16(dev_bf16(x), dev_e4m3(w), dev_f32(w_s))
+    torch.cuda.synchronize()
+    assert_gemm_close(host_bf16_f64(y), oracle.linear_bf16(x, w, w_s), "large scales")
+
+
+def test_linear_bf16_deterministic_and_k_zero():
+    x = synth.activations(9, 1024, seed=2, name="linA")
+    w, w_s = synth.weights(640, 1024, seed=3, name="linB")
+    args = (dev_bf16(x), dev_e4m3(w), dev_f32(w_s))
+    y1, y2 = fp8bs.linear_bf16(*args), fp8bs.linear_bf16(*args)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    y = torch.full((4, 32), 1.0, dtype=torch.bfloat16, device="cuda")
+    fp8bs.fp8bs_linear_bf16(0, 0, 0, y.data_ptr(), 4, 32, 0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y).item() == 0
+
+
 # ------------------------------------------------------------------------------ bounded waits
 
 def test_bounded_wait_reports_instead_of_hanging():
