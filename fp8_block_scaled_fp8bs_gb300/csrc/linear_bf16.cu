@@ -1,21 +1,26 @@
 // linear_bf16.cu -- the bf16 path of linear() with FP8 weights: y = x . W'^T, where W' is the
 // bf16 weight that weight_dequant would produce ("DeepSeek-V3 Administrator & Developer Guide",
-// §6.3: with gemm_impl = "bf16" the FP8 weight is dequantised (§8.5.2) and a bf16 GEMM runs;
-// the weight is dequantised per tile in shared memory instead of being written to and read back
+// §6.3: with gemm_impl = "bf16" the FP8 weight is dequantised (§8.5.2) and a bf16 GEMM runs).
+// Here the weight is dequantised tile by tile on chip instead of being written to and read back
 // from HBM as bf16.
 //
 // Decode orientation (M <= 64): 128-row slabs of W take the MMA's M side, the MT rows of x its
 // N side; one CTA per slab streams its e4m3 weight (half the bytes of bf16 weights).
 //   warp 0          TMA producer of the deep ring: per K block the e4m3 weight tile (the HBM
 //                   stream) and the bf16 rows of x (128-byte swizzle, two 64-wide halves)
-//   warp 1          MMA issuer: 8 x tcgen05.mma kind::f16 (K = 16) per K block into one TMEM
-//                   accumulator for the whole K loop (the block scale is inside W')
-//   warps 2 .. 5    epilogue: the accumulator to bf16 y
-//   warps 6 .. 13   dequantisers: per K block, e4m3 tile -> bf16 W' tile (fp32 product with
+//   warps 1, 2      MMA issuers, K block kb to issuer kb % 2: 8 x tcgen05.mma kind::f16
+//                   (K = 16) per K block into the issuer's own TMEM accumulator for the whole
+//                   K loop (the block scale is inside W'). One thread issuing alone is held
+//                   to about one small MMA per 60-80 clk and stalls at its next barrier wait
+//                   until the tensor core has caught up; two issuers keep the pipe fed.
+//   warps 2 .. 5    epilogue: the sum of the accumulators to bf16 y
+//   warps 6 .. 21   dequantisers, two groups of eight taking K blocks in turn (a warp's barrier
+//                   waits and arrivals cost a few hundred clk per K block, which the other
+//                   group overlaps): e4m3 tile -> bf16 W' tile (fp32 product with
 //                   the block scale, rounded to bf16: weight_dequant's arithmetic) written
 //                   straight into TMEM with tcgen05.st (lane = weight row, 32-bit column =
 //                   two consecutive K), where the MMA takes its A operand: a second, shallow
-//                   ring of two 64-column slots. W' never touches shared memory, which the
+//                   ring of four 64-column slots. W' never touches shared memory, which the
 //                   TMA stream, the dequantisers' reads and the MMA's reads of x already share.
 // A slot of the deep ring is free once the dequantisers have read its weight tile and the MMA
 // has read its rows of x.
@@ -31,16 +36,21 @@ namespace {
 template <int MT>
 struct LinCfg {
     static constexpr int EPI_WARPS = 4;
-    static constexpr int DQ_WARPS = 8;
+    static constexpr int DQ_GROUP = 8;                   // dequantiser warps per K block
+    static constexpr int DQ_GROUPS = 2;                  // groups, taking K blocks in turn
+    static constexpr int DQ_WARPS = DQ_GROUP * DQ_GROUPS;
     static constexpr int DQ0 = 2 + EPI_WARPS;            // first dequantiser warp
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + DQ_WARPS);
     static constexpr int WQ_TILE = BM * BK;              // e4m3 weight tile (128 x 128)
     static constexpr int HALF = 64;                      // bf16 K elements per 128-byte row
     static constexpr int XB_TILE = MT * BK * 2;          // bf16 activation tile: two halves
     static constexpr int A_SLOT = WQ_TILE + XB_TILE;     // deep ring: weight codes + rows of x
-    static constexpr int W_COL0 = 64;                    // TMEM: accumulator in 0 .. MT-1, then
-    static constexpr int W_COLS = BK / 2;                // W' slots of 64 columns (bf16 pairs)
-    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr int ISSUERS = 2;                    // MMA issuers: warps 1 .. ISSUERS
+    static constexpr int ACC_COLS = 64;                  // TMEM: accumulator i at 64 i ..,
+    static constexpr int W_COL0 = ISSUERS * ACC_COLS;    // then the W' slots of 64 columns
+    static constexpr int W_COLS = BK / 2;                // (bf16 pairs)
+    static constexpr int SB = 4;                         // W' slots
+    static constexpr uint32_t TMEM_COLS = 512;
 };
 
 // Eight e4m3 codes (one 64-bit word) -> eight bf16 (four words): fp32(code) * scale, rounded to
@@ -64,6 +74,18 @@ __device__ __forceinline__ void dequant8(uint32_t lo, uint32_t hi, float sc, uin
     }
 }
 
+// `CW` (16 or 32) consecutive TMEM columns of this warp's lane quarter into registers.
+template <int CW>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float* v) {
+    if constexpr (CW == 32) {
+        tmem_ld_32cols(taddr, v);
+        tmem_wait_ld_32(v);
+    } else {
+        tmem_ld_16cols(taddr, v);
+        tmem_wait_ld_16(v);
+    }
+}
+
 // Byte offset of 16-byte chunk `c` (0..7) of row `r` in a 128-byte-swizzled tile (8-row atoms
 // of 1024 bytes: the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B).
 __device__ __forceinline__ int sw128(int r, int c) {
@@ -75,7 +97,7 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     linear_bf16_swap_kernel(const __grid_constant__ CUtensorMap tmW,
                             const __grid_constant__ CUtensorMap tmX,
                             const float* __restrict__ w_s, void* y, const int M, const int N,
-                            const int K, const int sa, const int sb, const int weights_constant) {
+                            const int K, const int sa, const int weights_constant) {
     using Cfg = LinCfg<MT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -83,8 +105,8 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     uint64_t* fullA = reinterpret_cast<uint64_t*>(sA + sa * Cfg::A_SLOT);
     uint64_t* emptyA = fullA + sa;
     uint64_t* deqB = emptyA + sa;
-    uint64_t* emptyB = deqB + sb;
-    uint64_t* tfull = emptyB + sb;
+    uint64_t* emptyB = deqB + Cfg::SB;
+    uint64_t* tfull = emptyB + Cfg::SB;
     uint64_t* drain = tfull + 1;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
 
@@ -101,14 +123,14 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < sa; ++i) {
             mbar_init(&fullA[i], 1);
-            mbar_init(&emptyA[i], Cfg::DQ_WARPS + 1);   // dequantisers + the MMA's commit
+            mbar_init(&emptyA[i], Cfg::DQ_GROUP + 1);   // dequantisers + the MMA's commit
         }
-        for (int i = 0; i < sb; ++i) {
-            mbar_init(&deqB[i], Cfg::DQ_WARPS);
+        for (int i = 0; i < Cfg::SB; ++i) {
+            mbar_init(&deqB[i], Cfg::DQ_GROUP);
             mbar_init(&emptyB[i], 1);
         }
-        mbar_init(tfull, 1);
-        mbar_init(drain, 1);
+        mbar_init(tfull, Cfg::ISSUERS);
+        mbar_init(drain, Cfg::ISSUERS);
         fence_barrier_init();
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
@@ -126,6 +148,40 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+
+    if (warp >= 1 && warp <= Cfg::ISSUERS && lane == 0) {
+        // MMA issuer: K blocks kb = warp - 1, warp - 1 + ISSUERS, ... into accumulator warp - 1.
+        // The dequantisers waited for the stage's TMA before signalling deqB, so deqB alone
+        // says that both the weight slot in TMEM and the rows of x in shared memory are ready.
+        constexpr uint32_t idesc = idesc_bf16_f32(BM, MT);
+        const int me = warp - 1;
+        const uint32_t acc = tmem_base + static_cast<uint32_t>(me * Cfg::ACC_COLS);
+        int a = me;                                       // stage of kb (me < sa)
+        for (int kb = me; kb < num_kb; kb += Cfg::ISSUERS) {
+            const int b = kb % Cfg::SB;
+            if (!mbar_wait(&deqB[b], static_cast<uint32_t>((kb / Cfg::SB) & 1))) {
+                record_error(FP8BS_DEVERR_MMA_WAIT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t w_tmem = tmem_base + static_cast<uint32_t>(Cfg::W_COL0 + b * Cfg::W_COLS);
+            const uint32_t x_addr = smem_addr(sA + a * Cfg::A_SLOT + Cfg::WQ_TILE);
+#pragma unroll
+            for (int j = 0; j < BK / 16; ++j) {
+                const uint32_t h = j / 4, o = (j % 4) * 32;   // 64-wide half, 16-wide step
+                mma_bf16_ta(acc, w_tmem + 8 * j, smem_desc_k_sw128(x_addr + h * (MT * 128) + o),
+                            idesc, (kb > me || j > 0) ? 1u : 0u);
+            }
+            mma_commit(&emptyB[b]);
+            mma_commit(&emptyA[a]);
+            a += Cfg::ISSUERS;                            // ISSUERS < sa: at most one wrap
+            if (a >= sa) a -= sa;
+        }
+        mma_commit(tfull);
+        mma_commit(drain);
+        if (!mbar_wait(drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
+    }
+    __syncwarp();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -167,58 +223,30 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
                 }
             }
         }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            constexpr uint32_t idesc = idesc_bf16_f32(BM, MT);
-            int a = 0, b = 0;
-            uint32_t pa = 0, pb = 0;
-            for (int kb = 0; kb < num_kb; ++kb) {
-                if (!mbar_wait(&deqB[b], pb) || !mbar_wait(&fullA[a], pa)) {
-                    record_error(FP8BS_DEVERR_MMA_WAIT);
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t w_tmem =
-                    tmem_base + static_cast<uint32_t>(Cfg::W_COL0 + b * Cfg::W_COLS);
-                const uint32_t x_addr = smem_addr(sA + a * Cfg::A_SLOT + Cfg::WQ_TILE);
-#pragma unroll
-                for (int j = 0; j < BK / 16; ++j) {
-                    const uint32_t h = j / 4, o = (j % 4) * 32;   // 64-wide half, 16-wide step
-                    mma_bf16_ta(tmem_base, w_tmem + 8 * j,
-                                smem_desc_k_sw128(x_addr + h * (MT * 128) + o), idesc,
-                                (kb > 0 || j > 0) ? 1u : 0u);
-                }
-                mma_commit(&emptyB[b]);
-                mma_commit(&emptyA[a]);
-                if (++b == sb) {
-                    b = 0;
-                    pb ^= 1;
-                }
-                if (++a == sa) {
-                    a = 0;
-                    pa ^= 1;
-                }
-            }
-            mma_commit(tfull);
-            mma_commit(drain);
-            if (!mbar_wait(drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
-        }
     } else if (warp >= Cfg::DQ0) {
-        // Dequantisers: warp w handles the TMEM lane quarter w % 4 (weight rows 32 (w % 4) ..
-        // +31, one per lane) and one 64-wide half of the K block; each lane converts the 64
-        // codes of its row's half and stores them as 32 columns of bf16 pairs.
+        // Dequantisers: group g takes the K blocks kb with kb % 2 == g. Warp w handles the TMEM
+        // lane quarter w % 4 (weight rows 32 (w % 4) .. +31, one per lane) and one 64-wide half
+        // of the K block; each lane converts the 64 codes of its row's half and stores them as
+        // 32 columns of bf16 pairs.
+        const int group = (warp - Cfg::DQ0) / Cfg::DQ_GROUP;
         const int quarter = warp & 3;
-        const int khalf = (warp - Cfg::DQ0) >> 2;
+        const int khalf = ((warp - Cfg::DQ0) >> 2) & 1;
         const int r = quarter * 32 + lane;
-        int a = 0, b = 0;
-        uint32_t pa = 0, pb = 0;
-        for (int kb = 0; kb < num_kb; ++kb) {
-            if (!warp_wait(&emptyB[b], pb ^ 1) || !warp_wait(&fullA[a], pa)) {
+        const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(Cfg::W_COL0 + 32 * khalf);
+        float sc_next = group < num_kb ? __ldg(ws_row + group) : 0.f;
+        int a = group;                                  // stage of kb (group < sa)
+        uint32_t pa = 0;
+        for (int kb = group; kb < num_kb; kb += Cfg::DQ_GROUPS) {
+            const int b = kb % Cfg::SB;
+            const float sc = sc_next;                   // the block scale, fetched one step early
+            if (kb + Cfg::DQ_GROUPS < num_kb) sc_next = __ldg(ws_row + kb + Cfg::DQ_GROUPS);
+            if (!warp_wait(&emptyB[b], static_cast<uint32_t>(((kb / Cfg::SB) & 1) ^ 1)) ||
+                !warp_wait(&fullA[a], pa)) {
                 if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                 break;
             }
             tc_fence_after();
-            const float sc = __ldg(ws_row + kb);
             const uint8_t* qslot = sA + a * Cfg::A_SLOT;
             uint32_t o[32];
 #pragma unroll
@@ -227,9 +255,7 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
                 dequant8(v.x, v.y, sc, o + 8 * i);
                 dequant8(v.z, v.w, sc, o + 8 * i + 4);
             }
-            tmem_st_32cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                               static_cast<uint32_t>(Cfg::W_COL0 + b * Cfg::W_COLS + 32 * khalf),
-                           o);
+            tmem_st_32cols(lane_base + static_cast<uint32_t>(b * Cfg::W_COLS), o);
             tmem_wait_st();
             tc_fence_before();
             __syncwarp();
@@ -237,37 +263,40 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
                 mbar_arrive(&emptyA[a]);
                 mbar_arrive(&deqB[b]);
             }
-            if (++a == sa) {
-                a = 0;
+            a += Cfg::DQ_GROUPS;                        // DQ_GROUPS < sa: at most one wrap
+            if (a >= sa) {
+                a -= sa;
                 pa ^= 1;
             }
-            if (++b == sb) {
-                b = 0;
-                pb ^= 1;
-            }
         }
-    } else {
-        // Epilogue: TMEM lane = output column n0 + 32 * quarter + lane, columns = rows of x.
+    } else if (warp >= 2) {
+        // Epilogue: TMEM lane = output column n0 + 32 * quarter + lane, columns = rows of x;
+        // y = acc 0 + acc 1 in fp32 (accumulator i holds the K blocks kb with kb % 2 == i).
         const int quarter = warp & 3;
         const int n = n0 + quarter * 32 + lane;
         if (warp_wait(tfull, 0)) {
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            float acc[MT];
-            if constexpr (MT >= 32) {
+            const int used = min(num_kb, Cfg::ISSUERS);   // accumulators that were written
+            constexpr int CW = MT < 32 ? MT : 32;          // columns (rows of x) per chunk
+            __nv_bfloat16* yc = static_cast<__nv_bfloat16*>(y);
+#pragma unroll 1
+            for (int c = 0; c < MT / CW; ++c) {
+                float acc[CW];
+                tmem_ld_cols<CW>(taddr + CW * c, acc);
+                for (int i = 1; i < used; ++i) {
+                    float t[CW];
+                    tmem_ld_cols<CW>(taddr + i * Cfg::ACC_COLS + CW * c, t);
 #pragma unroll
-                for (int c = 0; c < MT / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
+                    for (int j = 0; j < CW; ++j) acc[j] += t[j];
+                }
+                if (n < N) {
 #pragma unroll
-                for (int c = 0; c < MT / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
-            } else {
-                tmem_ld_16cols(taddr, acc);
-                tmem_wait_ld_16(acc);
-            }
-            if (n < N) {
-                __nv_bfloat16* yc = static_cast<__nv_bfloat16*>(y);
-#pragma unroll
-                for (int j = 0; j < MT; ++j)
-                    if (m0 + j < M) yc[static_cast<int64_t>(m0 + j) * N + n] = __float2bfloat16_rn(acc[j]);
+                    for (int j = 0; j < CW; ++j) {
+                        const int m = m0 + CW * c + j;
+                        if (m < M) yc[static_cast<int64_t>(m) * N + n] = __float2bfloat16_rn(acc[j]);
+                    }
+                }
             }
         } else if (lane == 0) {
             record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
@@ -284,9 +313,8 @@ template <int MT>
 cudaError_t launch_lin(const CUtensorMap& tmW, const CUtensorMap& tmX, const float* w_s, void* y,
                        int M, int N, int K, int weights_constant, cudaStream_t stream) {
     using Cfg = LinCfg<MT>;
-    // a shallow bf16 ring (two slots), the rest of shared memory for the e4m3 weight stream
-    const int sb = 2;                              // W' slots in TMEM
-    const int bar_bytes = 8 * (2 * kMaxStages + 2 * sb + 2) + 16;
+    // the W' ring lives in TMEM; shared memory holds the e4m3 weight stream and the rows of x
+    const int bar_bytes = 8 * (2 * kMaxStages + 2 * Cfg::SB + 2) + 16;
     int sa = (kSmemLimit - 1024 - bar_bytes) / Cfg::A_SLOT;
     if (sa > kMaxStages) sa = kMaxStages;
     if (sa < 2) return cudaErrorInvalidValue;
@@ -295,7 +323,7 @@ cudaError_t launch_lin(const CUtensorMap& tmW, const CUtensorMap& tmX, const flo
     if (e != cudaSuccess) return e;
     const dim3 grid((N + BM - 1) / BM, (M + MT - 1) / MT);
     return launch_pdl(linear_bf16_swap_kernel<MT>, grid, Cfg::THREADS, smem, stream, tmW, tmX,
-                      w_s, y, M, N, K, sa, sb, weights_constant);
+                      w_s, y, M, N, K, sa, weights_constant);
 }
 
 }  // namespace

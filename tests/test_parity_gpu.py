@@ -553,12 +553,15 @@ def test_act_quant_gemm_without_workspace():
 
 
 # ------------------------------------------------------------------------------ bf16 path
-# fp8bs_linear_bf16: x . bf16(dequant(W))^T with the weight dequantised tile by tile in shared
-# memory; the oracle dequantises with weight_dequant's arithmetic and multiplies in binary64.
+# fp8bs_linear_bf16: x . bf16(dequant(W))^T with the weight dequantised tile by tile on chip;
+# the oracle dequantises with weight_dequant's arithmetic and multiplies in binary64.
 
 @pytest.mark.parametrize("M,N,K", [
     (1, 256, 128), (5, 576, 512), (16, 1000, 1024), (17, 384, 256), (40, 2048, 2048),
     (64, 1536, 7168),
+    (40, 128, 384),       # three K blocks: the two accumulators and dequantiser groups unequal
+    (64, 128, 640),       # five K blocks
+    (3, 256, 896),        # seven K blocks
 ])
 def test_linear_bf16_against_oracle(M, N, K):
     x = synth.activations(M, K, seed=M + N, name="linA", outlier_frac=0.01)
@@ -578,8 +581,8 @@ def test_linear_bf16_decode_full_size(M):
 
 
 def test_linear_bf16_large_block_scales():
-    """Block scales of 2^8 and above take the conversion path of the dequantisers (the integer
-    decode would overflow); small and large scales mixed in one weight."""
+    """Block scales of 2^8 and above, mixed with small ones in one weight: the dequantisers'
+    fp32 product and bf16 rounding must hold at any finite scale."""
     M, N, K = 8, 384, 768
     x = synth.activations(M, K, seed=6, name="linA")
     w, w_s = synth.weights(N, K, seed=7, name="linB")
