@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "a4b0791a5177531a", "per_launch_mb": (135.02 + 135.41) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "25cfcbdd7c8351e7", "per_launch_mb": (134.95 + 135.46) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -64,6 +64,11 @@ def gemm_bytes(M, N, K):
 
 def dequant_bytes(N, K):
     return N * K + 4 * (-(-N // 128)) * (-(-K // 128)) + 2 * N * K
+
+
+def linear_bf16_bytes(M, N, K):
+    """bf16 path: x bf16 + the e4m3 weight and its block scales + y bf16."""
+    return 2 * M * K + N * K + 4 * (-(-N // 128)) * (K // 128) + 2 * M * N
 
 
 def gemm_flops(M, N, K):
@@ -238,6 +243,10 @@ class Gpu:
 
     def dequant(self, w, s, y, N, K):
         self.fp8bs.fp8bs_weight_dequant(w.data_ptr(), s.data_ptr(), y.data_ptr(), N, K, self.sh)
+
+    def linear_bf16(self, x, w, s, y, M, N, K, flags=0):
+        self.fp8bs.fp8bs_linear_bf16(x.data_ptr(), w.data_ptr(), s.data_ptr(), y.data_ptr(), M, N,
+                                     K, flags, self.sh)
 
     def time_each(self, fn, reps, flush=True):
         """Device time (ms) of one fn() launch with a cold L2: `reps` launches back to back,
@@ -414,7 +423,24 @@ def secondary(g: Gpu, peaks, reps=20):
     gbs = dequant_bytes(N_DIM, K_DIM) / ms / 1e6
     out["weight_dequant"] = {"N": N_DIM, "K": K_DIM, "us": round(ms * 1e3, 2),
                              "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4)}
-    del W, WS, Y, bc
+    del Y
+    # the bf16 path (weight dequantised on chip inside the GEMM) on the same weight: decode rows
+    # against HBM, the prefill rows against the bf16 tensor peak
+    bf16_peak = peaks["bf16_tflops"]
+    for M, bits in ((1, synth.decode(1)), (64, synth.decode(64)), (4096, synth.prefill_up())):
+        x = g.bf16(bits)
+        y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device="cuda")
+        for _ in range(3):
+            g.linear_bf16(x, W, WS, y, M, N_DIM, K_DIM)
+        ms = g.time_each(lambda: g.linear_bf16(x, W, WS, y, M, N_DIM, K_DIM), reps)
+        gbs = linear_bf16_bytes(M, N_DIM, K_DIM) / ms / 1e6
+        tf = 2 * M * N_DIM * K_DIM / ms / 1e9
+        out[f"linear_bf16_M{M}"] = {"M": M, "N": N_DIM, "K": K_DIM, "us": round(ms * 1e3, 2),
+                                    "GB/s": round(gbs, 1), "frac_hbm": round(gbs / hbm, 4),
+                                    "TFLOP/s": round(tf, 1),
+                                    "frac_bf16_peak": round(tf / bf16_peak, 4)}
+        del x, y
+    del W, WS, bc
     xb = synth.prefill_down()
     bc, bs = synth.weights(K_DIM, N_DIM, 0, "prefill/B_down")
     gemm_entry("prefill_down", 4096, K_DIM, N_DIM, 0, xb, bc, bs)
@@ -625,6 +651,14 @@ def run_profile(case: str, launches: int, warmup: int):
         fn = lambda: g.fp8bs.fp8bs_gemm_grouped(  # noqa: E731
             y.data_ptr(), s.data_ptr(), B.data_ptr(), S.data_ptr(), c.data_ptr(), offs, 32,
             synth.MOE_INTER, K_DIM, 0, g.sh)
+    elif case.startswith("linear"):
+        # the bf16 path: linear1 (decode row), linear64, linear4096 (prefill rows)
+        M = int(case[len("linear"):] or 1)
+        b, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up")
+        W, WS = g.e4m3(b), g.f32(bs)
+        x = g.bf16(synth.prefill_up()[:M] if M > 64 else synth.decode(M))
+        Y = torch.empty((M, N_DIM), dtype=torch.bfloat16, device="cuda")
+        fn = lambda: g.linear_bf16(x, W, WS, Y, M, N_DIM, K_DIM)  # noqa: E731
     elif case == "dequant":
         b, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up")
         W, WS = g.e4m3(b), g.f32(bs)
@@ -685,7 +719,7 @@ def main(argv=None):
                     "and no CPU baseline")
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
     ap.add_argument("--profile", metavar="CASE", default=None,
-                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, mla1536, mla576, "
+                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, mla1536, mla576, linear1..linear4096, "
                          "act_quant, dequant, moe): warmup + steps launches, for ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
