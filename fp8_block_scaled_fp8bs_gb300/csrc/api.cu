@@ -347,8 +347,7 @@ int fp8bs_linear_bf16(const void* x, const void* w, const float* w_s, void* y, i
     if (!x || !w || !w_s) return FP8BS_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(w) || !aligned4(w_s)) return FP8BS_ERR_MISALIGNED;
     if (int e = check_device(&sms)) return e;
-    if (M > 64) return FP8BS_ERR_INVALID_ARG;
-    const int MT = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
     CUtensorMap tmW, tmX;
     if (!make_map(&tmW, w, N, K, 128) || !make_map_bf16_sw128(&tmX, x, M, K, MT))
         return FP8BS_ERR_CUDA;

@@ -4,8 +4,10 @@
 // Here the weight is dequantised tile by tile on chip instead of being written to and read back
 // from HBM as bf16.
 //
-// Decode orientation (M <= 64): 128-row slabs of W take the MMA's M side, the MT rows of x its
-// N side; one CTA per slab streams its e4m3 weight (half the bytes of bf16 weights).
+// 128-row slabs of W take the MMA's M side, MT (16, 32, 64 or 128) rows of x its N side; each
+// CTA streams the e4m3 codes of one slab (half the bytes of the bf16 weight) against one tile of
+// x. CTAs that share a slab are adjacent in launch order, so for M > 128 a slab is read from
+// HBM about once and the other tiles of x find it in L2.
 //   warp 0          TMA producer of the deep ring: per K block the e4m3 weight tile (the HBM
 //                   stream) and the bf16 rows of x (128-byte swizzle, two 64-wide halves)
 //   warps 1, 2      MMA issuers, K block kb to issuer kb % 2: 8 x tcgen05.mma kind::f16
@@ -46,7 +48,7 @@ struct LinCfg {
     static constexpr int XB_TILE = MT * BK * 2;          // bf16 activation tile: two halves
     static constexpr int A_SLOT = WQ_TILE + XB_TILE;     // deep ring: weight codes + rows of x
     static constexpr int ISSUERS = 2;                    // MMA issuers: warps 1 .. ISSUERS
-    static constexpr int ACC_COLS = 64;                  // TMEM: accumulator i at 64 i ..,
+    static constexpr int ACC_COLS = MT > 64 ? MT : 64;   // TMEM: accumulator i at ACC_COLS i,
     static constexpr int W_COL0 = ISSUERS * ACC_COLS;    // then the W' slots of 64 columns
     static constexpr int W_COLS = BK / 2;                // (bf16 pairs)
     static constexpr int SB = 4;                         // W' slots
@@ -113,9 +115,11 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int num_kb = K / BK;
-    const int n0 = blockIdx.x * BM;
-    const int m0 = blockIdx.y * MT;
-    const float* ws_row = w_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+    const int m_tiles = (M + MT - 1) / MT;
+    const int slab = static_cast<int>(blockIdx.x) / m_tiles;
+    const int n0 = slab * BM;
+    const int m0 = (static_cast<int>(blockIdx.x) - slab * m_tiles) * MT;
+    const float* ws_row = w_s + static_cast<int64_t>(slab) * num_kb;
     const int prefill = min(sa, num_kb);
     const uint64_t stream = l2_policy_evict_first();  // weights: read once
     const uint64_t keep = l2_policy_evict_last();     // x: read by every CTA
@@ -321,7 +325,9 @@ cudaError_t launch_lin(const CUtensorMap& tmW, const CUtensorMap& tmX, const flo
     const int smem = 1024 + sa * Cfg::A_SLOT + bar_bytes;
     cudaError_t e = set_smem(linear_bf16_swap_kernel<MT>, smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid((N + BM - 1) / BM, (M + MT - 1) / MT);
+    const int64_t ctas = static_cast<int64_t>((N + BM - 1) / BM) * ((M + MT - 1) / MT);
+    if (ctas > INT32_MAX) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>(ctas));
     return launch_pdl(linear_bf16_swap_kernel<MT>, grid, Cfg::THREADS, smem, stream, tmW, tmX,
                       w_s, y, M, N, K, sa, weights_constant);
 }
@@ -335,6 +341,7 @@ cudaError_t launch_linear_bf16_swap(const CUtensorMap& tmW, const CUtensorMap& t
         case 16: return launch_lin<16>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
         case 32: return launch_lin<32>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
         case 64: return launch_lin<64>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
+        case 128: return launch_lin<128>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
         default: return cudaErrorInvalidValue;
     }
 }

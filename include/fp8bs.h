@@ -196,8 +196,9 @@ FP8BS_API int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void*
  * fp8bs_linear_bf16 -- the bf16 path of linear() with an FP8 weight: y = x . W'^T, where W' is
  * the bf16 weight fp8bs_weight_dequant would produce from w and w_s ("DeepSeek-V3
  * Administrator & Developer Guide", §6.3: with gemm_impl = "bf16", weight_dequant (§8.5.2)
- * then a bf16 GEMM). W' is formed tile by tile in shared memory, never in HBM; products are
- * accumulated in fp32 on the tensor cores and y is rounded once to bf16.
+ * then a bf16 GEMM). W' is formed tile by tile on chip (in tensor memory), never in HBM;
+ * products are accumulated in fp32 on the tensor cores and y is rounded once to bf16. Any M:
+ * each CTA pairs one 128-row slab of w with up to 128 rows of x.
  *
  *   x    [in]  bf16 [M, K], 16-byte aligned.
  *   w    [in]  e4m3 [N, K], 16-byte aligned.

@@ -562,6 +562,10 @@ def test_act_quant_gemm_without_workspace():
     (40, 128, 384),       # three K blocks: the two accumulators and dequantiser groups unequal
     (64, 128, 640),       # five K blocks
     (3, 256, 896),        # seven K blocks
+    (65, 256, 512),       # 128 rows of x per CTA from here on
+    (128, 384, 1024),
+    (200, 1000, 768),     # ragged in M and N
+    (1000, 640, 384),     # eight tiles of x share each slab
 ])
 def test_linear_bf16_against_oracle(M, N, K):
     x = synth.activations(M, K, seed=M + N, name="linA", outlier_frac=0.01)
@@ -578,6 +582,19 @@ def test_linear_bf16_decode_full_size(M):
     y = fp8bs.linear_bf16(dev_bf16(x), dev_e4m3(w), dev_f32(w_s), weights_constant=True)
     torch.cuda.synchronize()
     assert_gemm_close(host_bf16_f64(y), oracle.linear_bf16(x, w, w_s), f"bf16 path decode M={M}")
+
+
+def test_linear_bf16_prefill_sampled_rows():
+    """Prefill size (4096 x 18432 x 7168, 32 tiles of x per weight slab): sixteen rows,
+    first and last rows of tiles among them, against the oracle."""
+    x = synth.prefill_up()
+    w, w_s = synth.weights(synth.INTER, synth.DIM, seed=0, name="prefill/B_up")
+    y = fp8bs.linear_bf16(dev_bf16(x), dev_e4m3(w), dev_f32(w_s), weights_constant=True)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 1000, 2047, 2048, 2049, 3071, 3200, 3968, 4000, 4094,
+                     4095, 255, 513])
+    got = host_bf16_f64(y[torch.from_numpy(rows).to(y.device)])
+    assert_gemm_close(got, oracle.linear_bf16(x[rows], w, w_s), "bf16 path prefill rows")
 
 
 def test_linear_bf16_large_block_scales():
