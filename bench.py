@@ -448,7 +448,9 @@ def secondary(g: Gpu, peaks, reps=20):
 
     # act_quant at large row counts (MoE gathered rows; ue8m0 MLA input)
     for name, M, K, fmt, bits in (("act_quant_moe", 8192, K_DIM, 0, None),
-                                  ("act_quant_mla_ue8m0", 2048, K_DIM, 1, synth.mla_acts())):
+                                  ("act_quant_mla_ue8m0", 2048, K_DIM, 1, synth.mla_acts()),
+                                  ("act_quant_prefill_up", 4096, K_DIM, 0, synth.prefill_up()),
+                                  ("act_quant_prefill_down", 4096, N_DIM, 0, synth.prefill_down())):
         if bits is None:
             rows, _ = synth.moe_routing(0)
             bits = synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows]

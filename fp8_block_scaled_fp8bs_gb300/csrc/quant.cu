@@ -5,6 +5,8 @@
 // Both stream HBM once with 16-byte vector accesses. act_quant: 8 threads own one 128-element
 // block (16 bf16 = 32 bytes each), reduce |x| with 3 xor-shuffles inside the 8-lane group and
 // write 16 e4m3 codes (16 bytes) each; lane 0 of the group writes the block's fp32 scale.
+// act_quant issues the loads of two grid-stride steps before using either, so that enough
+// bytes are in flight per SM to cover HBM latency (64 bytes per thread).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -17,7 +19,8 @@ namespace fp8bs {
 namespace {
 
 // Grid-stride over groups of 16 elements; thread g handles x[16g .. 16g+15], which lie in
-// block g/8 (blocks are contiguous because K % 128 == 0).
+// block g/8 (blocks are contiguous because K % 128 == 0). Two steps per iteration: both
+// groups' loads are issued first.
 template <bool UE8M0>
 __global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict__ x,
                                                         uint4* __restrict__ y,
@@ -26,11 +29,39 @@ __global__ void __launch_bounds__(256) act_quant_kernel(const uint4* __restrict_
     grid_dependency_wait();
     grid_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    // Every lane of a warp runs the same number of iterations (num_groups is a multiple of 8
-    // and the grid covers whole warps), so the shuffles below are always full-warp.
+    const int lane = threadIdx.x & 31;
+    // Every lane of a warp takes the same branches (num_groups is a multiple of 8 and the grid
+    // covers whole warps; the tests below use the warp's first group), so the shuffles inside
+    // quant_block16 are always full-warp. Inactive lanes quantise zeros and store nothing.
     for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-         g - (threadIdx.x & 31) < num_groups; g += stride)
-        act_quant_group16<UE8M0>(x, y, s, g, g < num_groups);
+         g - lane < num_groups; g += 2 * stride) {
+        const int64_t g2 = g + stride;
+        const bool a1 = g < num_groups, a2 = g2 < num_groups;
+        uint32_t w1[8] = {}, w2[8] = {};
+        if (a1) {
+            const uint4 v0 = __ldcs(x + 2 * g), v1 = __ldcs(x + 2 * g + 1);
+            w1[0] = v0.x; w1[1] = v0.y; w1[2] = v0.z; w1[3] = v0.w;
+            w1[4] = v1.x; w1[5] = v1.y; w1[6] = v1.z; w1[7] = v1.w;
+        }
+        if (a2) {
+            const uint4 v0 = __ldcs(x + 2 * g2), v1 = __ldcs(x + 2 * g2 + 1);
+            w2[0] = v0.x; w2[1] = v0.y; w2[2] = v0.z; w2[3] = v0.w;
+            w2[4] = v1.x; w2[5] = v1.y; w2[6] = v1.z; w2[7] = v1.w;
+        }
+        uint32_t out[4];
+        float sc = quant_block16<UE8M0>(w1, out);
+        if (a1) {
+            __stcs(y + g, make_uint4(out[0], out[1], out[2], out[3]));
+            if ((threadIdx.x & 7) == 0) s[g >> 3] = sc;
+        }
+        if (g2 - lane < num_groups) {
+            sc = quant_block16<UE8M0>(w2, out);
+            if (a2) {
+                __stcs(y + g2, make_uint4(out[0], out[1], out[2], out[3]));
+                if ((threadIdx.x & 7) == 0) s[g2 >> 3] = sc;
+            }
+        }
+    }
 }
 
 // weight_dequant, vector path (K % 16 == 0): thread g converts 16 consecutive codes of one row.

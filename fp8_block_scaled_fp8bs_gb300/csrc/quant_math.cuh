@@ -75,26 +75,5 @@ __device__ __forceinline__ float quant_block16(const uint32_t (&w)[8], uint32_t 
     return sc;
 }
 
-// One group of 16 consecutive elements (x[16g .. 16g+15], block g/8) in global memory: eight
-// consecutive lanes of a warp own one 128-element block. Every lane of the warp must call this;
-// lanes with active == false load nothing and store nothing.
-template <bool UE8M0>
-__device__ __forceinline__ void act_quant_group16(const uint4* __restrict__ x,
-                                                  uint4* __restrict__ y, float* __restrict__ s,
-                                                  int64_t g, bool active) {
-    uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
-    if (active) {
-        v0 = __ldcs(x + 2 * g);
-        v1 = __ldcs(x + 2 * g + 1);
-    }
-    const uint32_t w[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t out[4];
-    const float sc = quant_block16<UE8M0>(w, out);
-    if (active) {
-        __stcs(y + g, make_uint4(out[0], out[1], out[2], out[3]));
-        if ((threadIdx.x & 7) == 0) s[g >> 3] = sc;
-    }
-}
-
 }  // namespace
 }  // namespace fp8bs

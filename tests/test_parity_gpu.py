@@ -109,6 +109,20 @@ def test_act_quant_full_size_sampled_rows(name, M, K, fmt):
     assert_quant_equal(y[rows], s[rows], y_ref, s_ref, name)
 
 
+@pytest.mark.parametrize("fmt", ["fp32", "ue8m0"])
+@pytest.mark.parametrize("M,K", [
+    (333, 128 * 121),     # 40293 blocks
+    (1000, 128 * 56),     # 56000 blocks
+])
+def test_act_quant_large_ragged_bit_exact(fmt, M, K):
+    """Inputs large enough that every thread takes several grid-stride steps, with a ragged
+    last step; every code and scale against the oracle."""
+    x = synth.activations(M, K, seed=M + K, name="large", outlier_frac=0.01)
+    y, s = gpu_act_quant(x, fmt)
+    y_ref, s_ref = oracle.act_quant(x, FMTS[fmt])
+    assert_quant_equal(y, s, y_ref, s_ref, f"large {M}x{K} {fmt}")
+
+
 # ------------------------------------------------------------------------------ weight_dequant
 
 @pytest.mark.parametrize("N,K", [(1, 1), (5, 33), (128, 128), (300, 272), (333, 391),
