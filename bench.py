@@ -358,28 +358,57 @@ def decode_gemm_launch_ms(g: Gpu, state, rounds):
 
 def run_decode_e2e(g: Gpu, steps, warmup, world):
     """The same step through the C ABI with host buffers: pinned host -> device copy of each
-    activation, act_quant + fp8_gemm, device -> pinned host copy of each output."""
+    activation, act_quant + fp8_gemm, device -> pinned host copy of each output. Every step
+    copies its own inputs in and its outputs out; within a step the four independent
+    problems are pipelined: the copies run on a second stream, so the next activation comes in
+    and the previous output goes out while a GEMM runs. Steps stay ordered: the copy stream is
+    in order, so a step's inputs go in only after the previous step's outputs are out, as when
+    the next input depends on them."""
     torch = g.torch
     state = decode_setup(g, seed=1)
     hx = [st["x"].cpu().pin_memory() for st in state]
     hc = [torch.empty(st["c"].shape, dtype=torch.bfloat16).pin_memory() for st in state]
+    comp = g.stream
+    copy = torch.cuda.Stream()
+    n = len(state)
+    x_free = [torch.cuda.Event() for _ in range(n)]     # compute has read x_i
+    x_in = [torch.cuda.Event() for _ in range(n)]       # x_i is on the device
+    c_done = [torch.cuda.Event() for _ in range(n)]     # c_i is computed
+    c_out = [torch.cuda.Event() for _ in range(n)]      # c_i is on the host
+    for i in range(n):
+        x_free[i].record(comp)
+        c_out[i].record(comp)
 
     def step():
+        with torch.cuda.stream(copy):
+            for i, st in enumerate(state):
+                copy.wait_event(x_free[i])
+                st["x"].copy_(hx[i], non_blocking=True)
+                x_in[i].record(copy)
         for i, st in enumerate(state):
-            st["x"].copy_(hx[i], non_blocking=True)
+            comp.wait_event(x_in[i])
+            comp.wait_event(c_out[i])
             g.act_quant_gemm(st["x"], st["y"], st["s"], st["B"], st["S"], st["c"], st["M"],
                              N_DIM, K_DIM, 0, WEIGHTS_CONSTANT)
-            hc[i].copy_(st["c"], non_blocking=True)
+            x_free[i].record(comp)
+            c_done[i].record(comp)
+        with torch.cuda.stream(copy):
+            for i, st in enumerate(state):
+                copy.wait_event(c_done[i])
+                hc[i].copy_(st["c"], non_blocking=True)
+                c_out[i].record(copy)
 
     for _ in range(warmup):
         step()
     torch.cuda.synchronize()
     barrier(world)
     t0, t1 = g.event(), g.event()
-    t0.record()
+    t0.record(comp)
     for _ in range(steps):
         step()
-    t1.record()
+    for i in range(n):
+        comp.wait_event(c_out[i])     # the region ends with the last outputs on the host
+    t1.record(comp)
     torch.cuda.synchronize()
     barrier(world)
     h2d = sum(2 * st["M"] * K_DIM for st in state)
