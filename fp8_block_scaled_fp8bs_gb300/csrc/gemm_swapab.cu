@@ -114,8 +114,16 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     if (warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
         const int t = threadIdx.x - 64;
         if constexpr (!FUSED) {
-            for (int i = t; i < scale_rows * num_kb; i += 32 * Cfg::EPI_WARPS)
-                cp_async_4(sRaw + i, as_rows + i);
+            // The rows are one contiguous run of scale_rows * num_kb floats: 16-byte copies when
+            // its start and length allow (sRaw is 16-byte aligned), else 4-byte ones.
+            const int count = scale_rows * num_kb;
+            if ((reinterpret_cast<uintptr_t>(as_rows) & 15) == 0 && (count & 3) == 0) {
+                for (int i = 4 * t; i < count; i += 4 * 32 * Cfg::EPI_WARPS)
+                    cp_async_16(sRaw + i, as_rows + i);
+            } else {
+                for (int i = t; i < count; i += 32 * Cfg::EPI_WARPS)
+                    cp_async_4(sRaw + i, as_rows + i);
+            }
         }
         for (int i = t; i < num_kb; i += 32 * Cfg::EPI_WARPS) cp_async_4(sBs + i, bs_row + i);
         cp_async_commit();
@@ -274,11 +282,12 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         if constexpr (!FUSED) {
             // Combined scales sAs[kb][m] = a_s[m0+m, kb] * b_s[slab, kb] (zero past row M), from
-            // the rows copied at kernel start, transposed so that reads are coalesced along kb.
-            const int valid = scale_rows * num_kb;
+            // the rows copied at kernel start, transposed so that the promotion reads them as
+            // float4 along m. Consecutive threads take consecutive m of one kb, so the stores
+            // are conflict-free and the index split is a shift (MT is a power of two).
             for (int i = threadIdx.x - 64; i < MT * num_kb; i += 32 * Cfg::EPI_WARPS) {
-                const int j = i / num_kb, kb = i - j * num_kb;
-                sAs[kb * MT + j] = i < valid ? sRaw[i] * sBs[kb] : 0.0f;
+                const int kb = i / MT, j = i % MT;
+                sAs[i] = j < scale_rows ? sRaw[j * num_kb + kb] * sBs[kb] : 0.0f;
             }
             asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         }

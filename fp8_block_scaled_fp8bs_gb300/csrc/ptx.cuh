@@ -122,6 +122,13 @@ __device__ __forceinline__ void cp_async_4(void* smem_dst, const void* gmem_src)
                  : "memory");
 }
 
+// 16 bytes; both addresses 16-byte aligned.
+__device__ __forceinline__ void cp_async_16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gmem_src))
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() {
     asm volatile("cp.async.commit_group;" ::: "memory");
 }
