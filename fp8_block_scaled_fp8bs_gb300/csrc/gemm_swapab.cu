@@ -25,7 +25,8 @@ struct SwapCfg {
     static constexpr int EPI_WARPS = 4;
     static constexpr int Q_WARPS = FUSED ? 4 : 0;   // quantiser warps, after the promotion warps
     static constexpr int Q_WARP0 = 2 + EPI_WARPS;
-    static constexpr int THREADS = 64 + 32 * (EPI_WARPS + Q_WARPS);
+    static constexpr int S_WARPS = FUSED ? 0 : 1;   // scale warp (quantised input), same place
+    static constexpr int THREADS = 64 + 32 * (EPI_WARPS + Q_WARPS + S_WARPS);
     static constexpr int X_TILE = MT * BK;          // e4m3 activation rows per stage
     static constexpr int XB_TILE = FUSED ? MT * BK * 2 : 0;   // bf16 rows per stage (FUSED)
     static constexpr int STAGE = A_TILE + X_TILE + XB_TILE;
@@ -48,6 +49,16 @@ __device__ __forceinline__ bool spin_until_equal(const int* p, int target) {
     if (*v == target) return true;
     const uint64_t t0 = global_timer_ns();
     while (*v != target)
+        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+// Bounded spin until *p >= target.
+__device__ __forceinline__ bool spin_until_at_least(const int* p, int target) {
+    const volatile int* v = p;
+    if (*v >= target) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (*v < target)
         if (global_timer_ns() - t0 > kWaitLimitNs) return false;
     return true;
 }
@@ -89,8 +100,11 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     const int scale_rows = min(MT, g.M - m0);
     const float* as_rows = g.a_s + static_cast<int64_t>(m0) * num_kb;
     const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+    // Quantised input: the scale warp counts here the K blocks of sAs it has filled.
+    int* sScaleDone = reinterpret_cast<int*>(ring.tmem_holder + 1);
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
+        *sScaleDone = 0;
         if constexpr (FUSED) {
             for (int s = 0; s < stages; ++s) mbar_init(&qfull[s], Cfg::Q_WARPS);
             fence_barrier_init();
@@ -111,21 +125,21 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     }
     grid_dependency_wait();
     grid_launch_dependents();
-    if (warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
+    if (FUSED && warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
         const int t = threadIdx.x - 64;
-        if constexpr (!FUSED) {
-            // The rows are one contiguous run of scale_rows * num_kb floats: 16-byte copies when
-            // its start and length allow (sRaw is 16-byte aligned), else 4-byte ones.
-            const int count = scale_rows * num_kb;
-            if ((reinterpret_cast<uintptr_t>(as_rows) & 15) == 0 && (count & 3) == 0) {
-                for (int i = 4 * t; i < count; i += 4 * 32 * Cfg::EPI_WARPS)
-                    cp_async_16(sRaw + i, as_rows + i);
-            } else {
-                for (int i = t; i < count; i += 32 * Cfg::EPI_WARPS)
-                    cp_async_4(sRaw + i, as_rows + i);
-            }
-        }
         for (int i = t; i < num_kb; i += 32 * Cfg::EPI_WARPS) cp_async_4(sBs + i, bs_row + i);
+        cp_async_commit();
+    }
+    if (!FUSED && warp == Cfg::Q_WARP0) {
+        // The rows are one contiguous run of scale_rows * num_kb floats: 16-byte copies when
+        // its start and length allow (sRaw is 16-byte aligned), else 4-byte ones.
+        const int count = scale_rows * num_kb;
+        if ((reinterpret_cast<uintptr_t>(as_rows) & 15) == 0 && (count & 3) == 0) {
+            for (int i = 4 * lane; i < count; i += 4 * 32) cp_async_16(sRaw + i, as_rows + i);
+        } else {
+            for (int i = lane; i < count; i += 32) cp_async_4(sRaw + i, as_rows + i);
+        }
+        for (int i = lane; i < num_kb; i += 32) cp_async_4(sBs + i, bs_row + i);
         cp_async_commit();
     }
     if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
@@ -203,6 +217,24 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             mma_commit(ring.drain);
             if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
         }
+    } else if (!FUSED && warp == Cfg::Q_WARP0) {
+        // Scale warp: combined scales sAs[kb][m] = a_s[m0+m, kb] * b_s[slab, kb] (zero past row
+        // M), transposed from the copied rows so that the promotion reads them as float4 along
+        // m, one K block at a time and published as it goes: the promotion of block 0 need not
+        // wait for the whole table.
+        cp_async_wait_all();
+        __syncwarp();
+        for (int kb = 0; kb < num_kb; ++kb) {
+            const float sb = sBs[kb];
+#pragma unroll
+            for (int j = lane; j < MT; j += 32)
+                sAs[kb * MT + j] = j < scale_rows ? sRaw[j * num_kb + kb] * sb : 0.0f;
+            __syncwarp();
+            if (lane == 0) {
+                __threadfence_block();
+                *reinterpret_cast<volatile int*>(sScaleDone) = kb + 1;
+            }
+        }
     } else if (FUSED && warp >= Cfg::Q_WARP0) {
         // Quantiser warps: per K block, 8 lanes per row of MT: lane l of a group takes elements
         // 16 (l % 8) .. +15 of its row, i.e. one 16-byte chunk of the row's 128 e4m3 codes,
@@ -278,17 +310,8 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         }
     } else {
         // Promotion warps.
-        cp_async_wait_all();
-        asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
-        if constexpr (!FUSED) {
-            // Combined scales sAs[kb][m] = a_s[m0+m, kb] * b_s[slab, kb] (zero past row M), from
-            // the rows copied at kernel start, transposed so that the promotion reads them as
-            // float4 along m. Consecutive threads take consecutive m of one kb, so the stores
-            // are conflict-free and the index split is a shift (MT is a power of two).
-            for (int i = threadIdx.x - 64; i < MT * num_kb; i += 32 * Cfg::EPI_WARPS) {
-                const int kb = i / MT, j = i % MT;
-                sAs[i] = j < scale_rows ? sRaw[j * num_kb + kb] * sBs[kb] : 0.0f;
-            }
+        if constexpr (FUSED) {
+            cp_async_wait_all();
             asm volatile("bar.sync 1, %0;" ::"n"(32 * Cfg::EPI_WARPS) : "memory");
         }
         const int quarter = warp & 3;
@@ -308,6 +331,14 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             // FUSED: this block's a_s (written by the quantiser warps, long before the MMA that
             // just finished could run) times b_s; otherwise the staged products.
             float sb = 1.0f;
+            if constexpr (!FUSED) {
+                if (!spin_until_at_least(sScaleDone, kb + 1)) {
+                    if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                    ok = false;
+                    break;
+                }
+                __threadfence_block();
+            }
             if constexpr (FUSED) {
                 if (!spin_until_equal(&sReady[kb], Cfg::Q_WARPS)) {
                     if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
