@@ -5,12 +5,14 @@
 // from HBM as bf16.
 //
 // 128-row slabs of W take the MMA's M side, MT (16, 32, 64 or 128) rows of x its N side; each
-// CTA streams the e4m3 codes of one slab (half the bytes of the bf16 weight) against one tile of
-// x. CTAs that share a slab are adjacent in launch order, so for M > 128 a slab is read from
-// HBM about once and the other tiles of x find it in L2.
+// CTA streams the e4m3 codes of one slab (half the bytes of the bf16 weight) against XT tiles
+// of x (XT = 2 for M > 128: each dequantised K block then feeds two 128-row tiles, halving the
+// dequantisation per FLOP). CTAs that share a slab are adjacent in launch order, so for
+// M > 128 a slab is read from HBM about once and the other tiles of x find it in L2.
 //   warp 0          TMA producer of the deep ring: per K block the e4m3 weight tile (the HBM
 //                   stream) and the bf16 rows of x (128-byte swizzle, two 64-wide halves)
-//   warps 1, 2      MMA issuers, K block kb to issuer kb % 2: 8 x tcgen05.mma kind::f16
+//   warps 1, 2      MMA issuers. XT = 1: K block kb to issuer kb % 2; XT = 2: issuer t takes
+//                   tile t of x for every K block. Per K block 8 x tcgen05.mma kind::f16
 //                   (K = 16) per K block into the issuer's own TMEM accumulator for the whole
 //                   K loop (the block scale is inside W'). One thread issuing alone is held
 //                   to about one small MMA per 60-80 clk and stalls at its next barrier wait
@@ -35,7 +37,7 @@ namespace fp8bs {
 
 namespace {
 
-template <int MT>
+template <int MT, int XT>
 struct LinCfg {
     static constexpr int EPI_WARPS = 4;
     static constexpr int DQ_GROUP = 8;                   // dequantiser warps per K block
@@ -46,13 +48,15 @@ struct LinCfg {
     static constexpr int WQ_TILE = BM * BK;              // e4m3 weight tile (128 x 128)
     static constexpr int HALF = 64;                      // bf16 K elements per 128-byte row
     static constexpr int XB_TILE = MT * BK * 2;          // bf16 activation tile: two halves
-    static constexpr int A_SLOT = WQ_TILE + XB_TILE;     // deep ring: weight codes + rows of x
+    static constexpr int A_SLOT = WQ_TILE + XT * XB_TILE;   // ring: weight codes + XT x tiles
     static constexpr int ISSUERS = 2;                    // MMA issuers: warps 1 .. ISSUERS
     static constexpr int ACC_COLS = MT > 64 ? MT : 64;   // TMEM: accumulator i at ACC_COLS i,
     static constexpr int W_COL0 = ISSUERS * ACC_COLS;    // then the W' slots of 64 columns
     static constexpr int W_COLS = BK / 2;                // (bf16 pairs)
     static constexpr int SB = 4;                         // W' slots
     static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr int MMA_PER_KB = XT;                // issuer commits per K block
+    static_assert(XT == 1 || (XT == 2 && MT == 128), "two x tiles only with 128 rows each");
 };
 
 // Eight e4m3 codes (one 64-bit word) -> eight bf16 (four words): fp32(code) * scale, rounded to
@@ -94,13 +98,13 @@ __device__ __forceinline__ int sw128(int r, int c) {
     return (r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4);
 }
 
-template <int MT>
-__global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
+template <int MT, int XT>
+__global__ void __launch_bounds__(LinCfg<MT, XT>::THREADS, 1)
     linear_bf16_swap_kernel(const __grid_constant__ CUtensorMap tmW,
                             const __grid_constant__ CUtensorMap tmX,
                             const float* __restrict__ w_s, void* y, const int M, const int N,
                             const int K, const int sa, const int weights_constant) {
-    using Cfg = LinCfg<MT>;
+    using Cfg = LinCfg<MT, XT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sA = smem;                              // [sa][W e4m3 | x bf16]
@@ -115,23 +119,24 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int num_kb = K / BK;
-    const int m_tiles = (M + MT - 1) / MT;
+    const int m_tiles = (M + MT * XT - 1) / (MT * XT);
     const int slab = static_cast<int>(blockIdx.x) / m_tiles;
     const int n0 = slab * BM;
-    const int m0 = (static_cast<int>(blockIdx.x) - slab * m_tiles) * MT;
+    const int m0 = (static_cast<int>(blockIdx.x) - slab * m_tiles) * MT * XT;
     const float* ws_row = w_s + static_cast<int64_t>(slab) * num_kb;
     const int prefill = min(sa, num_kb);
-    const uint64_t stream = l2_policy_evict_first();  // weights: read once
+    // weights: read once, or (several tiles of x) by the neighbouring CTAs too
+    const uint64_t stream = m_tiles > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
     const uint64_t keep = l2_policy_evict_last();     // x: read by every CTA
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < sa; ++i) {
             mbar_init(&fullA[i], 1);
-            mbar_init(&emptyA[i], Cfg::DQ_GROUP + 1);   // dequantisers + the MMA's commit
+            mbar_init(&emptyA[i], Cfg::DQ_GROUP + Cfg::MMA_PER_KB);   // dequantisers + MMAs
         }
         for (int i = 0; i < Cfg::SB; ++i) {
             mbar_init(&deqB[i], Cfg::DQ_GROUP);
-            mbar_init(&emptyB[i], 1);
+            mbar_init(&emptyB[i], Cfg::MMA_PER_KB);
         }
         mbar_init(tfull, Cfg::ISSUERS);
         mbar_init(drain, Cfg::ISSUERS);
@@ -160,8 +165,12 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
         constexpr uint32_t idesc = idesc_bf16_f32(BM, MT);
         const int me = warp - 1;
         const uint32_t acc = tmem_base + static_cast<uint32_t>(me * Cfg::ACC_COLS);
-        int a = me;                                       // stage of kb (me < sa)
-        for (int kb = me; kb < num_kb; kb += Cfg::ISSUERS) {
+        // XT = 1: K blocks me, me + 2, ...; XT = 2: every K block, against tile me of x
+        constexpr int STEP = XT == 2 ? 1 : Cfg::ISSUERS;
+        const int first = XT == 2 ? 0 : me;
+        const int x_off = Cfg::WQ_TILE + (XT == 2 ? me : 0) * Cfg::XB_TILE;
+        int a = first;                                    // stage of kb (first < sa)
+        for (int kb = first; kb < num_kb; kb += STEP) {
             const int b = kb % Cfg::SB;
             if (!mbar_wait(&deqB[b], static_cast<uint32_t>((kb / Cfg::SB) & 1))) {
                 record_error(FP8BS_DEVERR_MMA_WAIT);
@@ -169,16 +178,16 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
             }
             tc_fence_after();
             const uint32_t w_tmem = tmem_base + static_cast<uint32_t>(Cfg::W_COL0 + b * Cfg::W_COLS);
-            const uint32_t x_addr = smem_addr(sA + a * Cfg::A_SLOT + Cfg::WQ_TILE);
+            const uint32_t x_addr = smem_addr(sA + a * Cfg::A_SLOT + x_off);
 #pragma unroll
             for (int j = 0; j < BK / 16; ++j) {
                 const uint32_t h = j / 4, o = (j % 4) * 32;   // 64-wide half, 16-wide step
                 mma_bf16_ta(acc, w_tmem + 8 * j, smem_desc_k_sw128(x_addr + h * (MT * 128) + o),
-                            idesc, (kb > me || j > 0) ? 1u : 0u);
+                            idesc, (kb > first || j > 0) ? 1u : 0u);
             }
             mma_commit(&emptyB[b]);
             mma_commit(&emptyA[a]);
-            a += Cfg::ISSUERS;                            // ISSUERS < sa: at most one wrap
+            a += STEP;                                    // STEP <= sa: at most one wrap
             if (a >= sa) a -= sa;
         }
         mma_commit(tfull);
@@ -190,9 +199,13 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     if (warp == 0) {
         if (lane == 0) {
             auto load_x = [&](int slot, int kb) {
-                uint8_t* xs = sA + slot * Cfg::A_SLOT + Cfg::WQ_TILE;
-                tma_load_2d_hint(xs, &tmX, &fullA[slot], kb * BK, m0, keep);
-                tma_load_2d_hint(xs + MT * 128, &tmX, &fullA[slot], kb * BK + Cfg::HALF, m0, keep);
+#pragma unroll
+                for (int t = 0; t < XT; ++t) {
+                    uint8_t* xs = sA + slot * Cfg::A_SLOT + Cfg::WQ_TILE + t * Cfg::XB_TILE;
+                    tma_load_2d_hint(xs, &tmX, &fullA[slot], kb * BK, m0 + t * MT, keep);
+                    tma_load_2d_hint(xs + MT * 128, &tmX, &fullA[slot], kb * BK + Cfg::HALF,
+                                     m0 + t * MT, keep);
+                }
             };
             for (int kb = 0; kb < prefill; ++kb) {
                 if (!weights_constant) {
@@ -281,13 +294,19 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
         if (warp_wait(tfull, 0)) {
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-            const int used = min(num_kb, Cfg::ISSUERS);   // accumulators that were written
+            // XT = 1: the written accumulators are summed; XT = 2: accumulator t is tile t
+            const int used = XT == 2 ? 1 : min(num_kb, Cfg::ISSUERS);
             constexpr int CW = MT < 32 ? MT : 32;          // columns (rows of x) per chunk
             __nv_bfloat16* yc = static_cast<__nv_bfloat16*>(y);
 #pragma unroll 1
-            for (int c = 0; c < MT / CW; ++c) {
+            for (int c = 0; c < XT * MT / CW; ++c) {
+                // chunk c: columns CW c .. of accumulator c / (MT / CW) (XT = 2), rows of x
+                // m0 + CW c ..
                 float acc[CW];
-                tmem_ld_cols<CW>(taddr + CW * c, acc);
+                tmem_ld_cols<CW>(taddr + (XT == 2 ? (c / (MT / CW)) * Cfg::ACC_COLS +
+                                                        (c % (MT / CW)) * CW
+                                                  : CW * c),
+                                 acc);
                 for (int i = 1; i < used; ++i) {
                     float t[CW];
                     tmem_ld_cols<CW>(taddr + i * Cfg::ACC_COLS + CW * c, t);
@@ -313,23 +332,24 @@ __global__ void __launch_bounds__(LinCfg<MT>::THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
-template <int MT>
+template <int MT, int XT>
 cudaError_t launch_lin(const CUtensorMap& tmW, const CUtensorMap& tmX, const float* w_s, void* y,
                        int M, int N, int K, int weights_constant, cudaStream_t stream) {
-    using Cfg = LinCfg<MT>;
+    using Cfg = LinCfg<MT, XT>;
     // the W' ring lives in TMEM; shared memory holds the e4m3 weight stream and the rows of x
     const int bar_bytes = 8 * (2 * kMaxStages + 2 * Cfg::SB + 2) + 16;
     int sa = (kSmemLimit - 1024 - bar_bytes) / Cfg::A_SLOT;
     if (sa > kMaxStages) sa = kMaxStages;
     if (sa < 2) return cudaErrorInvalidValue;
     const int smem = 1024 + sa * Cfg::A_SLOT + bar_bytes;
-    cudaError_t e = set_smem(linear_bf16_swap_kernel<MT>, smem);
+    cudaError_t e = set_smem(linear_bf16_swap_kernel<MT, XT>, smem);
     if (e != cudaSuccess) return e;
-    const int64_t ctas = static_cast<int64_t>((N + BM - 1) / BM) * ((M + MT - 1) / MT);
+    const int64_t ctas =
+        static_cast<int64_t>((N + BM - 1) / BM) * ((M + MT * XT - 1) / (MT * XT));
     if (ctas > INT32_MAX) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(ctas));
-    return launch_pdl(linear_bf16_swap_kernel<MT>, grid, Cfg::THREADS, smem, stream, tmW, tmX,
-                      w_s, y, M, N, K, sa, weights_constant);
+    return launch_pdl(linear_bf16_swap_kernel<MT, XT>, grid, Cfg::THREADS, smem, stream, tmW,
+                      tmX, w_s, y, M, N, K, sa, weights_constant);
 }
 
 }  // namespace
@@ -338,10 +358,14 @@ cudaError_t launch_linear_bf16_swap(const CUtensorMap& tmW, const CUtensorMap& t
                                     const float* w_s, void* y, int M, int N, int K, int MT,
                                     int weights_constant, cudaStream_t stream) {
     switch (MT) {
-        case 16: return launch_lin<16>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
-        case 32: return launch_lin<32>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
-        case 64: return launch_lin<64>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
-        case 128: return launch_lin<128>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
+        case 16: return launch_lin<16, 1>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
+        case 32: return launch_lin<32, 1>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
+        case 64: return launch_lin<64, 1>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
+        case 128:
+            // beyond one 128-row tile of x, each CTA takes two
+            if (M > 128)
+                return launch_lin<128, 2>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
+            return launch_lin<128, 1>(tmW, tmX, w_s, y, M, N, K, weights_constant, stream);
         default: return cudaErrorInvalidValue;
     }
 }
