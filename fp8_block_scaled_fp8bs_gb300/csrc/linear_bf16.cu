@@ -9,25 +9,29 @@
 // of x (XT = 2 for M > 128: each dequantised K block then feeds two 128-row tiles, halving the
 // dequantisation per FLOP). CTAs that share a slab are adjacent in launch order, so for
 // M > 128 a slab is read from HBM about once and the other tiles of x find it in L2.
-//   warp 0          TMA producer of the deep ring: per K block the e4m3 weight tile (the HBM
-//                   stream) and the bf16 rows of x (128-byte swizzle, two 64-wide halves)
+//   warp 0          weight producer: per K block the e4m3 tile (the HBM stream) into the
+//                   weight ring; a slot is free as soon as the dequantisers have read it
+//   warp 3 (lane 0) x producer: the bf16 rows of x (128-byte swizzle, 64-wide K halves) into
+//                   the x ring; a slot is free once the MMAs reading it are done. Warp 3 is an
+//                   epilogue warp, idle until the end of the K loop.
 //   warps 1, 2      MMA issuers. XT = 1: K block kb to issuer kb % 2; XT = 2: issuer t takes
 //                   tile t of x for every K block. Per K block 8 x tcgen05.mma kind::f16
-//                   (K = 16) per K block into the issuer's own TMEM accumulator for the whole
-//                   K loop (the block scale is inside W'). One thread issuing alone is held
-//                   to about one small MMA per 60-80 clk and stalls at its next barrier wait
-//                   until the tensor core has caught up; two issuers keep the pipe fed.
-//   warps 2 .. 5    epilogue: the sum of the accumulators to bf16 y
+//                   (K = 16) into the issuer's own TMEM accumulator for the whole K loop (the
+//                   block scale is inside W'). One thread issuing alone is held to about one
+//                   small MMA per 60-80 clk and stalls at its next barrier wait until the
+//                   tensor core has caught up; two issuers keep the pipe fed.
+//   warps 2 .. 5    epilogue: the accumulators to bf16 y (summed for XT = 1)
 //   warps 6 .. 21   dequantisers, two groups of eight taking K blocks in turn (a warp's barrier
 //                   waits and arrivals cost a few hundred clk per K block, which the other
 //                   group overlaps): e4m3 tile -> bf16 W' tile (fp32 product with
 //                   the block scale, rounded to bf16: weight_dequant's arithmetic) written
 //                   straight into TMEM with tcgen05.st (lane = weight row, 32-bit column =
-//                   two consecutive K), where the MMA takes its A operand: a second, shallow
-//                   ring of four 64-column slots. W' never touches shared memory, which the
-//                   TMA stream, the dequantisers' reads and the MMA's reads of x already share.
-// A slot of the deep ring is free once the dequantisers have read its weight tile and the MMA
-// has read its rows of x.
+//                   two consecutive K), where the MMA takes its A operand: a third ring, of
+//                   four 64-column TMEM slots. W' never touches shared memory, which the
+//                   TMA streams, the dequantisers' reads and the MMA's reads of x share.
+// Separate weight and x rings let the weight ring run ahead of the MMAs (its slots recycle at
+// dequantisation) and, with two tiles of x, let the x ring work in K halves so that four slots
+// fit.
 #include "gemm_common.cuh"
 
 #include <cuda_fp16.h>
@@ -39,16 +43,27 @@ namespace {
 
 template <int MT, int XT>
 struct LinCfg {
+    static_assert(XT == 1 || (XT == 2 && MT == 128), "two x tiles only with 128 rows each");
     static constexpr int EPI_WARPS = 4;
     static constexpr int DQ_GROUP = 8;                   // dequantiser warps per K block
     static constexpr int DQ_GROUPS = 2;                  // groups, taking K blocks in turn
     static constexpr int DQ_WARPS = DQ_GROUP * DQ_GROUPS;
     static constexpr int DQ0 = 2 + EPI_WARPS;            // first dequantiser warp
+    static constexpr int X_PRODUCER = 3;                 // an epilogue warp, idle until the end
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + DQ_WARPS);
-    static constexpr int WQ_TILE = BM * BK;              // e4m3 weight tile (128 x 128)
+    static constexpr int W_TILE = BM * BK;               // e4m3 weight tile (128 x 128)
     static constexpr int HALF = 64;                      // bf16 K elements per 128-byte row
-    static constexpr int XB_TILE = MT * BK * 2;          // bf16 activation tile: two halves
-    static constexpr int A_SLOT = WQ_TILE + XT * XB_TILE;   // ring: weight codes + XT x tiles
+    static constexpr int XH_TILE = MT * 128;             // one tile of x, one 64-wide K half
+    // x ring slot: XT tiles x HPS K halves. Two tiles (large M): one K half per slot, so that
+    // four slots fit beside the weight ring; one tile: a whole K block per slot, so that an
+    // issuer waits once per K block (each wait after issued MMAs costs it a drain).
+    static constexpr int HPS = XT == 2 ? 1 : 2;
+    static constexpr int X_SLOT = XT * HPS * XH_TILE;
+    static constexpr int SX = (XT == 2 || MT >= 128) ? 4 : 8;   // x ring slots
+    static constexpr int BAR_BYTES = 8 * (2 * kMaxStages + 2 * SX + 2 * 4 + 2) + 16;
+    static constexpr int SW_FIT = (kSmemLimit - 1024 - BAR_BYTES - SX * X_SLOT) / W_TILE;
+    static constexpr int SW = SW_FIT > kMaxStages ? kMaxStages : SW_FIT;   // weight ring slots
+    static_assert(SW >= 2, "shared memory");
     static constexpr int ISSUERS = 2;                    // MMA issuers: warps 1 .. ISSUERS
     static constexpr int ACC_COLS = MT > 64 ? MT : 64;   // TMEM: accumulator i at ACC_COLS i,
     static constexpr int W_COL0 = ISSUERS * ACC_COLS;    // then the W' slots of 64 columns
@@ -56,7 +71,7 @@ struct LinCfg {
     static constexpr int SB = 4;                         // W' slots
     static constexpr uint32_t TMEM_COLS = 512;
     static constexpr int MMA_PER_KB = XT;                // issuer commits per K block
-    static_assert(XT == 1 || (XT == 2 && MT == 128), "two x tiles only with 128 rows each");
+    static constexpr int SMEM = 1024 + SW * W_TILE + SX * X_SLOT + BAR_BYTES;
 };
 
 // Eight e4m3 codes (one 64-bit word) -> eight bf16 (four words): fp32(code) * scale, rounded to
@@ -103,14 +118,17 @@ __global__ void __launch_bounds__(LinCfg<MT, XT>::THREADS, 1)
     linear_bf16_swap_kernel(const __grid_constant__ CUtensorMap tmW,
                             const __grid_constant__ CUtensorMap tmX,
                             const float* __restrict__ w_s, void* y, const int M, const int N,
-                            const int K, const int sa, const int weights_constant) {
+                            const int K, const int weights_constant) {
     using Cfg = LinCfg<MT, XT>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
-    uint8_t* sA = smem;                              // [sa][W e4m3 | x bf16]
-    uint64_t* fullA = reinterpret_cast<uint64_t*>(sA + sa * Cfg::A_SLOT);
-    uint64_t* emptyA = fullA + sa;
-    uint64_t* deqB = emptyA + sa;
+    uint8_t* sW = smem;                                   // [SW][W e4m3 tile]
+    uint8_t* sX = sW + Cfg::SW * Cfg::W_TILE;             // [SX][XT tiles x one K half of x]
+    uint64_t* fullW = reinterpret_cast<uint64_t*>(sX + Cfg::SX * Cfg::X_SLOT);
+    uint64_t* emptyW = fullW + Cfg::SW;
+    uint64_t* fullX = emptyW + Cfg::SW;
+    uint64_t* emptyX = fullX + Cfg::SX;
+    uint64_t* deqB = emptyX + Cfg::SX;
     uint64_t* emptyB = deqB + Cfg::SB;
     uint64_t* tfull = emptyB + Cfg::SB;
     uint64_t* drain = tfull + 1;
@@ -124,15 +142,19 @@ __global__ void __launch_bounds__(LinCfg<MT, XT>::THREADS, 1)
     const int n0 = slab * BM;
     const int m0 = (static_cast<int>(blockIdx.x) - slab * m_tiles) * MT * XT;
     const float* ws_row = w_s + static_cast<int64_t>(slab) * num_kb;
-    const int prefill = min(sa, num_kb);
+    const int w_prefill = min(Cfg::SW, num_kb);
     // weights: read once, or (several tiles of x) by the neighbouring CTAs too
     const uint64_t stream = m_tiles > 1 ? l2_policy_evict_normal() : l2_policy_evict_first();
     const uint64_t keep = l2_policy_evict_last();     // x: read by every CTA
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < sa; ++i) {
-            mbar_init(&fullA[i], 1);
-            mbar_init(&emptyA[i], Cfg::DQ_GROUP + Cfg::MMA_PER_KB);   // dequantisers + MMAs
+        for (int i = 0; i < Cfg::SW; ++i) {
+            mbar_init(&fullW[i], 1);
+            mbar_init(&emptyW[i], Cfg::DQ_GROUP);        // the dequantisers have read the codes
+        }
+        for (int i = 0; i < Cfg::SX; ++i) {
+            mbar_init(&fullX[i], 1);
+            mbar_init(&emptyX[i], Cfg::MMA_PER_KB);      // the MMAs reading it are done
         }
         for (int i = 0; i < Cfg::SB; ++i) {
             mbar_init(&deqB[i], Cfg::DQ_GROUP);
@@ -145,9 +167,9 @@ __global__ void __launch_bounds__(LinCfg<MT, XT>::THREADS, 1)
         tma_prefetch_desc(&tmX);
         // Weights the caller declared constant start streaming before earlier kernels finish.
         if (weights_constant)
-            for (int kb = 0; kb < prefill; ++kb) {
-                mbar_arrive_expect_tx(&fullA[kb], Cfg::A_SLOT);
-                tma_load_2d_hint(sA + kb * Cfg::A_SLOT, &tmW, &fullA[kb], kb * BK, n0, stream);
+            for (int kb = 0; kb < w_prefill; ++kb) {
+                mbar_arrive_expect_tx(&fullW[kb], Cfg::W_TILE);
+                tma_load_2d_hint(sW + kb * Cfg::W_TILE, &tmW, &fullW[kb], kb * BK, n0, stream);
             }
     }
     grid_dependency_wait();
@@ -159,92 +181,110 @@ __global__ void __launch_bounds__(LinCfg<MT, XT>::THREADS, 1)
     const uint32_t tmem_base = *tmem_holder;
 
     if (warp >= 1 && warp <= Cfg::ISSUERS && lane == 0) {
-        // MMA issuer: K blocks kb = warp - 1, warp - 1 + ISSUERS, ... into accumulator warp - 1.
-        // The dequantisers waited for the stage's TMA before signalling deqB, so deqB alone
-        // says that both the weight slot in TMEM and the rows of x in shared memory are ready.
+        // MMA issuer me. XT = 1: K blocks me, me + 2, ... into accumulator me; XT = 2: every K
+        // block against tile me of x, into accumulator me. Per K block: wait for its W' slot,
+        // then per 64-wide K half for the x slot, 4 MMAs (K = 16), release the x slot; after
+        // both halves release the W' slot.
         constexpr uint32_t idesc = idesc_bf16_f32(BM, MT);
         const int me = warp - 1;
         const uint32_t acc = tmem_base + static_cast<uint32_t>(me * Cfg::ACC_COLS);
-        // XT = 1: K blocks me, me + 2, ...; XT = 2: every K block, against tile me of x
         constexpr int STEP = XT == 2 ? 1 : Cfg::ISSUERS;
         const int first = XT == 2 ? 0 : me;
-        const int x_off = Cfg::WQ_TILE + (XT == 2 ? me : 0) * Cfg::XB_TILE;
-        int a = first;                                    // stage of kb (first < sa)
-        for (int kb = first; kb < num_kb; kb += STEP) {
+        const int x_off = (XT == 2 ? me : 0) * Cfg::XH_TILE;
+        bool ok = true;
+        for (int kb = first; ok && kb < num_kb; kb += STEP) {
             const int b = kb % Cfg::SB;
             if (!mbar_wait(&deqB[b], static_cast<uint32_t>((kb / Cfg::SB) & 1))) {
                 record_error(FP8BS_DEVERR_MMA_WAIT);
                 break;
             }
-            tc_fence_after();
             const uint32_t w_tmem = tmem_base + static_cast<uint32_t>(Cfg::W_COL0 + b * Cfg::W_COLS);
-            const uint32_t x_addr = smem_addr(sA + a * Cfg::A_SLOT + x_off);
 #pragma unroll
-            for (int j = 0; j < BK / 16; ++j) {
-                const uint32_t h = j / 4, o = (j % 4) * 32;   // 64-wide half, 16-wide step
-                mma_bf16_ta(acc, w_tmem + 8 * j, smem_desc_k_sw128(x_addr + h * (MT * 128) + o),
-                            idesc, (kb > first || j > 0) ? 1u : 0u);
+            for (int p = 0; p < 2 / Cfg::HPS; ++p) {
+                const int q = (2 / Cfg::HPS) * kb + p;    // x slot sequence number
+                const int xs = q % Cfg::SX;
+                // One tile: the first dequantiser warp of the K block waited for this slot
+                // before signalling deqB, so the issuer need not wait again.
+                if (XT == 2 && !mbar_wait(&fullX[xs], static_cast<uint32_t>((q / Cfg::SX) & 1))) {
+                    record_error(FP8BS_DEVERR_MMA_WAIT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t x_addr = smem_addr(sX + xs * Cfg::X_SLOT + x_off);
+#pragma unroll
+                for (int j = 0; j < 4 * Cfg::HPS; ++j) {
+                    const int h = p * Cfg::HPS + j / 4;   // K half of the block
+                    mma_bf16_ta(acc, w_tmem + 8 * (4 * h + j % 4),
+                                smem_desc_k_sw128(x_addr + (j / 4) * Cfg::XH_TILE + 32 * (j % 4)),
+                                idesc, (kb > first || h > 0 || j % 4 > 0) ? 1u : 0u);
+                }
+                mma_commit(&emptyX[xs]);
             }
             mma_commit(&emptyB[b]);
-            mma_commit(&emptyA[a]);
-            a += STEP;                                    // STEP <= sa: at most one wrap
-            if (a >= sa) a -= sa;
         }
         mma_commit(tfull);
         mma_commit(drain);
         if (!mbar_wait(drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
     }
+    if (warp == Cfg::X_PRODUCER && lane == 0) {
+        // x producer: per slot, the XT tiles' HPS 64-wide K halves (128-byte swizzled rows).
+        const int slots = (2 / Cfg::HPS) * num_kb;
+        int issued = 0;
+        for (int q = 0; q < slots; ++q) {
+            const int xs = q % Cfg::SX;
+            if (q >= Cfg::SX &&
+                !mbar_wait(&emptyX[xs], static_cast<uint32_t>(((q / Cfg::SX) & 1) ^ 1))) {
+                record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                for (int i = issued > Cfg::SX ? issued - Cfg::SX : 0; i < issued; ++i)
+                    if (!mbar_wait(&fullX[i % Cfg::SX], static_cast<uint32_t>((i / Cfg::SX) & 1),
+                                   kDrainLimitNs))
+                        record_error(FP8BS_DEVERR_DRAIN_WAIT);
+                break;
+            }
+            mbar_arrive_expect_tx(&fullX[xs], Cfg::X_SLOT);
+#pragma unroll
+            for (int t = 0; t < XT; ++t)
+#pragma unroll
+                for (int h = 0; h < Cfg::HPS; ++h)
+                    tma_load_2d_hint(sX + xs * Cfg::X_SLOT + (t * Cfg::HPS + h) * Cfg::XH_TILE,
+                                     &tmX, &fullX[xs], (q * Cfg::HPS + h) * Cfg::HALF,
+                                     m0 + t * MT, keep);
+            ++issued;
+        }
+    }
     __syncwarp();
 
     if (warp == 0) {
         if (lane == 0) {
-            auto load_x = [&](int slot, int kb) {
-#pragma unroll
-                for (int t = 0; t < XT; ++t) {
-                    uint8_t* xs = sA + slot * Cfg::A_SLOT + Cfg::WQ_TILE + t * Cfg::XB_TILE;
-                    tma_load_2d_hint(xs, &tmX, &fullA[slot], kb * BK, m0 + t * MT, keep);
-                    tma_load_2d_hint(xs + MT * 128, &tmX, &fullA[slot], kb * BK + Cfg::HALF,
-                                     m0 + t * MT, keep);
-                }
-            };
-            for (int kb = 0; kb < prefill; ++kb) {
-                if (!weights_constant) {
-                    mbar_arrive_expect_tx(&fullA[kb], Cfg::A_SLOT);
-                    tma_load_2d_hint(sA + kb * Cfg::A_SLOT, &tmW, &fullA[kb], kb * BK, n0,
+            // weight producer: the e4m3 tile of each K block
+            if (!weights_constant)
+                for (int kb = 0; kb < w_prefill; ++kb) {
+                    mbar_arrive_expect_tx(&fullW[kb], Cfg::W_TILE);
+                    tma_load_2d_hint(sW + kb * Cfg::W_TILE, &tmW, &fullW[kb], kb * BK, n0,
                                      stream);
                 }
-                load_x(kb, kb);
-            }
-            int stage = prefill % sa;
-            uint32_t phase = prefill == sa ? 1u : 0u;
-            int64_t issued = prefill;
-            for (int kb = prefill; kb < num_kb; ++kb) {
-                if (!mbar_wait(&emptyA[stage], phase ^ 1)) {
+            int issued = w_prefill;
+            for (int kb = w_prefill; kb < num_kb; ++kb) {
+                const int ws = kb % Cfg::SW;
+                if (!mbar_wait(&emptyW[ws], static_cast<uint32_t>(((kb / Cfg::SW) & 1) ^ 1))) {
                     record_error(FP8BS_DEVERR_PRODUCER_WAIT);
-                    // drain what is in flight before leaving
-                    const int64_t first = issued > sa ? issued - sa : 0;
-                    for (int64_t i = first; i < issued; ++i)
-                        if (!mbar_wait(&fullA[i % sa], static_cast<uint32_t>((i / sa) & 1),
-                                       kDrainLimitNs))
+                    for (int i = issued > Cfg::SW ? issued - Cfg::SW : 0; i < issued; ++i)
+                        if (!mbar_wait(&fullW[i % Cfg::SW],
+                                       static_cast<uint32_t>((i / Cfg::SW) & 1), kDrainLimitNs))
                             record_error(FP8BS_DEVERR_DRAIN_WAIT);
                     break;
                 }
-                mbar_arrive_expect_tx(&fullA[stage], Cfg::A_SLOT);
-                tma_load_2d_hint(sA + stage * Cfg::A_SLOT, &tmW, &fullA[stage], kb * BK, n0,
-                                 stream);
-                load_x(stage, kb);
+                mbar_arrive_expect_tx(&fullW[ws], Cfg::W_TILE);
+                tma_load_2d_hint(sW + ws * Cfg::W_TILE, &tmW, &fullW[ws], kb * BK, n0, stream);
                 ++issued;
-                if (++stage == sa) {
-                    stage = 0;
-                    phase ^= 1;
-                }
             }
         }
     } else if (warp >= Cfg::DQ0) {
         // Dequantisers: group g takes the K blocks kb with kb % 2 == g. Warp w handles the TMEM
         // lane quarter w % 4 (weight rows 32 (w % 4) .. +31, one per lane) and one 64-wide half
-        // of the K block; each lane converts the 64 codes of its row's half and stores them as
-        // 32 columns of bf16 pairs.
+        // of the K block; each lane reads the 64 codes of its row's half, hands the weight slot
+        // back, and stores them dequantised as 32 columns of bf16 pairs.
         const int group = (warp - Cfg::DQ0) / Cfg::DQ_GROUP;
         const int quarter = warp & 3;
         const int khalf = ((warp - Cfg::DQ0) >> 2) & 1;
@@ -252,39 +292,42 @@ __global__ void __launch_bounds__(LinCfg<MT, XT>::THREADS, 1)
         const uint32_t lane_base = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(Cfg::W_COL0 + 32 * khalf);
         float sc_next = group < num_kb ? __ldg(ws_row + group) : 0.f;
-        int a = group;                                  // stage of kb (group < sa)
-        uint32_t pa = 0;
         for (int kb = group; kb < num_kb; kb += Cfg::DQ_GROUPS) {
-            const int b = kb % Cfg::SB;
+            const int b = kb % Cfg::SB, ws = kb % Cfg::SW;
             const float sc = sc_next;                   // the block scale, fetched one step early
             if (kb + Cfg::DQ_GROUPS < num_kb) sc_next = __ldg(ws_row + kb + Cfg::DQ_GROUPS);
-            if (!warp_wait(&emptyB[b], static_cast<uint32_t>(((kb / Cfg::SB) & 1) ^ 1)) ||
-                !warp_wait(&fullA[a], pa)) {
+            if (!warp_wait(&fullW[ws], static_cast<uint32_t>((kb / Cfg::SW) & 1))) {
+                if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                break;
+            }
+            const uint8_t* wslot = sW + ws * Cfg::W_TILE;
+            uint4 v[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                v[i] = *reinterpret_cast<const uint4*>(wslot + sw128(r, 4 * khalf + i));
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&emptyW[ws]);
+            if (!warp_wait(&emptyB[b], static_cast<uint32_t>(((kb / Cfg::SB) & 1) ^ 1))) {
                 if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                 break;
             }
             tc_fence_after();
-            const uint8_t* qslot = sA + a * Cfg::A_SLOT;
             uint32_t o[32];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint4 v = *reinterpret_cast<const uint4*>(qslot + sw128(r, 4 * khalf + i));
-                dequant8(v.x, v.y, sc, o + 8 * i);
-                dequant8(v.z, v.w, sc, o + 8 * i + 4);
+                dequant8(v[i].x, v[i].y, sc, o + 8 * i);
+                dequant8(v[i].z, v[i].w, sc, o + 8 * i + 4);
             }
             tmem_st_32cols(lane_base + static_cast<uint32_t>(b * Cfg::W_COLS), o);
             tmem_wait_st();
             tc_fence_before();
+            if (XT == 1 && (warp - Cfg::DQ0) % Cfg::DQ_GROUP == 0 &&
+                !warp_wait(&fullX[kb % Cfg::SX], static_cast<uint32_t>((kb / Cfg::SX) & 1))) {
+                if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                break;
+            }
             __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&emptyA[a]);
-                mbar_arrive(&deqB[b]);
-            }
-            a += Cfg::DQ_GROUPS;                        // DQ_GROUPS < sa: at most one wrap
-            if (a >= sa) {
-                a -= sa;
-                pa ^= 1;
-            }
+            if (lane == 0) mbar_arrive(&deqB[b]);
         }
     } else if (warp >= 2) {
         // Epilogue: TMEM lane = output column n0 + 32 * quarter + lane, columns = rows of x;
@@ -336,20 +379,14 @@ template <int MT, int XT>
 cudaError_t launch_lin(const CUtensorMap& tmW, const CUtensorMap& tmX, const float* w_s, void* y,
                        int M, int N, int K, int weights_constant, cudaStream_t stream) {
     using Cfg = LinCfg<MT, XT>;
-    // the W' ring lives in TMEM; shared memory holds the e4m3 weight stream and the rows of x
-    const int bar_bytes = 8 * (2 * kMaxStages + 2 * Cfg::SB + 2) + 16;
-    int sa = (kSmemLimit - 1024 - bar_bytes) / Cfg::A_SLOT;
-    if (sa > kMaxStages) sa = kMaxStages;
-    if (sa < 2) return cudaErrorInvalidValue;
-    const int smem = 1024 + sa * Cfg::A_SLOT + bar_bytes;
-    cudaError_t e = set_smem(linear_bf16_swap_kernel<MT, XT>, smem);
+    cudaError_t e = set_smem(linear_bf16_swap_kernel<MT, XT>, Cfg::SMEM);
     if (e != cudaSuccess) return e;
     const int64_t ctas =
         static_cast<int64_t>((N + BM - 1) / BM) * ((M + MT * XT - 1) / (MT * XT));
     if (ctas > INT32_MAX) return cudaErrorInvalidValue;
     const dim3 grid(static_cast<unsigned>(ctas));
-    return launch_pdl(linear_bf16_swap_kernel<MT, XT>, grid, Cfg::THREADS, smem, stream, tmW,
-                      tmX, w_s, y, M, N, K, sa, weights_constant);
+    return launch_pdl(linear_bf16_swap_kernel<MT, XT>, grid, Cfg::THREADS, Cfg::SMEM, stream, tmW,
+                      tmX, w_s, y, M, N, K, weights_constant);
 }
 
 }  // namespace
