@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "de8004d4487b4a63", "per_launch_mb": (134.96 + 135.11) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "ed96b08a310ef277", "per_launch_mb": (135.04 + 135.09) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting
