@@ -228,7 +228,8 @@ class Gpu:
         return self._ws
 
     def act_quant_gemm(self, x, y, s, b, b_s, c, M, N, K, fmt=0, flags=0):
-        """act_quant + fp8_gemm through fp8bs_act_quant_gemm (one launch at decode sizes)."""
+        """act_quant + fp8_gemm through fp8bs_act_quant_gemm: two launches (the GEMM starting
+        under act_quant), or one with FP8BS_GEMM_QUANT_IN_KERNEL in flags."""
         ws = self.workspace()
         self.fp8bs.fp8bs_act_quant_gemm(x.data_ptr(), y.data_ptr(), s.data_ptr(), b.data_ptr(),
                                         b_s.data_ptr(), c.data_ptr(), M, N, K, fmt, flags,
