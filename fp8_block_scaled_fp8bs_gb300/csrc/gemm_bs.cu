@@ -46,20 +46,28 @@ namespace {
 
 template <int BN>
 struct BsCfg {
-    static_assert(BN == 64 || BN == 128, "the B exponent must be uniform over a tile");
+    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static constexpr int SF_WARPS = 4;
     static constexpr int EPI_WARPS = 4;
     static constexpr int THREADS = 32 * (SF_WARPS + EPI_WARPS + 2);
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
-    static constexpr int SF_COLS = 8;                 // per stage: A in 0..3, B in 4..7
-    static constexpr int SF_COL0 = 2 * BN;            // after the two accumulators
+    // Scale-factor columns per stage: A in 0..3, then B: 4 columns (one 128-row block of B
+    // per tile, BN <= 128) or 8 (BN = 256: columns 4..7 for the tile's first block, 8..11 for
+    // its second).
+    static constexpr int SF_B_COLS = BN > 128 ? 8 : 4;
+    static constexpr int SF_COLS = 4 + SF_B_COLS;
+    // Accumulators: two BN-column buffers (the epilogue of one tile overlaps the next), or at
+    // BN = 256 one (two would fill TMEM and leave no room for scale factors).
+    static constexpr int NBUF = BN > 128 ? 1 : 2;
+    static constexpr int SF_COL0 = NBUF * BN;
     static constexpr int PART = BM * BN * 4;          // one fp32 partial tile (stream-K)
 };
 
 template <int BN>
 __host__ __device__ constexpr uint32_t bs_tmem_cols(int stages) {
-    return tmem_cols_for(static_cast<uint32_t>(2 * BN + stages * BsCfg<BN>::SF_COLS));
+    return tmem_cols_for(
+        static_cast<uint32_t>(BsCfg<BN>::NBUF * BN + stages * BsCfg<BN>::SF_COLS));
 }
 
 // Biased exponent of a scale that must be 2^e with -126 <= e <= 127: for such a value the
@@ -192,7 +200,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                 }
                 if (!ok) break;
                 mma_commit(&ring.tfull[buf]);
-                buf ^= 1;
+                if (Cfg::NBUF == 2) buf ^= 1;
                 if (buf == 0) tphase ^= 1;
             }
             // Make sure nothing this thread issued is still running before TMEM is freed.
@@ -215,12 +223,15 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             const float* as_row = g.a_s + static_cast<int64_t>(row) * num_kb;
             const float* bs_row =
                 g.b_s + (static_cast<int64_t>(t.g) * nb_count + t.n0 / 128) * num_kb;
-            float va[P], vb[P];
+            // BN = 256: the tile's second 128-row block of B (the first again past N)
+            const float* bs_row2 = BN > 128 && t.n0 / 128 + 1 < nb_count ? bs_row + num_kb : bs_row;
+            float va[P], vb[P], vb2[P];
 #pragma unroll
             for (int i = 0; i < P; ++i) {
                 if (kb0 + i < kb1) {
                     va[i] = __ldg(as_row + kb0 + i);
                     vb[i] = __ldg(bs_row + kb0 + i);
+                    if constexpr (BN > 128) vb2[i] = __ldg(bs_row2 + kb0 + i);
                 }
             }
             for (int kbp = kb0; ok && kbp < kb1; kbp += P) {
@@ -230,9 +241,12 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     if (kb >= kb1) break;
                     const uint32_t wa = splat4(ue8m0_code(va[i], pow2));
                     const uint32_t wb = splat4(ue8m0_code(vb[i], pow2));
+                    uint32_t wb2 = 0;
+                    if constexpr (BN > 128) wb2 = splat4(ue8m0_code(vb2[i], pow2));
                     if (kb + P < kb1) {                 // the scales of kb + P, in flight
                         va[i] = __ldg(as_row + kb + P);
                         vb[i] = __ldg(bs_row + kb + P);
+                        if constexpr (BN > 128) vb2[i] = __ldg(bs_row2 + kb + P);
                     }
                     if (!warp_wait(&ring.empty[stage], phase ^ 1)) {
                         if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
@@ -244,6 +258,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                                            static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
                     tmem_st_4cols(taddr, wa, wa, wa, wa);
                     tmem_st_4cols(taddr + 4, wb, wb, wb, wb);
+                    if constexpr (BN > 128) tmem_st_4cols(taddr + 8, wb2, wb2, wb2, wb2);
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -311,14 +326,32 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             const bool vec = (g.N & 7) == 0;
 
             if (kb0 == 0 && kb1 == num_kb) {
-                // A whole tile: the accumulator into registers, the buffer back, then store.
-                float acc[BN];
+                if constexpr (BN > 128) {
+                    // A whole 256-wide tile (one buffer): 32 columns at a time, the next
+                    // chunk's load in flight while one is stored; the buffer goes back after
+                    // the last load.
+                    float va[32], vb[32];
+                    tmem_ld_32cols(taddr, va);
+                    tmem_wait_ld_32(va);
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
+                    for (int c = 0; c < BN / 32; ++c) {
+                        float* cur = (c & 1) ? vb : va;
+                        float* nxt = (c & 1) ? va : vb;
+                        if (c + 1 < BN / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+                        if (store) store_row_bf16<32>(crow + 32 * c, cur, valid - 32 * c, vec);
+                        if (c + 1 < BN / 32) tmem_wait_ld_32(nxt);
+                    }
+                    release_tmem(&ring.tempty[buf], lane);
+                } else {
+                    // A whole tile: the accumulator into registers, the buffer back, then store.
+                    float acc[BN];
 #pragma unroll
-                for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
-                release_tmem(&ring.tempty[buf], lane);
-                if (store) store_row_bf16<BN>(crow, acc, valid, vec);
+                    for (int c = 0; c < BN / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
+#pragma unroll
+                    for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
+                    release_tmem(&ring.tempty[buf], lane);
+                    if (store) store_row_bf16<BN>(crow, acc, valid, vec);
+                }
             } else if (kb0 > 0) {
                 // A piece that does not start its tile: publish the partial in this CTA's slot,
                 // 32 columns at a time, and count it in the flag of the tile's owner.
@@ -378,7 +411,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                 release_tmem(&ring.tempty[buf], lane);
                 if (!have) ok = false;
             }
-            buf ^= 1;
+            if (Cfg::NBUF == 2) buf ^= 1;
             if (buf == 0) tphase ^= 1;
         }
     }
@@ -394,6 +427,8 @@ cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
                       const GroupTable& gt, int num_sms, const StreamKArgs& ska,
                       cudaStream_t stream) {
     using Cfg = BsCfg<BN>;
+    // A 256-wide partial tile would not fit in shared memory: that width runs whole tiles.
+    if (BN > 128 && ska.workspace) return cudaErrorInvalidValue;
     int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
     static_assert(bs_tmem_cols<BN>(kMaxStages) <= 512, "TMEM holds 512 columns");
     // Stream-K keeps one partial tile (and its barrier) in shared memory, at two stages' cost.
@@ -414,7 +449,10 @@ cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 
 }  // namespace
 
+// 256-wide tiles (a third fewer shared-memory bytes per MAC than 128) once they alone give every
+// SM at least two; else 128, or 64 when 128-wide tiles would leave many SMs idle.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
+    if (m_tiles_total * ((N + 255) / 256) >= 2 * static_cast<int64_t>(num_sms)) return 256;
     return m_tiles_total * ((N + 127) / 128) * 5 >= num_sms * 4 ? 128 : 64;
 }
 
@@ -424,6 +462,7 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     switch (BN) {
         case 64: return launch_bs<64>(tmA, tmB, g, gt, num_sms, ska, stream);
         case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, ska, stream);
+        case 256: return launch_bs<256>(tmA, tmB, g, gt, num_sms, ska, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -396,17 +396,30 @@ def test_gemm_ue8m0_block_scaled_full_compare(M, N, K):
                       f"ue8m0 {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (2560, 4096, 256),     # 320 tiles of 128 x 256: the 256-wide block-scaled kernel
+    (2600, 3900, 384),     # ragged rows; the last tile holds one 128-row block of B, half past N
+])
+def test_gemm_ue8m0_256_wide_tiles(M, N, K):
+    a, a_s, b, b_s = pow2_case(M, N, K, M + N + K)
+    assert_gemm_close(run_gemm(a, a_s, b, b_s, "ue8m0"), oracle.gemm(a, a_s, b, b_s),
+                      f"ue8m0 {M}x{N}x{K}")
+
+
 def random_codes(rng, rows, cols):
     c = rng.integers(0, 256, size=(rows, cols), dtype=np.uint8)
     c[(c & 0x7F) == 0x7F] = 0x00                        # no NaN codes
     return c
 
 
-def test_gemm_ue8m0_per_row_and_block_exponents():
+@pytest.mark.parametrize("M,N,K", [
+    (384, 384, 1152),      # 128-wide tiles
+    (2560, 4096, 640),     # 256-wide tiles: two blocks of B, two exponents per tile
+])
+def test_gemm_ue8m0_per_row_and_block_exponents(M, N, K):
     """Every row of A and every 128-row block of B carries its own exponent in every K block,
     so a scale factor taken from the wrong row, column block, K block or pipeline stage moves
     whole output regions out of tolerance."""
-    M, N, K = 384, 384, 1152
     rng = np.random.default_rng(11)
     a, b = random_codes(rng, M, K), random_codes(rng, N, K)
     m = np.arange(M)[:, None]
@@ -414,8 +427,13 @@ def test_gemm_ue8m0_per_row_and_block_exponents():
     a_s = np.ldexp(1.0, ((m * 7 + kb * 3) % 9) - 4 - 8).astype(np.float32)
     nb = np.arange(N // 128)[:, None]
     b_s = np.ldexp(1.0, ((nb * 5 + kb * 2) % 7) - 3 - 8).astype(np.float32)
-    assert_gemm_close(run_gemm(a, a_s, b, b_s, "ue8m0"), oracle.gemm(a, a_s, b, b_s),
-                      "ue8m0 exponent pattern")
+    c = run_gemm(a, a_s, b, b_s, "ue8m0")
+    if M * N <= 384 * 384:
+        assert_gemm_close(c, oracle.gemm(a, a_s, b, b_s), "ue8m0 exponent pattern")
+    else:
+        mi, ni = tile_samples(M, N, 2, seed=K)
+        assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni),
+                          "ue8m0 exponent pattern (sampled)")
 
 
 def test_gemm_ue8m0_extreme_exponents():
