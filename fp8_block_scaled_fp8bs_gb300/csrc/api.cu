@@ -136,8 +136,9 @@ fp8bs::StreamKArgs plan_stream_k_bs(int64_t m_tiles, int64_t N, int64_t num_kb, 
                                     void* workspace) {
     if (!workspace || num_kb < 2) return no_stream_k();
     const int bn_dp = fp8bs::pick_tile_n_bs(m_tiles, N, sms);
-    if (bn_dp > 128) return no_stream_k();      // enough 256-wide tiles for every SM
-    const int64_t cost_dp = ceil_div(m_tiles * ceil_div(N, bn_dp), sms) * num_kb;
+    // whole tiles at bn_dp against shared 128-wide tiles, in 128-wide K-block times
+    const int64_t cost_dp =
+        ceil_div(m_tiles * ceil_div(N, bn_dp), sms) * num_kb * (bn_dp > 128 ? 134 : 100) / 100;
     const int64_t tiles = m_tiles * ceil_div(N, 128);
     if (tiles < sms || !units_fit(tiles, num_kb)) return no_stream_k();
     const int dp = dp_tiles_before_sharing(tiles, sms);

@@ -449,11 +449,23 @@ cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
 
 }  // namespace
 
-// 256-wide tiles (a third fewer shared-memory bytes per MAC than 128) once they alone give every
-// SM at least two; else 128, or 64 when 128-wide tiles would leave many SMs idle.
+// Tile width by rounds of tiles over the SMs times the measured time of one K block at that
+// width (~886 clk at 256, ~660 at 128 and about the same at 64, at prefill shapes): 256-wide
+// tiles carry a third fewer operand bytes per MAC but leave more SMs idle when tiles are few.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
-    if (m_tiles_total * ((N + 255) / 256) >= 2 * static_cast<int64_t>(num_sms)) return 256;
-    return m_tiles_total * ((N + 127) / 128) * 5 >= num_sms * 4 ? 128 : 64;
+    static const int kWidth[3] = {256, 64, 128};     // on a tie the narrower of 64 and 128
+    static const int kCost[3] = {134, 100, 100};
+    int best = 128;
+    int64_t best_cost = INT64_MAX;
+    for (int i = 0; i < 3; ++i) {
+        const int64_t tiles = m_tiles_total * ((N + kWidth[i] - 1) / kWidth[i]);
+        const int64_t cost = (tiles + num_sms - 1) / num_sms * kCost[i];
+        if (cost < best_cost) {
+            best_cost = cost;
+            best = kWidth[i];
+        }
+    }
+    return best;
 }
 
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
