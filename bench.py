@@ -652,6 +652,16 @@ def run_profile(case: str, launches: int, warmup: int):
         c = torch.empty((4096, N), dtype=torch.bfloat16, device="cuda")
         g.act_quant(x, y, s, 4096, K)
         fn = lambda: g.gemm_ws(y, s, B, S, c, 4096, N, K)  # noqa: E731
+    elif case == "prefill_up_ue8m0":
+        # the prefill up-projection with ue8m0 scales, on the block-scaled kernel
+        b, bs = synth.weights(N_DIM, K_DIM, 0, "prefill/B_up", pow2=True)
+        B, S = g.e4m3(b), g.f32(bs)
+        x = g.bf16(synth.prefill_up())
+        y = torch.empty((4096, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((4096, K_DIM // 128), dtype=torch.float32, device="cuda")
+        c = torch.empty((4096, N_DIM), dtype=torch.bfloat16, device="cuda")
+        g.act_quant(x, y, s, 4096, K_DIM, 1)
+        fn = lambda: g.gemm_ws(y, s, B, S, c, 4096, N_DIM, K_DIM, 1)  # noqa: E731
     elif case.startswith("mla"):
         # ue8m0 MLA projection on the block-scaled kernel: mla1536 or mla576
         N = int(case[len("mla"):] or synth.Q_LORA)
@@ -751,7 +761,7 @@ def main(argv=None):
                     "and no CPU baseline")
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
     ap.add_argument("--profile", metavar="CASE", default=None,
-                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, mla1536, mla576, linear1..linear4096, "
+                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, prefill_up_ue8m0, mla1536, mla576, linear1..linear4096, "
                          "act_quant, dequant, moe): warmup + steps launches, for ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
