@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "ed96b08a310ef277", "per_launch_mb": (135.04 + 135.09) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "380089e60e1f3fad", "per_launch_mb": (134.90 + 135.37) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting

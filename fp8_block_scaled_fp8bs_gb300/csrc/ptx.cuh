@@ -192,17 +192,6 @@ __device__ __forceinline__ void mma_f8(uint32_t d_tmem, uint64_t a_desc, uint64_
         : "memory");
 }
 
-// D[tmem] (+)= A * B^T for bf16 operands (kind::f16, K = 16 per instruction); one thread issues.
-__device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                         uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
 // D[tmem] (+)= (A * 2^sfa) * (B * 2^sfb)^T with ue8m0 scale factors read from TMEM, one per 32
 // elements of K per row of A and per row of B (kind::mxf8f6f4, scale_vec::1X); one thread issues.
 __device__ __forceinline__ void mma_f8_block_scaled(uint32_t d_tmem, uint64_t a_desc,
