@@ -540,14 +540,38 @@ def secondary(g: Gpu, peaks, reps=20):
     # one launch: max(total FLOPs / peak, total bytes / bandwidth)
     total_bytes = sum(gemm_bytes(int(m), synth.MOE_INTER, K_DIM) for m in counts if m > 0)
     bound = max(flops / (fp8_peak * 1e9), total_bytes / (hbm * 1e6))
-    for name, fn in (("moe_32_experts_grouped", moe_grouped), ("moe_32_experts_loop", moe)):
+    # The per-expert loop captured once in a CUDA graph (the host's per-call work, argument
+    # checks and tensor maps, is then paid at capture, not per replay).
+    cap = torch.cuda.Stream()
+    cap.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+
+    def moe_on(stream_handle):
+        for e in range(32):
+            lo, hi = int(offs[e]), int(offs[e + 1])
+            if hi > lo:
+                g.fp8bs.fp8bs_gemm(y[lo:hi].data_ptr(), s[lo:hi].data_ptr(), Bs[e][0].data_ptr(),
+                                   Bs[e][1].data_ptr(), cs[e].data_ptr(), hi - lo,
+                                   synth.MOE_INTER, K_DIM, 0, stream_handle)
+    variants = [("moe_32_experts_grouped", moe_grouped), ("moe_32_experts_loop", moe)]
+    try:
+        with torch.cuda.stream(cap):
+            moe_on(cap.cuda_stream)                   # warm-up: one-time kernel attributes
+        cap.synchronize()
+        with torch.cuda.graph(graph, stream=cap):
+            moe_on(cap.cuda_stream)
+        variants.append(("moe_32_experts_loop_graph", graph.replay))
+    except RuntimeError as err:                       # reported, not fatal to the benchmark
+        out["moe_32_experts_loop_graph"] = {"unavailable": str(err).splitlines()[0][:200]}
+
+    for name, fn in variants:
         fn()
         ms = g.time_each(fn, reps)
         out[name] = {"M_e_min": int(counts.min()), "M_e_max": int(counts.max()),
                      "N": synth.MOE_INTER, "K": K_DIM, "us": round(ms * 1e3, 2),
                      "TFLOP/s": round(flops / ms / 1e9, 1),
                      "frac_roofline": round(bound / ms, 4),
-                     "launches": 1 if fn is moe_grouped else int((counts > 0).sum())}
+                     "launches": 1 if name == "moe_32_experts_grouped" else int((counts > 0).sum())}
     return out
 
 
