@@ -788,7 +788,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--quick", action="store_true", help="headline only: no secondary workloads "
                     "and no CPU baseline")
-    ap.add_argument("--out-dir", default=os.path.join(ROOT, "gpurun_out"))
+    ap.add_argument("--out-dir", default=os.path.join(ROOT, "bench_out"),
+                    help="where the per-rank clock samples (clocks_rank<r>.csv) are written")
     ap.add_argument("--profile", metavar="CASE", default=None,
                     help="run one kernel only (decode1..decode64, prefill_up, prefill_down, prefill_up_ue8m0, mla1536, mla576, linear1..linear4096, "
                          "act_quant, dequant, moe): warmup + steps launches, for ncu")
