@@ -198,7 +198,8 @@ FP8BS_API int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void*
  * Administrator & Developer Guide", §6.3: with gemm_impl = "bf16", weight_dequant (§8.5.2)
  * then a bf16 GEMM). W' is formed tile by tile on chip (in tensor memory), never in HBM;
  * products are accumulated in fp32 on the tensor cores and y is rounded once to bf16. Any M:
- * each CTA pairs one 128-row slab of w with up to 128 rows of x.
+ * each CTA pairs one 128-row slab of w with up to 128 rows of x, or two tiles of 128 rows
+ * when M > 128.
  *
  *   x    [in]  bf16 [M, K], 16-byte aligned.
  *   w    [in]  e4m3 [N, K], 16-byte aligned.
