@@ -58,3 +58,25 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch):
     with redirect_stdout(buf):
         assert bench.run_reference(Args, 2, 0) == 0
     assert called == [256] and '"impl": "reference"' in buf.getvalue()
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` end to end on CPU (it times the oracle, no GPU): one JSON
+    line with the keys and units of the GPU arm's line, on the same workload."""
+    import json
+    import subprocess
+    sys.path.insert(0, ROOT)
+    import bench
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                          "--steps", "1", "--warmup", "3"], capture_output=True, text=True,
+                         timeout=300, cwd=ROOT, check=True).stdout.strip().splitlines()
+    line = json.loads(out[-1])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True
+    assert (line["steps"], line["warmup"], line["n_gpus"]) == (1, 3, 1)
+    assert line["config"] == bench.workload_config()
+    assert line["value"] > 0 and line["ms_per_step"] > 0
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
