@@ -8,15 +8,21 @@
 // sum_kb a_s * b_s * P_kb exactly as §8.5.3 defines it (a power-of-two factor is exact in
 // fp32), and the accumulator then stays in TMEM for the whole K loop: no promotion pass.
 //
-// Warp layout (320 threads):
+// Warp layout (320 threads; 352 at BN = 64):
 //   warps 0 .. 3   scale-factor writers: per K block, tcgen05.st the exponents of the tile's
 //                  128 rows of a_s and of its b_s block into the stage's TMEM scale slot
 //   warps 4 .. 7   epilogue: read the finished accumulator, round to bf16, store
 //   warp 8         TMA producer
 //   warp 9         MMA issuer (allocates and frees TMEM)
-// TMEM: two BN-column accumulators, then per stage 8 columns of scale factors (4 for A, 4 for
-// B). A stage's full barrier completes when its TMA bytes have landed AND the four scale-factor
-// warps have written its slot; the MMA's commit to the stage's empty barrier frees both.
+//   warp 10        BN = 64 only: a second MMA issuer. The two take a tile's K blocks in turn,
+//                  each into its own accumulator; the epilogue adds the two. One thread
+//                  issuing alone waits for its MMAs to drain at every barrier wait, which at
+//                  this width costs more than the MMAs themselves (MLA N = 576: 22.2 us with
+//                  one issuer, 17.9-18.3 us with two).
+// TMEM: two accumulator buffers (BN columns per issuer), then per stage 8 columns of scale
+// factors (4 for A, 4 or 8 for B). A stage's full barrier completes when its TMA bytes have
+// landed AND the four scale-factor warps have written its slot; the MMA's commit to the
+// stage's empty barrier frees both.
 //
 // Scale-factor placement. The tensor core takes the exponent of row m of A from lane m,
 // column m/32 of the A slot, and the exponent of row n of B (for output rows of lane quarter q)
@@ -49,7 +55,10 @@ struct BsCfg {
     static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
     static constexpr int SF_WARPS = 4;
     static constexpr int EPI_WARPS = 4;
-    static constexpr int THREADS = 32 * (SF_WARPS + EPI_WARPS + 2);
+    // MMA issuers: two at BN = 64, taking a tile's K blocks in turn into accumulators of their
+    // own. Wider tiles keep one: two buffers of two accumulators would not fit in TMEM.
+    static constexpr int ISSUERS = BN <= 64 ? 2 : 1;
+    static constexpr int THREADS = 32 * (SF_WARPS + EPI_WARPS + 1 + ISSUERS);
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
     // Scale-factor columns per stage: A in 0..3, then B: 4 columns (one 128-row block of B
@@ -60,14 +69,15 @@ struct BsCfg {
     // Accumulators: two BN-column buffers (the epilogue of one tile overlaps the next), or at
     // BN = 256 one (two would fill TMEM and leave no room for scale factors).
     static constexpr int NBUF = BN > 128 ? 1 : 2;
-    static constexpr int SF_COL0 = NBUF * BN;
+    static constexpr int ACC = ISSUERS * BN;          // TMEM columns of one buffer
+    static constexpr int SF_COL0 = NBUF * ACC;
     static constexpr int PART = BM * BN * 4;          // one fp32 partial tile (stream-K)
 };
 
 template <int BN>
 __host__ __device__ constexpr uint32_t bs_tmem_cols(int stages) {
     return tmem_cols_for(
-        static_cast<uint32_t>(BsCfg<BN>::NBUF * BN + stages * BsCfg<BN>::SF_COLS));
+        static_cast<uint32_t>(BsCfg<BN>::NBUF * BsCfg<BN>::ACC + stages * BsCfg<BN>::SF_COLS));
 }
 
 // Biased exponent of a scale that must be 2^e with -126 <= e <= 127: for such a value the
@@ -120,6 +130,12 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     grid_launch_dependents();
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS, 1 + Cfg::SF_WARPS);
+        if constexpr (Cfg::ISSUERS > 1) {
+            // every issuer commits each finished buffer and its final drain
+            for (int b = 0; b < 2; ++b) mbar_init(&ring.tfull[b], Cfg::ISSUERS);
+            mbar_init(ring.drain, Cfg::ISSUERS);
+            fence_barrier_init();
+        }
         if (stream_k) {
             mbar_init(part_bar, 1);
             fence_barrier_init();
@@ -163,8 +179,9 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             }
             if (!ok) drain_tma(ring, stages, issued);
         }
-    } else if (warp == ISSUER) {
+    } else if (warp >= ISSUER && warp < ISSUER + Cfg::ISSUERS) {
         if (lane == 0) {
+            const int me = warp - ISSUER;
             constexpr uint32_t idesc = idesc_e4m3_block_scaled(BM, BN);
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
@@ -175,8 +192,16 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                const uint32_t d_tmem =
+                    tmem_base + static_cast<uint32_t>(buf * Cfg::ACC + me * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
+                    if ((kb - kb0) % Cfg::ISSUERS != me) {     // the other issuer's K block
+                        if (++stage == stages) {
+                            stage = 0;
+                            phase ^= 1;
+                        }
+                        continue;
+                    }
                     if (!mbar_wait(&ring.full[stage], phase)) {
                         record_error(FP8BS_DEVERR_MMA_WAIT);
                         ok = false;
@@ -191,7 +216,8 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     for (int j = 0; j < BK / MMA_K; ++j)
                         mma_f8_block_scaled(d_tmem, smem_desc_k_sw128(a_addr + j * MMA_K),
                                             smem_desc_k_sw128(b_addr + j * MMA_K), idesc, sfa,
-                                            sfa + 4, (kb > kb0 || j > 0) ? 1u : 0u);
+                                            sfa + 4,
+                                            (kb - kb0 >= Cfg::ISSUERS || j > 0) ? 1u : 0u);
                     mma_commit(&ring.empty[stage]);
                     if (++stage == stages) {
                         stage = 0;
@@ -317,7 +343,9 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             }
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                                   static_cast<uint32_t>(buf * BN);
+                                   static_cast<uint32_t>(buf * Cfg::ACC);
+            // the second issuer's accumulator (BN columns on) holds K blocks kb0 + 1, kb0 + 3..
+            const bool two = Cfg::ISSUERS > 1 && kb1 - kb0 > 1;
             const int row = t.m0 + row_in_tile;
             const bool store = row < t.row_end;
             __nv_bfloat16* crow =
@@ -349,6 +377,18 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     for (int c = 0; c < BN / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
+                    if constexpr (Cfg::ISSUERS > 1) {
+                        if (two) {
+                            float t[BN];
+#pragma unroll
+                            for (int c = 0; c < BN / 32; ++c)
+                                tmem_ld_32cols(taddr + BN + 32 * c, t + 32 * c);
+#pragma unroll
+                            for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(t + 32 * c);
+#pragma unroll
+                            for (int i = 0; i < BN; ++i) acc[i] += t[i];
+                        }
+                    }
                     release_tmem(&ring.tempty[buf], lane);
                     if (store) store_row_bf16<BN>(crow, acc, valid, vec);
                 }
@@ -361,6 +401,15 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     float v[32];
                     tmem_ld_32cols(taddr + 32 * c, v);
                     tmem_wait_ld_32(v);
+                    if constexpr (Cfg::ISSUERS > 1) {
+                        if (two) {
+                            float t[32];
+                            tmem_ld_32cols(taddr + BN + 32 * c, t);
+                            tmem_wait_ld_32(t);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += t[i];
+                        }
+                    }
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         __stcg(slot + (8 * c + q) * BM + row_in_tile,
@@ -383,6 +432,15 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     float v[32];
                     tmem_ld_32cols(taddr + 32 * c, v);
                     tmem_wait_ld_32(v);
+                    if constexpr (Cfg::ISSUERS > 1) {
+                        if (two) {
+                            float t[32];
+                            tmem_ld_32cols(taddr + BN + 32 * c, t);
+                            tmem_wait_ld_32(t);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += t[i];
+                        }
+                    }
                     if (have) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
