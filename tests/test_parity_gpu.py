@@ -389,6 +389,7 @@ def pow2_case(M, N, K, seed):
     (64, 1536, 1024),                                   # few rows: swapped kernel, ue8m0 scales
     (129, 256, 512), (200, 640, 1024), (300, 576, 384), (513, 97, 256), (1024, 2048, 256),
     (2048, 1536, 512), (700, 1000, 256), (1100, 4736, 256), (256, 128, 7168), (384, 200, 2048),
+    (300, 576, 128),        # 64-wide tiles, one K block: the second MMA issuer has none
 ])
 def test_gemm_ue8m0_block_scaled_full_compare(M, N, K):
     a, a_s, b, b_s = pow2_case(M, N, K, M + N + K)
