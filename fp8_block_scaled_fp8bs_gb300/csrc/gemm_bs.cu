@@ -28,9 +28,10 @@
 // column m/32 of the A slot, and the exponent of row n of B (for output rows of lane quarter q)
 // from lane 32q + n%32, column n/32 of the B slot -- measured on GB300 by giving every lane,
 // column and byte of the slots a distinct exponent. Lane L writes the exponent of tile row L
-// into all four columns of the A slot. Tiles are BN <= 128 columns wide and start on a multiple
-// of BN, so a tile lies inside one 128-row block of B and its B exponent is one value, written
-// to every lane and column of the B slot. Every byte of a word holds the same exponent.
+// into all four columns of the A slot. Tiles start on a multiple of BN: a 64- or 128-wide tile
+// lies inside one 128-row block of B, whose exponent is written to every lane and column of a
+// 4-column B slot; a 256-wide tile spans two blocks, whose exponents fill columns 0-3 and 4-7
+// of an 8-column B slot. Every byte of a word holds the same exponent.
 //
 // Work schedule. Data-parallel: CTA c computes tiles c, c + gridDim.x, ... whole. Stream-K
 // (when a workspace is given and the tiles alone would leave SMs idle): the tiles x K blocks
@@ -39,9 +40,9 @@
 // start inside a tile; that CTA writes its fp32 partial to its own workspace slot and counts it
 // in the flag of the tile's owner, the CTA holding the tile's first K blocks (the last piece of
 // its own range). The owner waits for its flag, adds the partials in K order -- a fixed order,
-// so results do not depend on timing -- resets the flag and stores. It only waits on CTAs after it, each of which
-// writes its partial before anything else, and every CTA of the grid is resident (one per
-// SM), so the wait always ends.
+// so results do not depend on timing -- resets the flag and stores. It only waits on CTAs
+// after it, each of which writes its partial before anything else, and every CTA of the grid
+// is resident (one per SM), so the wait always ends.
 #include <atomic>
 
 #include "gemm_common.cuh"
