@@ -43,8 +43,8 @@ DECODE_MS = synth.DECODE_MS
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 
-# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the decode GEMM,
-# from the ncu captures summarised in profiles/gemm_swapab_decode.md (mean of M=1 and M=64),
+# DRAM traffic (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the decode GEMM
+# kernel (gemm_swapab_kernel), from ncu captures of its M=1 and M=64 launches (their mean),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
 DECODE_TRAFFIC_MB = {"kernel_sha": "380089e60e1f3fad", "per_launch_mb": (134.90 + 135.37) / 2}
@@ -610,7 +610,7 @@ def cpu_baseline(target_s: float = 12.0):
         oracle_step(xs, b, bs)
     dt = (time.perf_counter() - t0) / reps
     return {"value": round(oracle_sample_bytes(n_rows) / dt / 1e9, 4), "unit": "GB/s", "cores": 1,
-            "kind": "oracle",
+            "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": (f"decode workload with N cut to the first {n_rows} of {N_DIM} weight rows: "
                        f"act_quant of all M in {list(DECODE_MS)} rows x {K_DIM} and fp8_gemm "
                        f"[M x {n_rows} x {K_DIM}]; single-threaded C, {reps} repetitions, "
@@ -771,7 +771,7 @@ def run_reference(args, world, rank):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle",
+                             "host_cores": os.cpu_count(), "kind": "oracle",
                              "sample": f"per step: decode workload with N cut to {n_rows} of "
                                        f"{N_DIM} weight rows (all M rows of act_quant)"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -831,8 +831,8 @@ def main(argv=None):
                 "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
                 "peak_source": f"{peaks['source']} hbm_gbs (copy bandwidth)",
                 "traffic": decode_traffic(),
-                "traffic_note": "dram read+write bytes per launch, ncu "
-                                "(profiles/gemm_swapab_decode.md); null if the kernel's sources changed",
+                "traffic_note": "dram read+write bytes per launch of gemm_swapab_kernel, from an "
+                                "ncu capture; null if the kernel's sources changed since",
                 "per_launch": [{"M": M, "us": round(d * 1e3, 2),
                                 "GB/s": round(gemm_bytes(M, N_DIM, K_DIM) / (d * 1e6), 1)}
                                for M, d in per_m]}

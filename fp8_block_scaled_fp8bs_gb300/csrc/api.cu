@@ -4,9 +4,57 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "../../include/fp8bs.h"
 #include "kernels.h"
+
+namespace fp8bs {
+
+int max_active_clusters(const void* kernel, int threads, int smem, int cluster_x) {
+    struct Entry {
+        const void* kernel;
+        int threads, smem, cluster_x, dev, n;
+    };
+    static std::mutex mu;
+    static Entry cache[128];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i) {
+            const Entry& c = cache[i];
+            if (c.kernel == kernel && c.threads == threads && c.smem == smem &&
+                c.cluster_x == cluster_x && c.dev == dev)
+                return c.n;
+        }
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(cluster_x));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(smem);
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+    }
+    std::lock_guard<std::mutex> lock(mu);
+    if (used < 128) cache[used++] = Entry{kernel, threads, smem, cluster_x, dev, n};
+    return n;
+}
+
+}  // namespace fp8bs
 
 namespace {
 
@@ -106,7 +154,7 @@ int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CU
 // Stream-K plans (see StreamKArgs in kernels.h). Whole tiles for all but the last one to two
 // waves, the rest shared; used when the busiest SM's K blocks (plus the hand-over of a partial)
 // drop clearly below the data-parallel schedule's ceil(tiles / SMs) whole tiles.
-fp8bs::StreamKArgs no_stream_k() { return fp8bs::StreamKArgs{nullptr, 0}; }
+fp8bs::StreamKArgs no_stream_k() { return fp8bs::StreamKArgs{nullptr, 0, 1}; }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -125,7 +173,48 @@ fp8bs::StreamKArgs plan_stream_k_tn(int64_t tiles, int64_t num_kb, int sms, void
     const int64_t cost_dp = ceil_div(tiles, sms) * num_kb;
     const int64_t cost_sk = dp / sms * num_kb + ceil_div((tiles - dp) * num_kb, sms) + 2;
     if (cost_sk * 100 >= cost_dp * 97) return no_stream_k();
-    return fp8bs::StreamKArgs{workspace, dp};
+    return fp8bs::StreamKArgs{workspace, dp, 1};
+}
+
+// Relative time of one K block of a 128 x bn tile (the tile-width models of the two kernels).
+int64_t width_cost(bool block_scaled, int bn) {
+    switch (bn) {
+        case 256: return block_scaled ? 134 : 141;
+        case 192: return block_scaled ? 117 : 129;
+        case 128: return 100;
+        default: return block_scaled ? 100 : 80;
+    }
+}
+
+// Split K inside a cluster (StreamKArgs::ksplit) when the tiles are few: the tile width and
+// split with the lowest modelled time -- a CTA's share of the K blocks plus two K blocks for the
+// exchange of partials, at the width's K-block cost -- provided every cluster of the grid can
+// be resident at once. Taken only if it beats `cost_plain` (the whole-tile schedule) by 10 %;
+// otherwise ksplit = 1.
+struct SplitPlan {
+    int bn;
+    int ksplit;
+};
+
+SplitPlan plan_split(bool block_scaled, int64_t m_tiles, int64_t N, int64_t num_kb, int sms,
+                     int64_t cost_plain) {
+    static const int kWidths[4] = {64, 128, 192, 256};    // on a tie the narrower
+    SplitPlan best = {0, 1};
+    int64_t best_cost = cost_plain * 9 / 10;
+    for (int bn : kWidths) {
+        const int64_t tiles = m_tiles * ceil_div(N, bn);
+        for (int S = fp8bs::kMaxSplit; S > 1; --S) {
+            if (tiles * S > sms || num_kb / S < 2) continue;
+            const int64_t cost = (ceil_div(num_kb, S) + 2) * width_cost(block_scaled, bn);
+            if (cost >= best_cost) continue;
+            const int fit = block_scaled ? fp8bs::max_split_clusters_bs(bn, S)
+                                         : fp8bs::max_split_clusters_tn(bn, S);
+            if (fit < tiles) continue;
+            best = SplitPlan{bn, S};
+            best_cost = cost;
+        }
+    }
+    return best;
 }
 
 // ue8m0 scales (block-scaled kernel, 128-column tiles when shared). Measured: with ranges
@@ -138,13 +227,65 @@ fp8bs::StreamKArgs plan_stream_k_bs(int64_t m_tiles, int64_t N, int64_t num_kb, 
     const int bn_dp = fp8bs::pick_tile_n_bs(m_tiles, N, sms);
     // whole tiles at bn_dp against shared 128-wide tiles, in 128-wide K-block times
     const int64_t cost_dp =
-        ceil_div(m_tiles * ceil_div(N, bn_dp), sms) * num_kb * (bn_dp > 128 ? 134 : 100) / 100;
+        ceil_div(m_tiles * ceil_div(N, bn_dp), sms) * num_kb * width_cost(true, bn_dp) / 100;
     const int64_t tiles = m_tiles * ceil_div(N, 128);
     if (tiles < sms || !units_fit(tiles, num_kb)) return no_stream_k();
     const int dp = dp_tiles_before_sharing(tiles, sms);
     const int64_t cost_sk = dp / sms * num_kb + ceil_div((tiles - dp) * num_kb, sms) + 4;
     if (cost_sk * 10 >= cost_dp * 9) return no_stream_k();
-    return fp8bs::StreamKArgs{workspace, dp};
+    return fp8bs::StreamKArgs{workspace, dp, 1};
+}
+
+// The kernel and launch configuration for a GEMM of this shape (fp8bs_gemm_plan reports it).
+struct GemmPlan {
+    int kind;                  // FP8BS_KERNEL_*
+    int tile;                  // MT (swapped) or BN (normal orientation)
+    fp8bs::StreamKArgs ska;    // stream-K workspace or split K (normal orientation)
+    int ksplit;                // CTAs per tile sharing its K loop in a cluster (1: none)
+};
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool block_scaled, void* workspace,
+                   int sms) {
+    GemmPlan p;
+    p.ska = no_stream_k();
+    p.ksplit = 1;
+    if (M <= 128) {
+        // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA (or
+        // per cluster, with the K loop split).
+        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+        const int S = fp8bs::plan_gemm_swapab(MT, false, static_cast<int>(M), static_cast<int>(N),
+                                              static_cast<int>(K), sms);
+        if (S > 0) {
+            p.kind = FP8BS_KERNEL_SWAPPED;
+            p.tile = MT;
+            p.ksplit = S;
+            return p;
+        }
+        // K too long to stage the activation scales: the normal kernel below.
+    }
+    const int64_t m_tiles = (M + 127) / 128;
+    int BN;
+    if (block_scaled) {
+        p.ska = plan_stream_k_bs(m_tiles, N, K / 128, sms, workspace);
+        BN = p.ska.workspace ? 128 : fp8bs::pick_tile_n_bs(m_tiles, N, sms);
+    } else {
+        BN = fp8bs::pick_tile_n(m_tiles, N, sms);
+        p.ska = plan_stream_k_tn(m_tiles * ceil_div(N, BN), K / 128, sms, workspace);
+    }
+    if (!p.ska.workspace) {
+        // Few tiles: split their K loops between the CTAs of a cluster, if that pays.
+        const int64_t cost_plain =
+            ceil_div(m_tiles * ceil_div(N, BN), sms) * (K / 128) * width_cost(block_scaled, BN);
+        const SplitPlan sp = plan_split(block_scaled, m_tiles, N, K / 128, sms, cost_plain);
+        if (sp.ksplit > 1) {
+            BN = sp.bn;
+            p.ska = fp8bs::StreamKArgs{nullptr, 0, sp.ksplit};
+            p.ksplit = sp.ksplit;
+        }
+    }
+    p.kind = block_scaled ? FP8BS_KERNEL_BLOCK_SCALED : FP8BS_KERNEL_PROMOTED;
+    p.tile = BN;
+    return p;
 }
 
 // fp8bs_gemm_ex and fp8bs_gemm_ws: checks, then the kernel for the shape (see fp8bs.h).
@@ -185,32 +326,22 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
     g.K = static_cast<int>(K);
     g.weights_constant = (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0;
 
-    CUtensorMap tmA, tmB;
-    if (M <= 128) {
-        // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA.
-        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-        if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, MT)) return FP8BS_ERR_CUDA;
-        cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, fp8bs::FusedQuant{}, st);
-        if (e != cudaErrorInvalidValue) return status_of(e);
-        // K too long to stage the activation scales: fall through to the normal kernel.
-    }
     const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
-    const int64_t m_tiles = (M + 127) / 128;
-    fp8bs::StreamKArgs ska;
-    int BN;
-    if (block_scaled) {
-        ska = plan_stream_k_bs(m_tiles, N, K / 128, sms, workspace);
-        BN = ska.workspace ? 128 : fp8bs::pick_tile_n_bs(m_tiles, N, sms);
-    } else {
-        BN = fp8bs::pick_tile_n(m_tiles, N, sms);
-        ska = plan_stream_k_tn(m_tiles * ceil_div(N, BN), K / 128, sms, workspace);
+    const GemmPlan p = plan_gemm(M, N, K, block_scaled, workspace, sms);
+    CUtensorMap tmA, tmB;
+    if (p.kind == FP8BS_KERNEL_SWAPPED) {
+        if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, p.tile))
+            return FP8BS_ERR_CUDA;
+        return status_of(
+            fp8bs::launch_gemm_swapab(tmB, tmA, g, p.tile, fp8bs::FusedQuant{}, p.ksplit, st));
     }
-    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, BN)) return FP8BS_ERR_CUDA;
+    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, p.tile)) return FP8BS_ERR_CUDA;
     const int64_t rows[2] = {0, M};
     fp8bs::GroupTable gt;
-    fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), BN);
-    if (block_scaled) return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, ska, st));
-    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, ska, st));
+    fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), p.tile);
+    if (block_scaled)
+        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, p.tile, sms, p.ska, st));
+    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, p.tile, sms, p.ska, st));
 }
 
 }  // namespace
@@ -319,12 +450,16 @@ int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b, const 
         fq.y = static_cast<uint4*>(y);
         fq.s = s;
         fq.ue8m0 = ue8m0 ? 1 : 0;
-        CUtensorMap tmA, tmB;
-        if (!make_map(&tmB, b, N, K, 128) || !make_map_bf16(&tmA, x, M, K, MT))
-            return FP8BS_ERR_CUDA;
-        const cudaError_t e = fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, fq, st);
-        if (e != cudaErrorInvalidValue) return status_of(e);
-        // K too long to stage the scales: two launches below.
+        // Only where the separate GEMM would not split its K loop either: the one kernel
+        // promotes every K block in order, and C must equal that of the separate calls.
+        if (fp8bs::plan_gemm_swapab(MT, false, g.M, g.N, g.K, sms) == 1 &&
+            fp8bs::plan_gemm_swapab(MT, true, g.M, g.N, g.K, sms) == 1) {
+            CUtensorMap tmA, tmB;
+            if (!make_map(&tmB, b, N, K, 128) || !make_map_bf16(&tmA, x, M, K, MT))
+                return FP8BS_ERR_CUDA;
+            return status_of(fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, fq, 1, st));
+        }
+        // K too long to stage the scales, or a split K loop: two launches below.
     }
     // Two launches: act_quant, then the GEMM on its output.
     if (int st2 = status_of(fp8bs::launch_act_quant(x, y, s, M, K, ue8m0, sms, st))) return st2;
@@ -369,6 +504,26 @@ int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b, const flo
     if (e == cudaErrorInvalidValue) return FP8BS_ERR_UNSUPPORTED_DEVICE;
     if (e != cudaSuccess) return FP8BS_ERR_CUDA;
     return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, ws, bytes, stream);
+}
+
+int fp8bs_gemm_plan(int64_t M, int64_t N, int64_t K, int scale_fmt, int with_workspace,
+                    int* kernel, int* tile, int* ksplit, int* stream_k) {
+    if (!kernel || !tile || !ksplit || !stream_k) return FP8BS_ERR_INVALID_ARG;
+    if (M <= 0 || N <= 0 || K <= 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return FP8BS_ERR_INVALID_ARG;
+    if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
+        return FP8BS_ERR_INVALID_ARG;
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    // Any non-null pointer stands for a workspace here: the plan only asks whether one is given.
+    static char marker;
+    const GemmPlan p = plan_gemm(M, N, K, scale_fmt == FP8BS_SCALE_UE8M0,
+                                 with_workspace ? &marker : nullptr, sms);
+    *kernel = p.kind;
+    *tile = p.tile;
+    *ksplit = p.ksplit;
+    *stream_k = p.ska.workspace != nullptr ? 1 : 0;
+    return FP8BS_OK;
 }
 
 int fp8bs_gemm_workspace_size(size_t* bytes) {

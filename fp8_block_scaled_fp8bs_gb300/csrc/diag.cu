@@ -30,6 +30,7 @@ cudaError_t read_device_error(unsigned int* out, bool clear, cudaStream_t stream
     if (e == cudaSuccess) e = read_error_bs(&words[2], clear, stream);
     if (e == cudaSuccess) e = read_error_swapab(&words[3], clear, stream);
     if (e == cudaSuccess) e = read_error_linear(&words[4], clear, stream);
+    if (e == cudaSuccess && clear) e = reset_static_workspace_counters(stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     *out = words[0] | words[1] | words[2] | words[3] | words[4];
     return e;

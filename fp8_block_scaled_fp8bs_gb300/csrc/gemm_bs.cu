@@ -53,7 +53,7 @@ namespace {
 
 template <int BN>
 struct BsCfg {
-    static_assert(BN == 64 || BN == 128 || BN == 256, "tile width");
+    static_assert(BN == 64 || BN == 128 || BN == 192 || BN == 256, "tile width");
     static constexpr int SF_WARPS = 4;
     static constexpr int EPI_WARPS = 4;
     // MMA issuers: two at BN = 64, taking a tile's K blocks in turn into accumulators of their
@@ -63,13 +63,13 @@ struct BsCfg {
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
     // Scale-factor columns per stage: A in 0..3, then B: 4 columns (one 128-row block of B
-    // per tile, BN <= 128) or 8 (BN = 256: columns 4..7 for the tile's first block, 8..11 for
-    // its second).
+    // per tile, BN <= 128) or 8 (BN = 192 or 256: the tile spans two blocks of B; column c of
+    // the slot covers tile rows 32c .. 32c+31).
     static constexpr int SF_B_COLS = BN > 128 ? 8 : 4;
     static constexpr int SF_COLS = 4 + SF_B_COLS;
     // Accumulators: two BN-column buffers (the epilogue of one tile overlaps the next), or at
     // BN = 256 one (two would fill TMEM and leave no room for scale factors).
-    static constexpr int NBUF = BN > 128 ? 1 : 2;
+    static constexpr int NBUF = BN > 192 ? 1 : 2;
     static constexpr int ACC = ISSUERS * BN;          // TMEM columns of one buffer
     static constexpr int SF_COL0 = NBUF * ACC;
     static constexpr int PART = BM * BN * 4;          // one fp32 partial tile (stream-K)
@@ -152,6 +152,8 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
 
     Sched sched = sched_begin(sk, num_tiles, num_kb);
     int tile, kb0, kb1;
+    const bool split = sk.ksplit > 1;
+    bool exchanged = false;      // split K: this thread has been through the exchange
 
     if (warp == PRODUCER) {
         if (lane == 0) {
@@ -250,8 +252,11 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             const float* as_row = g.a_s + static_cast<int64_t>(row) * num_kb;
             const float* bs_row =
                 g.b_s + (static_cast<int64_t>(t.g) * nb_count + t.n0 / 128) * num_kb;
-            // BN = 256: the tile's second 128-row block of B (the first again past N)
+            // BN = 192 or 256: the tile's second 128-row block of B (the first again past N)
             const float* bs_row2 = BN > 128 && t.n0 / 128 + 1 < nb_count ? bs_row + num_kb : bs_row;
+            // A 192-wide tile starting at an odd multiple of 64 meets its second block of B at
+            // tile row 64 (column 2 of the slot), otherwise at row 128 (column 4).
+            const bool b_shift = BN > 128 && (t.n0 & 127) != 0;
             float va[P], vb[P], vb2[P];
 #pragma unroll
             for (int i = 0; i < P; ++i) {
@@ -284,8 +289,13 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     const uint32_t taddr = tmem_base + lane_base +
                                            static_cast<uint32_t>(Cfg::SF_COL0 + stage * Cfg::SF_COLS);
                     tmem_st_4cols(taddr, wa, wa, wa, wa);
-                    tmem_st_4cols(taddr + 4, wb, wb, wb, wb);
-                    if constexpr (BN > 128) tmem_st_4cols(taddr + 8, wb2, wb2, wb2, wb2);
+                    if constexpr (BN > 128) {
+                        const uint32_t wx = b_shift ? wb2 : wb;
+                        tmem_st_4cols(taddr + 4, wb, wb, wx, wx);
+                        tmem_st_4cols(taddr + 8, wb2, wb2, wb2, wb2);
+                    } else {
+                        tmem_st_4cols(taddr + 4, wb, wb, wb, wb);
+                    }
                     tmem_wait_st();
                     tc_fence_before();
                     __syncwarp();
@@ -308,7 +318,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
         bool ok = true;
         while (ok && sched_next(sched, num_kb, tile, kb0, kb1)) {
             const TileCoord t = decode_tile<BN>(gt, tile, n_tiles);
-            const bool owner = kb0 == 0 && kb1 < num_kb;
+            const bool owner = !split && kb0 == 0 && kb1 < num_kb;
             int parts = 0;
             bool got = true;
             if (owner) {
@@ -347,6 +357,39 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                                    static_cast<uint32_t>(buf * Cfg::ACC);
             // the second issuer's accumulator (BN columns on) holds K blocks kb0 + 1, kb0 + 3..
             const bool two = Cfg::ISSUERS > 1 && kb1 - kb0 > 1;
+            if (split) {
+                // Split K: once every CTA of the cluster is past its K loop (its stage memory
+                // free), send each slice of the accumulator to the CTA that adds that slice up;
+                // then add up this CTA's slice and store it.
+                const SplitTile sp = split_tile(BN, sk.ksplit, smem);
+                cluster_sync();
+                tc_fence_after();
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    float v[32];
+                    tmem_ld_32cols(taddr + 32 * c, v);
+                    tmem_wait_ld_32(v);
+                    if constexpr (Cfg::ISSUERS > 1) {
+                        if (two) {
+                            float u[32];
+                            tmem_ld_32cols(taddr + BN + 32 * c, u);
+                            tmem_wait_ld_32(u);
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += u[i];
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        split_push4(sp, row_in_tile, 32 * c + 4 * j,
+                                    make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+                }
+                release_tmem(&ring.tempty[buf], lane);
+                cluster_sync();
+                split_reduce_store<128>(sp, reinterpret_cast<const float4*>(smem), epi_thread, BN,
+                                        t, g);
+                exchanged = true;
+                break;
+            }
             const int row = t.m0 + row_in_tile;
             const bool store = row < t.row_end;
             __nv_bfloat16* crow =
@@ -475,10 +518,34 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
         }
     }
 
+    // Split K: every thread takes part in the exchange's two cluster barriers (the epilogue
+    // warps above, unless a wait ran out before them).
+    if (split && !exchanged) {
+        cluster_sync();
+        cluster_sync();
+    }
+
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == ISSUER) tmem_dealloc(tmem_base, tmem_cols);
+}
+
+// Stages and dynamic shared memory: with a stream-K workspace one partial tile (and its
+// barrier) is kept in shared memory, at two stages' cost.
+template <int BN>
+constexpr int bs_stages(bool stream_k) {
+    return (kSmemLimit - 1024 - ring_bytes(kMaxStages) -
+            (stream_k ? BsCfg<BN>::PART + 16 : 0)) / BsCfg<BN>::STAGE > kMaxStages
+               ? kMaxStages
+               : (kSmemLimit - 1024 - ring_bytes(kMaxStages) -
+                  (stream_k ? BsCfg<BN>::PART + 16 : 0)) / BsCfg<BN>::STAGE;
+}
+
+template <int BN>
+constexpr int bs_smem(bool stream_k) {
+    return 1024 + bs_stages<BN>(stream_k) * BsCfg<BN>::STAGE +
+           (stream_k ? BsCfg<BN>::PART + 16 : 0) + ring_bytes(bs_stages<BN>(stream_k));
 }
 
 template <int BN>
@@ -486,37 +553,49 @@ cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
                       const GroupTable& gt, int num_sms, const StreamKArgs& ska,
                       cudaStream_t stream) {
     using Cfg = BsCfg<BN>;
-    // A 256-wide partial tile would not fit in shared memory: that width runs whole tiles.
+    // A partial tile wider than 128 would not fit in shared memory: those widths run whole
+    // tiles or split K in a cluster.
     if (BN > 128 && ska.workspace) return cudaErrorInvalidValue;
-    int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
     static_assert(bs_tmem_cols<BN>(kMaxStages) <= 512, "TMEM holds 512 columns");
-    // Stream-K keeps one partial tile (and its barrier) in shared memory, at two stages' cost.
-    const int part_bytes = ska.workspace ? Cfg::PART + 16 : 0;
-    if (ska.workspace)
-        stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages) - part_bytes) / Cfg::STAGE;
-    if (stages > kMaxStages) stages = kMaxStages;
-    const int smem = 1024 + stages * Cfg::STAGE + part_bytes + ring_bytes(stages);
+    const bool stream_k = ska.workspace != nullptr && ska.ksplit <= 1;
+    const int stages = bs_stages<BN>(stream_k);
+    const int smem = bs_smem<BN>(stream_k);
+    if (ska.ksplit > 1 && split_recv_bytes(BN, ska.ksplit) > stages * Cfg::STAGE)
+        return cudaErrorInvalidValue;
     cudaError_t e = set_smem(gemm_bs_kernel<BN>, kSmemLimit);
     if (e != cudaSuccess) return e;
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
-    StreamK sk = {nullptr, nullptr, 0};
+    StreamK sk = {nullptr, nullptr, 0, 1};
     const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
-    return launch_pdl(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, tmA, tmB, g, gt,
-                      stages, sk);
+    return launch_pdl_cluster(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
+                              tmA, tmB, g, gt, stages, sk);
+}
+
+template <int BN>
+int split_clusters_bs(int S) {
+    using Cfg = BsCfg<BN>;
+    if (split_recv_bytes(BN, S) > bs_stages<BN>(false) * Cfg::STAGE) return 0;
+    if (set_smem(gemm_bs_kernel<BN>, kSmemLimit) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return max_active_clusters(reinterpret_cast<const void*>(gemm_bs_kernel<BN>), Cfg::THREADS,
+                               bs_smem<BN>(false), S);
 }
 
 }  // namespace
 
 // Tile width by rounds of tiles over the SMs times the measured time of one K block at that
-// width (~886 clk at 256, ~660 at 128 and about the same at 64, at prefill shapes): 256-wide
-// tiles carry a third fewer operand bytes per MAC but leave more SMs idle when tiles are few.
+// width (~886 clk at 256, ~660 at 128 and about the same at 64, at prefill shapes; 192 taken
+// between them): wider tiles carry fewer operand bytes per MAC but leave more SMs idle when
+// tiles are few.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
-    static const int kWidth[3] = {256, 64, 128};     // on a tie the narrower of 64 and 128
-    static const int kCost[3] = {134, 100, 100};
+    static const int kWidth[4] = {256, 192, 64, 128};   // on a tie the narrower of 64 and 128
+    static const int kCost[4] = {134, 117, 100, 100};
     int best = 128;
     int64_t best_cost = INT64_MAX;
-    for (int i = 0; i < 3; ++i) {
+    for (int i = 0; i < 4; ++i) {
         const int64_t tiles = m_tiles_total * ((N + kWidth[i] - 1) / kWidth[i]);
         const int64_t cost = (tiles + num_sms - 1) / num_sms * kCost[i];
         if (cost < best_cost) {
@@ -533,36 +612,61 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     switch (BN) {
         case 64: return launch_bs<64>(tmA, tmB, g, gt, num_sms, ska, stream);
         case 128: return launch_bs<128>(tmA, tmB, g, gt, num_sms, ska, stream);
+        case 192: return launch_bs<192>(tmA, tmB, g, gt, num_sms, ska, stream);
         case 256: return launch_bs<256>(tmA, tmB, g, gt, num_sms, ska, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
+int max_split_clusters_bs(int BN, int S) {
+    switch (BN) {
+        case 64: return split_clusters_bs<64>(S);
+        case 128: return split_clusters_bs<128>(S);
+        case 192: return split_clusters_bs<192>(S);
+        case 256: return split_clusters_bs<256>(S);
+        default: return 0;
+    }
+}
+
 // A stream-K workspace that needs no allocation: a file-scope device array, zero at module
 // load (every call that completes leaves its counters at zero again), big enough for devices
-// with up to kStaticWsSms SMs. Its address is looked up once per device.
+// with up to kStaticWsSms SMs. Its address is looked up once per device, on the first call made
+// with that device current, and kept for the life of the process.
 constexpr int kStaticWsSms = 160;
 constexpr size_t kStaticWsBytes = stream_k_workspace(kStaticWsSms);
 static __device__ __align__(256) unsigned char g_static_ws[kStaticWsBytes];
+constexpr int kMaxDevices = 64;
+static std::atomic<void*> g_static_ws_addr[kMaxDevices];
 
 cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes) {
-    constexpr int kMaxDevices = 64;
-    static std::atomic<void*> addr[kMaxDevices];
     if (num_sms > kStaticWsSms || stream_k_workspace(num_sms) > kStaticWsBytes)
         return cudaErrorInvalidValue;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    void* p = addr[dev].load(std::memory_order_acquire);
+    void* p = g_static_ws_addr[dev].load(std::memory_order_acquire);
     if (!p) {
         e = cudaGetSymbolAddress(&p, g_static_ws);
         if (e != cudaSuccess) return e;
-        addr[dev].store(p, std::memory_order_release);
+        g_static_ws_addr[dev].store(p, std::memory_order_release);
     }
     *ws = p;
     *bytes = kStaticWsBytes;
     return cudaSuccess;
+}
+
+// Zero the counters of the static workspace on the current device, if a call has used it: a
+// call abandoned after a device wait error may have left a counter that no later call would
+// bring back to zero. Enqueued on `stream`; nothing to do before the first use.
+cudaError_t reset_static_workspace_counters(cudaStream_t stream) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaSuccess;
+    void* p = g_static_ws_addr[dev].load(std::memory_order_acquire);
+    if (!p) return cudaSuccess;
+    return cudaMemsetAsync(p, 0, stream_k_flag_bytes(kStaticWsSms), stream);
 }
 
 cudaError_t read_error_bs(unsigned int* out, bool clear, cudaStream_t stream) {

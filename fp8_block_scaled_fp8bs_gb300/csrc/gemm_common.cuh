@@ -194,13 +194,96 @@ struct StreamK {
     int* flags;       // [gridDim.x] partials published for the tile each CTA owns
     float4* parts;    // [gridDim.x][BN/4][128]: a CTA's partial, float4 of columns x rows
     int dp_tiles;     // tiles computed whole before the shared ones (a multiple of gridDim.x)
+    int ksplit;       // > 1: split K inside a cluster (no workspace; see split_k_range)
 };
 
 struct Sched {
     int tile;           // next data-parallel tile
     int dp_tiles;
     int u, u_end;       // shared units (fewer than 2^31): cursor and end of this CTA's range
+    int kb_lo, kb_hi;   // K blocks of a data-parallel tile (all of them unless split)
 };
+
+// ------------------------------------------------------------------ split K inside a cluster
+//
+// With StreamK::ksplit = S > 1 the grid holds S CTAs per output tile, launched as clusters of S
+// consecutive CTAs: CTA r of cluster t computes K blocks [r*num_kb/S, (r+1)*num_kb/S) of tile
+// t into fp32. The S partials are then added through distributed shared memory -- the columns
+// of the tile are cut into S slices of W (a multiple of 8) and CTA q adds slice q of every
+// partial in rank order, i.e. in K order -- and stored as bf16. No workspace, no flags, no
+// waiting on other CTAs beyond two cluster barriers, and a fixed order of additions.
+__device__ __forceinline__ void split_k_range(int num_kb, int S, int& tile, int& kb0, int& kb1) {
+    tile = blockIdx.x / S;
+    const int r = blockIdx.x - tile * S;
+    kb0 = r * num_kb / S;
+    kb1 = (r + 1) * num_kb / S;
+}
+
+__host__ __device__ constexpr int split_slice(int bn, int S) { return ((bn + S - 1) / S + 7) / 8 * 8; }
+
+// Bytes of the receive area of a split tile: S slots of W columns x 128 rows of fp32.
+__host__ __device__ constexpr int split_recv_bytes(int bn, int S) {
+    return S * split_slice(bn, S) * BM * 4;
+}
+
+struct SplitTile {
+    int S, rank, W;
+    uint32_t recv;   // shared-window address of the receive area (the same in every CTA)
+};
+
+__device__ __forceinline__ SplitTile split_tile(int bn, int S, const void* recv) {
+    SplitTile sp;
+    sp.S = S;
+    sp.rank = static_cast<int>(cluster_ctarank());
+    sp.W = split_slice(bn, S);
+    sp.recv = smem_addr(recv);
+    return sp;
+}
+
+// Send columns col .. col+3 (col % 4 == 0) of row `row` of this CTA's partial to the CTA that
+// adds up their slice: slot `rank` of its receive area, stored as float4 [W/4][128] per slot.
+__device__ __forceinline__ void split_push4(const SplitTile& sp, int row, int col, float4 v) {
+    const int q = col / sp.W;
+    const uint32_t off =
+        static_cast<uint32_t>(((sp.rank * sp.W + col - q * sp.W) / 4 * BM + row) * 16);
+    st_shared_cluster_f4(mapa_shared(sp.recv + off, static_cast<uint32_t>(q)), v);
+}
+
+// This CTA's slice of the tile: the S partials added in rank order, rounded to bf16 and stored
+// (rows past row_end and columns past N are skipped). `tid` counts the calling threads.
+template <int THREADS>
+__device__ __forceinline__ void split_reduce_store(const SplitTile& sp, const float4* recv,
+                                                   int tid, int bn, const TileCoord& t,
+                                                   const GemmArgs& g) {
+    const int c_lo = sp.rank * sp.W;
+    const int c_hi = min(bn, c_lo + sp.W);
+    const int items = c_hi > c_lo ? (c_hi - c_lo) / 8 * BM : 0;
+    const bool vec = (g.N & 7) == 0;
+    for (int i = tid; i < items; i += THREADS) {
+        const int row = i % BM;
+        const int grp = i / BM;
+        float v[8];
+        for (int r = 0; r < sp.S; ++r) {
+            const float4* slot = recv + (r * sp.W / 4 + 2 * grp) * BM + row;
+            const float4 p0 = slot[0];
+            const float4 p1 = slot[BM];
+            if (r == 0) {
+                v[0] = p0.x; v[1] = p0.y; v[2] = p0.z; v[3] = p0.w;
+                v[4] = p1.x; v[5] = p1.y; v[6] = p1.z; v[7] = p1.w;
+            } else {
+                v[0] += p0.x; v[1] += p0.y; v[2] += p0.z; v[3] += p0.w;
+                v[4] += p1.x; v[5] += p1.y; v[6] += p1.z; v[7] += p1.w;
+            }
+        }
+        const int grow = t.m0 + row;
+        const int col = t.n0 + c_lo + 8 * grp;
+        if (grow < t.row_end && col < g.N) {
+            __nv_bfloat16* crow =
+                static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(grow) * g.N + col;
+            store_row_bf16<8>(crow, v, g.N - col, vec);
+        }
+    }
+}
 
 // Start of CTA `cta`'s range of the `units` shared units.
 __device__ __forceinline__ int64_t sk_range_start(int cta, int64_t units) {
@@ -223,14 +306,20 @@ __device__ __forceinline__ Sched sched_begin(const StreamK& sk, int num_tiles, i
     const int64_t units = sk_units(sk, num_tiles, num_kb);
     s.u = sk.parts ? static_cast<int>(sk_range_start(blockIdx.x, units)) : 0;
     s.u_end = sk.parts ? static_cast<int>(sk_range_start(blockIdx.x + 1, units)) : 0;
+    s.kb_lo = 0;
+    s.kb_hi = num_kb;
+    if (sk.ksplit > 1) {            // one piece: this CTA's K range of its cluster's tile
+        split_k_range(num_kb, sk.ksplit, s.tile, s.kb_lo, s.kb_hi);
+        s.dp_tiles = s.tile + 1;
+    }
     return s;
 }
 
 __device__ __forceinline__ bool sched_next(Sched& s, int num_kb, int& tile, int& kb0, int& kb1) {
     if (s.tile < s.dp_tiles) {
         tile = s.tile;
-        kb0 = 0;
-        kb1 = num_kb;
+        kb0 = s.kb_lo;
+        kb1 = s.kb_hi;
         s.tile += gridDim.x;
         return true;
     }
@@ -247,6 +336,11 @@ __device__ __forceinline__ bool sched_next(Sched& s, int num_kb, int& tile, int&
 // Piece p of this CTA's sequence (the same sequence as sched_next), computed from p alone.
 __device__ __forceinline__ bool piece_at(const StreamK& sk, int p, int num_tiles, int num_kb,
                                          int& tile, int& kb0, int& kb1) {
+    if (sk.ksplit > 1) {
+        if (p > 0) return false;
+        split_k_range(num_kb, sk.ksplit, tile, kb0, kb1);
+        return true;
+    }
     const int dp_tiles = sk.parts ? sk.dp_tiles : num_tiles;
     const int n_dp = blockIdx.x < dp_tiles ? (dp_tiles - blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
     if (p < n_dp) {
@@ -317,9 +411,15 @@ __device__ __forceinline__ void epilogue_bar() {
     asm volatile("bar.sync 1, %0;" ::"n"(threads) : "memory");
 }
 
-// Host: grid size and kernel parameter for a stream-K plan (see StreamKArgs in kernels.h).
+// Host: grid size and kernel parameter for a stream-K or split-K plan (see StreamKArgs in
+// kernels.h).
 inline int stream_k_grid(const StreamKArgs& ska, int tiles, int num_kb, int num_sms,
                          StreamK* sk) {
+    sk->ksplit = 1;
+    if (ska.ksplit > 1) {
+        sk->ksplit = ska.ksplit;
+        return tiles * ska.ksplit;
+    }
     if (!ska.workspace) return tiles < num_sms ? tiles : num_sms;
     const int64_t units = static_cast<int64_t>(tiles - ska.dp_tiles) * num_kb;
     const int grid = ska.dp_tiles > 0 || units >= num_sms ? num_sms : static_cast<int>(units);

@@ -4,6 +4,12 @@
 // weight slab. The promotion warps fold each K block's TMEM partial into fp32 registers with
 // the combined scale a_s[m, kb] * b_s[slab, kb], as in gemm_tn.cu.
 //
+// Split K (quantised input only): when the slabs alone would leave most SMs idle (N = 2048 or
+// 576 at decode: 16 or 5 slabs on 152 SMs), S CTAs, launched as one thread-block cluster, share
+// each slab: CTA r streams K blocks [r*num_kb/S, (r+1)*num_kb/S) of it, and the S partial sums
+// of the C rows are added in rank order (K order) through distributed shared memory before the
+// bf16 store -- no workspace and no flags, and the additions happen in a fixed order.
+//
 // Two ways in for the activations:
 //   quantised (fp8bs_gemm): TMA brings e4m3 rows of A; their scales are staged in shared memory
 //       transposed to [kb][m] before the main loop.
@@ -34,13 +40,12 @@ struct SwapCfg {
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * MT);
 };
 
-// Shared-memory bytes after the stages: transposed scales [num_kb][MT], then (quantised input)
-// the raw a_s rows [MT][num_kb] or (FUSED) a ready count per K block, the b_s row, and (FUSED)
-// one "quantised" barrier per stage.
+// Shared-memory bytes after the stages, for a CTA that takes nkb K blocks: transposed scales
+// [nkb][MT], then (quantised input) the raw a_s rows [MT][nkb] or (FUSED) a ready count per K
+// block, the b_s row, and (FUSED) one "quantised" barrier per stage.
 template <int MT, bool FUSED>
-__host__ __device__ constexpr int swap_scale_bytes(int num_kb) {
-    return num_kb * MT * 4 + (FUSED ? num_kb * 4 : num_kb * MT * 4) + ((num_kb + 3) & ~3) * 4 +
-           16;
+__host__ __device__ constexpr int swap_scale_bytes(int nkb) {
+    return nkb * MT * 4 + (FUSED ? nkb * 4 : nkb * MT * 4) + ((nkb + 3) & ~3) * 4 + 16;
 }
 
 // Bounded spin until *p == target (a shared-memory count written by other warps).
@@ -63,11 +68,17 @@ __device__ __forceinline__ bool spin_until_at_least(const int* p, int target) {
     return true;
 }
 
+// Receive area of the split-K exchange (at the start of the stage memory, free once every CTA
+// of the cluster has finished its K loop): S slots of `wm` rows of C x 128 columns, fp32.
+__host__ __device__ constexpr int swap_recv_bytes(int MT, int S) {
+    return S * ((MT + S - 1) / S) * BM * 4;
+}
+
 template <int MT, bool FUSED>
 __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const GemmArgs g,
-                       const int stages, const FusedQuant fq) {
+                       const int stages, const FusedQuant fq, const int ksplit) {
     using Cfg = SwapCfg<MT, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -75,31 +86,36 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     uint8_t* sX = smem + stages * A_TILE;                 // [stages][MT x 128] e4m3 activations
     uint8_t* sXb = sX + stages * Cfg::X_TILE;             // [stages][MT x 128] bf16 (FUSED)
     const int num_kb = g.K / BK;
-    float* sAs = reinterpret_cast<float*>(sXb + stages * Cfg::XB_TILE);  // [num_kb][MT]
-    float* sRaw = sAs + num_kb * MT;   // a_s rows m0 .. m0+MT-1 as stored: [MT][num_kb]
+    // This CTA's slab and K blocks kb_lo .. kb_lo + nkb - 1 (all of them unless split).
+    const int S = FUSED ? 1 : ksplit;
+    const int slab = blockIdx.x / S;
+    const int kb_lo = (blockIdx.x - slab * S) * num_kb / S;
+    const int nkb = (blockIdx.x - slab * S + 1) * num_kb / S - kb_lo;
+    float* sAs = reinterpret_cast<float*>(sXb + stages * Cfg::XB_TILE);  // [nkb][MT]
+    float* sRaw = sAs + nkb * MT;      // a_s rows m0 .. m0+MT-1, this CTA's K blocks: [MT][nkb]
     int* sReady = reinterpret_cast<int*>(sRaw);          // FUSED: [num_kb] quantiser warps done
-    float* sBs = sRaw + (FUSED ? num_kb : num_kb * MT);  // b_s row of this slab: [num_kb]
-    uint8_t* ring_mem = reinterpret_cast<uint8_t*>(sBs + ((num_kb + 3) & ~3));
+    float* sBs = sRaw + (FUSED ? nkb : nkb * MT);        // b_s row of this slab: [nkb]
+    uint8_t* ring_mem = reinterpret_cast<uint8_t*>(sBs + ((nkb + 3) & ~3));
     const Ring ring = carve_ring(ring_mem, stages);
     uint64_t* qfull = reinterpret_cast<uint64_t*>(ring_mem + ring_bytes(stages));  // FUSED
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int n0 = blockIdx.x * BM;
+    const int n0 = slab * BM;
     const int m0 = blockIdx.y * MT;
 
     // Prologue order: barriers; (weights declared constant: the whole weight ring, before
     // waiting for earlier kernels); wait; scales; TMEM; block sync; activations (and weights).
     const uint64_t keep = l2_policy_evict_last();    // activations: reused by every CTA
     const uint64_t stream = l2_policy_evict_first(); // weights: read once
-    const int prefill = min(stages, num_kb);
+    const int prefill = min(stages, nkb);
     // The scales (a few hundred bytes: rows a_s[m0 .. m0+rows) and the slab's b_s row, both
     // contiguous) are requested by the promotion threads before the block synchronises, and the
     // weight stream only starts after it: the scales then return at unloaded latency instead of
     // queueing behind megabytes of weights.
     const int scale_rows = min(MT, g.M - m0);
     const float* as_rows = g.a_s + static_cast<int64_t>(m0) * num_kb;
-    const float* bs_row = g.b_s + static_cast<int64_t>(blockIdx.x) * num_kb;
+    const float* bs_row = g.b_s + static_cast<int64_t>(slab) * num_kb + kb_lo;
     // Quantised input: the scale warp counts here the K blocks of sAs it has filled.
     int* sScaleDone = reinterpret_cast<int*>(ring.tmem_holder + 1);
     if (threadIdx.x == 0) {
@@ -114,9 +130,10 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         // Weights the caller declared constant need not wait for the kernels before this one:
         // the ring starts filling while they finish.
         if (g.weights_constant) {
-            for (int kb = 0; kb < prefill; ++kb) {
-                mbar_arrive_expect_tx(&ring.full[kb], Cfg::TX_BYTES);
-                tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
+            for (int i = 0; i < prefill; ++i) {
+                mbar_arrive_expect_tx(&ring.full[i], Cfg::TX_BYTES);
+                tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], (kb_lo + i) * BK, n0,
+                                 stream);
             }
         }
     }
@@ -131,15 +148,23 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         cp_async_commit();
     }
     if (!FUSED && warp == Cfg::Q_WARP0) {
-        // The rows are one contiguous run of scale_rows * num_kb floats: 16-byte copies when
-        // its start and length allow (sRaw is 16-byte aligned), else 4-byte ones.
-        const int count = scale_rows * num_kb;
-        if ((reinterpret_cast<uintptr_t>(as_rows) & 15) == 0 && (count & 3) == 0) {
-            for (int i = 4 * lane; i < count; i += 4 * 32) cp_async_16(sRaw + i, as_rows + i);
+        if (S == 1) {
+            // The rows are one contiguous run of scale_rows * num_kb floats: 16-byte copies
+            // when its start and length allow (sRaw is 16-byte aligned), else 4-byte ones.
+            const int count = scale_rows * num_kb;
+            if ((reinterpret_cast<uintptr_t>(as_rows) & 15) == 0 && (count & 3) == 0) {
+                for (int i = 4 * lane; i < count; i += 4 * 32) cp_async_16(sRaw + i, as_rows + i);
+            } else {
+                for (int i = lane; i < count; i += 32) cp_async_4(sRaw + i, as_rows + i);
+            }
         } else {
-            for (int i = lane; i < count; i += 32) cp_async_4(sRaw + i, as_rows + i);
+            // This CTA's K blocks of each row.
+            for (int i = lane; i < scale_rows * nkb; i += 32) {
+                const int j = i / nkb;
+                cp_async_4(sRaw + i, as_rows + static_cast<int64_t>(j) * num_kb + kb_lo + i - j * nkb);
+            }
         }
-        for (int i = lane; i < num_kb; i += 32) cp_async_4(sBs + i, bs_row + i);
+        for (int i = lane; i < nkb; i += 32) cp_async_4(sBs + i, bs_row + i);
         cp_async_commit();
     }
     if (warp == 1) tmem_alloc(ring.tmem_holder, Cfg::TMEM_COLS);
@@ -152,12 +177,13 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     constexpr int ACT_TILE = FUSED ? Cfg::XB_TILE : Cfg::X_TILE;
     if (threadIdx.x == 0) {
         // fill the whole ring at once
-        for (int kb = 0; kb < prefill; ++kb) {
+        for (int i = 0; i < prefill; ++i) {
+            const int kb = kb_lo + i;
             if (!g.weights_constant) {
-                mbar_arrive_expect_tx(&ring.full[kb], Cfg::TX_BYTES);
-                tma_load_2d_hint(sW + kb * A_TILE, &tmB, &ring.full[kb], kb * BK, n0, stream);
+                mbar_arrive_expect_tx(&ring.full[i], Cfg::TX_BYTES);
+                tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], kb * BK, n0, stream);
             }
-            tma_load_2d_hint(sAct + kb * ACT_TILE, &tmA, &ring.full[kb], kb * BK, m0, keep);
+            tma_load_2d_hint(sAct + i * ACT_TILE, &tmA, &ring.full[i], kb * BK, m0, keep);
         }
     }
 
@@ -167,7 +193,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             uint32_t phase = prefill == stages ? 1u : 0u;
             int64_t issued = prefill;
             bool ok = true;
-            for (int kb = prefill; kb < num_kb; ++kb) {
+            for (int kb = kb_lo + prefill; kb < kb_lo + nkb; ++kb) {
                 if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
                     record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                     ok = false;
@@ -190,7 +216,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, MT);
             int stage = 0, buf = 0;
             uint32_t phase = 0, tphase = 0;
-            for (int kb = 0; kb < num_kb; ++kb) {
+            for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
                     !mbar_wait(&ring.full[stage], phase) ||
                     (FUSED && !mbar_wait(&qfull[stage], phase))) {
@@ -224,11 +250,11 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         // wait for the whole table.
         cp_async_wait_all();
         __syncwarp();
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
             const float sb = sBs[kb];
 #pragma unroll
             for (int j = lane; j < MT; j += 32)
-                sAs[kb * MT + j] = j < scale_rows ? sRaw[j * num_kb + kb] * sb : 0.0f;
+                sAs[kb * MT + j] = j < scale_rows ? sRaw[j * nkb + kb] * sb : 0.0f;
             __syncwarp();
             if (lane == 0) {
                 __threadfence_block();
@@ -322,7 +348,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         int buf = 0;
         uint32_t tphase = 0;
         bool ok = true;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < nkb; ++kb) {
             if (!warp_wait(&ring.tfull[buf], tphase)) {
                 if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
                 ok = false;
@@ -403,12 +429,55 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             buf ^= 1;
             if (buf == 0) tphase ^= 1;
         }
-        if (ok && n < g.N) {
-            __nv_bfloat16* c = static_cast<__nv_bfloat16*>(g.c);
+        if (S == 1) {
+            if (ok && n < g.N) {
+                __nv_bfloat16* c = static_cast<__nv_bfloat16*>(g.c);
 #pragma unroll
-            for (int j = 0; j < MT; ++j)
-                if (m0 + j < g.M) c[static_cast<int64_t>(m0 + j) * g.N + n] = __float2bfloat16_rn(acc[j]);
+                for (int j = 0; j < MT; ++j)
+                    if (m0 + j < g.M)
+                        c[static_cast<int64_t>(m0 + j) * g.N + n] = __float2bfloat16_rn(acc[j]);
+            }
+        } else {
+            // Split K: row j of C (j < scale_rows) is added up by CTA j / wm of the cluster,
+            // which receives this CTA's partial of it in slot `rank` of its receive area
+            // ([slot][wm][128] fp32 at the start of the stage memory).
+            const int t = quarter * 32 + lane;
+            const int wm = (scale_rows + S - 1) / S;
+            const int rank = static_cast<int>(cluster_ctarank());
+            const uint32_t recv = smem_addr(smem);
+            cluster_sync();               // every CTA of the cluster is done with its stages
+            if (ok) {
+#pragma unroll
+                for (int j = 0; j < MT; ++j) {
+                    if (j < scale_rows) {
+                        const int q = j / wm;
+                        const uint32_t off =
+                            static_cast<uint32_t>(((rank * wm + j - q * wm) * BM + t) * 4);
+                        st_shared_cluster_f32(mapa_shared(recv + off, static_cast<uint32_t>(q)),
+                                              acc[j]);
+                    }
+                }
+            }
+            cluster_sync();               // every partial has landed
+            const float* rv = reinterpret_cast<const float*>(smem);
+            const int j_end = min(scale_rows, (rank + 1) * wm);
+            for (int j = rank * wm; ok && j < j_end; ++j) {
+                float v = 0.0f;
+                for (int r = 0; r < S; ++r) {
+                    const float p = rv[(r * wm + j - rank * wm) * BM + t];
+                    v = r == 0 ? p : v + p;
+                }
+                if (n < g.N)
+                    static_cast<__nv_bfloat16*>(g.c)[static_cast<int64_t>(m0 + j) * g.N + n] =
+                        __float2bfloat16_rn(v);
+            }
         }
+    }
+    // The other warps take part in the two cluster barriers of the split-K exchange.
+    const bool promotion_warp = warp >= 2 && warp < 2 + Cfg::EPI_WARPS;
+    if (S > 1 && !promotion_warp) {
+        cluster_sync();
+        cluster_sync();
     }
 
     tc_fence_before();
@@ -417,43 +486,106 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
 }
 
+// Stages and dynamic shared-memory bytes of a launch whose CTAs take nkb K blocks each.
 template <int MT, bool FUSED>
-cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const GemmArgs& g,
-                        const FusedQuant& fq, cudaStream_t stream) {
+bool swap_smem(int nkb, int* stages_out, int* smem_out) {
     using Cfg = SwapCfg<MT, FUSED>;
-    const int num_kb = g.K / BK;
-    const int scale_bytes = swap_scale_bytes<MT, FUSED>(num_kb);
+    const int scale_bytes = swap_scale_bytes<MT, FUSED>(nkb);
     const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages) + (FUSED ? 8 * kMaxStages : 0);
     int stages = (kSmemLimit - fixed) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2) return cudaErrorInvalidValue;   // K too large for the scale staging
-    const int smem = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages) +
-                     (FUSED ? 8 * stages : 0);
-    cudaError_t e = set_smem(gemm_swapab_kernel<MT, FUSED>, smem);
+    if (stages < 2) return false;   // K too large for the scale staging
+    *stages_out = stages;
+    *smem_out = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages) +
+                (FUSED ? 8 * stages : 0);
+    return true;
+}
+
+// Fewest K blocks per CTA worth a split of the K loop.
+constexpr int kMinSplitKb = 4;
+
+// CTAs per slab for this launch: the largest S (up to kMaxSplit) for which every CTA of the
+// grid is resident at once, as whole clusters, with at least kMinSplitKb K blocks each; 1 for
+// no split; 0 if the kernel cannot take this K (the activation scales do not fit).
+template <int MT, bool FUSED>
+int plan_swap(int M, int N, int K, int num_sms) {
+    using Cfg = SwapCfg<MT, FUSED>;
+    auto kernel = gemm_swapab_kernel<MT, FUSED>;
+    const int num_kb = K / BK;
+    const int slabs = (N + BM - 1) / BM;
+    const int m_tiles = (M + MT - 1) / MT;
+    if (set_smem(kernel, kSmemLimit) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    for (int c = FUSED ? 1 : kMaxSplit; c > 1; --c) {
+        int st = 0, sm = 0;
+        if (static_cast<int64_t>(slabs) * m_tiles * c > num_sms || num_kb / c < kMinSplitKb ||
+            !swap_smem<MT, FUSED>((num_kb + c - 1) / c, &st, &sm) ||
+            swap_recv_bytes(MT, c) > st * Cfg::STAGE)
+            continue;
+        if (max_active_clusters(reinterpret_cast<const void*>(kernel), Cfg::THREADS, sm, c) <
+            static_cast<int64_t>(slabs) * m_tiles)
+            continue;
+        return c;
+    }
+    int st = 0, sm = 0;
+    return swap_smem<MT, FUSED>(num_kb, &st, &sm) ? 1 : 0;
+}
+
+template <int MT, bool FUSED>
+cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const GemmArgs& g,
+                        const FusedQuant& fq, int S, cudaStream_t stream) {
+    using Cfg = SwapCfg<MT, FUSED>;
+    auto kernel = gemm_swapab_kernel<MT, FUSED>;
+    cudaError_t e = set_smem(kernel, kSmemLimit);
     if (e != cudaSuccess) return e;
-    const dim3 grid((g.N + BM - 1) / BM, (g.M + MT - 1) / MT);
-    return launch_pdl(gemm_swapab_kernel<MT, FUSED>, grid, Cfg::THREADS, smem, stream, tmB, tmA,
-                      g, stages, fq);
+    const int num_kb = g.K / BK;
+    int stages = 0, smem = 0;
+    if (S < 1 || (FUSED && S != 1) || !swap_smem<MT, FUSED>((num_kb + S - 1) / S, &stages, &smem))
+        return cudaErrorInvalidValue;
+    if (S > 1 && swap_recv_bytes(MT, S) > stages * Cfg::STAGE) return cudaErrorInvalidValue;
+    const dim3 grid(((g.N + BM - 1) / BM) * S, (g.M + MT - 1) / MT);
+    return launch_pdl_cluster(kernel, grid, Cfg::THREADS, smem, stream, S, tmB, tmA, g, stages,
+                              fq, S);
 }
 
 }  // namespace
 
+int plan_gemm_swapab(int MT, bool fused, int M, int N, int K, int num_sms) {
+    if (fused) {
+        switch (MT) {
+            case 16: return plan_swap<16, true>(M, N, K, num_sms);
+            case 32: return plan_swap<32, true>(M, N, K, num_sms);
+            case 64: return plan_swap<64, true>(M, N, K, num_sms);
+            default: return 0;
+        }
+    }
+    switch (MT) {
+        case 16: return plan_swap<16, false>(M, N, K, num_sms);
+        case 32: return plan_swap<32, false>(M, N, K, num_sms);
+        case 64: return plan_swap<64, false>(M, N, K, num_sms);
+        case 128: return plan_swap<128, false>(M, N, K, num_sms);
+        default: return 0;
+    }
+}
+
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
-                               const GemmArgs& g, int MT, const FusedQuant& fq,
+                               const GemmArgs& g, int MT, const FusedQuant& fq, int ksplit,
                                cudaStream_t stream) {
     if (fq.x) {
         switch (MT) {
-            case 16: return launch_swap<16, true>(tmB, tmA, g, fq, stream);
-            case 32: return launch_swap<32, true>(tmB, tmA, g, fq, stream);
-            case 64: return launch_swap<64, true>(tmB, tmA, g, fq, stream);
+            case 16: return launch_swap<16, true>(tmB, tmA, g, fq, ksplit, stream);
+            case 32: return launch_swap<32, true>(tmB, tmA, g, fq, ksplit, stream);
+            case 64: return launch_swap<64, true>(tmB, tmA, g, fq, ksplit, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (MT) {
-        case 16: return launch_swap<16, false>(tmB, tmA, g, fq, stream);
-        case 32: return launch_swap<32, false>(tmB, tmA, g, fq, stream);
-        case 64: return launch_swap<64, false>(tmB, tmA, g, fq, stream);
-        case 128: return launch_swap<128, false>(tmB, tmA, g, fq, stream);
+        case 16: return launch_swap<16, false>(tmB, tmA, g, fq, ksplit, stream);
+        case 32: return launch_swap<32, false>(tmB, tmA, g, fq, ksplit, stream);
+        case 64: return launch_swap<64, false>(tmB, tmA, g, fq, ksplit, stream);
+        case 128: return launch_swap<128, false>(tmB, tmA, g, fq, ksplit, stream);
         default: return cudaErrorInvalidValue;
     }
 }

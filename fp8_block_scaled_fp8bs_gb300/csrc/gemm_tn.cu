@@ -8,6 +8,11 @@
 //                     the block's scale a_s[m,kb] * b_s[n/128,kb]; after the last block, bf16
 //                     and store. The two buffers let the tensor cores compute block kb+1
 //                     while block kb is promoted.
+//
+// Split K (StreamK::ksplit = S > 1, when the tiles alone would leave most SMs idle, e.g. one
+// MoE expert's few hundred rows): S CTAs, one thread-block cluster per tile, each promote one
+// K range of the tile into registers, then add the S partials slice by slice through
+// distributed shared memory in rank order (gemm_common.cuh, split_reduce_store).
 #include "gemm_common.cuh"
 
 namespace fp8bs {
@@ -82,6 +87,7 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
 
     Sched sched = sched_begin(sk, num_tiles, num_kb);
     int tile, kb0, kb1;
+    bool exchanged = false;      // split K: this thread has been through the exchange
 
     if (warp >= Cfg::EPI_WARPS) {
         if constexpr (Cfg::SPLIT_REGS) regs_dec<Cfg::kCtlRegs>();
@@ -158,6 +164,7 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
         // Pieces are recomputed from their index (piece_at), so that only the index and the K
         // end stay live through the K loop: these warps are at their register limit.
         bool ok = true;
+        const bool split = sk.ksplit > 1;
         for (int p = 0; ok; ++p) {
             int tile, kb0, kb1;
             if (!piece_at(sk, p, num_tiles, num_kb, tile, kb0, kb1)) break;
@@ -177,7 +184,7 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
             float acc[Cfg::CW];
 #pragma unroll
             for (int i = 0; i < Cfg::CW; ++i) acc[i] = 0.0f;
-            if (kb0 == 0 && kb1 < num_kb) {
+            if (!split && kb0 == 0 && kb1 < num_kb) {
                 // This CTA owns a shared tile: the pieces after its own are computed first by
                 // the next CTAs (their ranges are at least a tile long, so they are done by
                 // now); start from the sum of their partials.
@@ -316,6 +323,23 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
                 if (buf == 0) tphase ^= 1;
             }
             if (!ok) break;
+            if (split) {
+                // Split K: once every CTA of the cluster is past its K loop (its stage memory
+                // free), send each slice of this partial to the CTA that adds it up; then add
+                // up this CTA's slice and store it.
+                const SplitTile sp = split_tile(BN, sk.ksplit, smem);
+                cluster_sync();
+#pragma unroll
+                for (int i = 0; i < Cfg::CW / 4; ++i)
+                    split_push4(sp, row_in_tile, col0 + 4 * i,
+                                make_float4(acc[4 * i], acc[4 * i + 1], acc[4 * i + 2],
+                                            acc[4 * i + 3]));
+                cluster_sync();
+                split_reduce_store<EPI_THREADS>(sp, reinterpret_cast<const float4*>(smem),
+                                                threadIdx.x, BN, t, g);
+                exchanged = true;
+                break;
+            }
             if (kb0 > 0) {
                 // A piece that does not start its tile: publish the partial in this CTA's slot
                 // and count it in the flag of the tile's owner.
@@ -356,6 +380,13 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
         }
     }
 
+    // Split K: every thread takes part in the exchange's two cluster barriers (the promotion
+    // warps above, unless a wait ran out before them).
+    if (sk.ksplit > 1 && !exchanged) {
+        cluster_sync();
+        cluster_sync();
+    }
+
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -363,21 +394,46 @@ __global__ void __launch_bounds__(TnCfg<BN>::THREADS, 1)
 }
 
 template <int BN>
+constexpr int tn_stages() {
+    return (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / TnCfg<BN>::STAGE > kMaxStages
+               ? kMaxStages
+               : (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / TnCfg<BN>::STAGE;
+}
+
+template <int BN>
+constexpr int tn_smem() {
+    return 1024 + tn_stages<BN>() * TnCfg<BN>::STAGE + ring_bytes(tn_stages<BN>());
+}
+
+template <int BN>
 cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
                       const GroupTable& gt, int num_sms, const StreamKArgs& ska,
                       cudaStream_t stream) {
     using Cfg = TnCfg<BN>;
-    int stages = (kSmemLimit - 1024 - ring_bytes(kMaxStages)) / Cfg::STAGE;
-    if (stages > kMaxStages) stages = kMaxStages;
-    const int smem = 1024 + stages * Cfg::STAGE + ring_bytes(stages);
+    constexpr int stages = tn_stages<BN>();
+    constexpr int smem = tn_smem<BN>();
+    if (ska.ksplit > 1 && split_recv_bytes(BN, ska.ksplit) > stages * Cfg::STAGE)
+        return cudaErrorInvalidValue;
     cudaError_t e = set_smem(gemm_tn_kernel<BN>, smem);
     if (e != cudaSuccess) return e;
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
-    StreamK sk = {nullptr, nullptr, 0};
+    StreamK sk = {nullptr, nullptr, 0, 1};
     const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
-    return launch_pdl(gemm_tn_kernel<BN>, grid, Cfg::THREADS, smem, stream, tmA, tmB, g, gt,
-                      stages, sk);
+    return launch_pdl_cluster(gemm_tn_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
+                              tmA, tmB, g, gt, stages, sk);
+}
+
+template <int BN>
+int split_clusters_tn(int S) {
+    using Cfg = TnCfg<BN>;
+    if (split_recv_bytes(BN, S) > tn_stages<BN>() * Cfg::STAGE) return 0;
+    if (set_smem(gemm_tn_kernel<BN>, tn_smem<BN>()) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return max_active_clusters(reinterpret_cast<const void*>(gemm_tn_kernel<BN>), Cfg::THREADS,
+                               tn_smem<BN>(), S);
 }
 
 }  // namespace
@@ -421,6 +477,16 @@ cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const
         case 192: return launch_tn<192>(tmA, tmB, g, gt, num_sms, ska, stream);
         case 256: return launch_tn<256>(tmA, tmB, g, gt, num_sms, ska, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_split_clusters_tn(int BN, int S) {
+    switch (BN) {
+        case 64: return split_clusters_tn<64>(S);
+        case 128: return split_clusters_tn<128>(S);
+        case 192: return split_clusters_tn<192>(S);
+        case 256: return split_clusters_tn<256>(S);
+        default: return 0;
     }
 }
 

@@ -11,21 +11,41 @@ namespace fp8bs {
 
 // Launch with programmatic stream serialisation (see grid_dependency_wait in ptx.cuh): the
 // launch may begin while the previous kernel on the stream is finishing.
+// With cluster_x > 1 the grid is launched as clusters of cluster_x consecutive CTAs along x
+// (grid.x must be a multiple of it).
 template <typename... KArgs, typename... Args>
-cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                       cudaStream_t stream, Args&&... args) {
+cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                               cudaStream_t stream, int cluster_x, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = cluster_x > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    return launch_pdl_cluster(kernel, grid, block, smem, stream, 1, static_cast<Args&&>(args)...);
+}
+
+// Split K inside a cluster: at most this many CTAs share a tile (the portable cluster size).
+constexpr int kMaxSplit = 8;
+
+// How many clusters of `cluster_x` CTAs of `kernel` (with `threads` threads and `smem` bytes of
+// dynamic shared memory, already allowed by cudaFuncSetAttribute) can be resident at once on
+// the current device; 0 if the query fails. Cached per (kernel, cluster size, smem, device).
+int max_active_clusters(const void* kernel, int threads, int smem, int cluster_x);
 
 cudaError_t launch_act_quant(const void* x, void* y, float* s, int64_t M, int64_t K, bool ue8m0,
                              int num_sms, cudaStream_t stream);
@@ -62,6 +82,7 @@ void fill_group_table(GroupTable* gt, const int64_t* row_off, int groups, int N,
 struct StreamKArgs {
     void* workspace;
     int dp_tiles;
+    int ksplit;       // > 1: no workspace; ksplit CTAs (one cluster) share each tile's K loop
 };
 
 // Workspace layout: one int counter per SM (rounded up to 256 bytes), then one 128 x 256 fp32
@@ -85,6 +106,11 @@ cudaError_t launch_gemm_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const
                            const GroupTable& gt, int BN, int num_sms, const StreamKArgs& ska,
                            cudaStream_t stream);
 
+// Clusters of S CTAs of the normal-orientation kernel at tile width BN (fp32 scales: _tn;
+// ue8m0: _bs) that can be resident at once for a split-K launch; 0 if that split does not fit.
+int max_split_clusters_tn(int BN, int S);
+int max_split_clusters_bs(int BN, int S);
+
 // Block-scaled orientation, for scales that are all powers of two (FP8BS_SCALE_UE8M0): the
 // tensor core applies a_s and b_s as ue8m0 exponents per K block; tiles of 128 rows x BN
 // (64 or 128; 128 when K loops are shared) columns, same maps and group table as
@@ -96,6 +122,8 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
 // The library's static stream-K workspace on the current device (no allocation); fails with
 // cudaErrorInvalidValue on a device with more SMs than it covers.
 cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes);
+// Zero the static workspace's counters on the current device (enqueued on `stream`).
+cudaError_t reset_static_workspace_counters(cudaStream_t stream);
 
 // Activations quantised inside the decode GEMM launch (MT <= 64): x bf16 [M, K] -> y e4m3,
 // s fp32 (as act_quant writes them); every CTA quantises the rows of each K block it reads,
@@ -110,8 +138,13 @@ struct FusedQuant {
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
 // on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K] (with
 // FusedQuant: a bf16 map over x, box {128, MT}, no swizzle).
+// ksplit > 1 (quantised input only): the K loop of each 128-row slab is split between the
+// ksplit CTAs of a cluster, whose fp32 partials are added in rank order through distributed
+// shared memory. plan_gemm_swapab gives the split for a problem (1: none; 0: this kernel cannot
+// take K, whose activation scales would not fit in shared memory).
+int plan_gemm_swapab(int MT, bool fused, int M, int N, int K, int num_sms);
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
-                               const GemmArgs& g, int MT, const FusedQuant& fq,
+                               const GemmArgs& g, int MT, const FusedQuant& fq, int ksplit,
                                cudaStream_t stream);
 
 // bf16 path, decode orientation (M <= 64, MT = 16, 32 or 64): y bf16 [M, N] = x . W'^T with W'

@@ -159,9 +159,30 @@ FP8BS_API int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, cons
                             void* stream);
 
 /*
+ * fp8bs_gemm_plan -- which kernel, tile and schedule fp8bs_gemm_ws (or fp8bs_gemm_ex, when
+ * with_workspace == 0) would launch for these sizes on the current device. Launches nothing.
+ * The pages' fp8_gemm picks its configuration by autotuning ("DeepSeek-V3 Administrator &
+ * Developer Guide", §8.5.3 and §6.5); this library picks it from the shape, and this call shows
+ * the pick.
+ *
+ *   M, N, K > 0 with K % 128 == 0; scale_fmt as in fp8bs_gemm.
+ *   kernel   [out] FP8BS_KERNEL_SWAPPED (M <= 128: 128-row weight slabs on the MMA's M side),
+ *                  FP8BS_KERNEL_PROMOTED (fp32 scales applied by CUDA cores per K block) or
+ *                  FP8BS_KERNEL_BLOCK_SCALED (ue8m0 scales applied by the tensor cores).
+ *   tile     [out] rows of A per CTA (swapped) or columns of B per tile (otherwise).
+ *   ksplit   [out] CTAs of one thread-block cluster that share each tile's K loop (1: none).
+ *   stream_k [out] 1 if tiles share K loops through the workspace (stream-K), else 0.
+ */
+#define FP8BS_KERNEL_SWAPPED 0
+#define FP8BS_KERNEL_PROMOTED 1
+#define FP8BS_KERNEL_BLOCK_SCALED 2
+FP8BS_API int fp8bs_gemm_plan(int64_t M, int64_t N, int64_t K, int scale_fmt, int with_workspace,
+                              int* kernel, int* tile, int* ksplit, int* stream_k);
+
+/*
  * fp8bs_gemm_workspace_size -- bytes of workspace fp8bs_gemm_ws uses on the current device: the
- * same for every problem size (one 128 x 128 fp32 partial and one counter per SM, about 10 MB
- * on 152 SMs).
+ * same for every problem size (one 128 x 256 fp32 partial tile and one counter per SM, about
+ * 20 MB on 152 SMs).
  *   bytes [out] host pointer receiving the size.
  */
 FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
@@ -174,7 +195,8 @@ FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
  * FP8BS_GEMM_WEIGHTS_CONSTANT, streams its weights meanwhile). With
  * FP8BS_GEMM_QUANT_IN_KERNEL and M <= 64 one kernel does both: each CTA of the GEMM quantises
  * the rows of every K block it reads, as act_quant would, and the CTAs of the first 128
- * columns also write y and s. On GB300 at decode sizes this single kernel measured slower than
+ * columns also write y and s. Where the separate GEMM would split each weight slab's K loop
+ * between several CTAs (few slabs, see fp8bs_gemm_plan), the two launches run instead. On GB300 at decode sizes this single kernel measured slower than
  * the two (the quantisation sits on every K block's critical path), so it is not the default.
  *
  *   x      [in]  bf16 [M, K], 16-byte aligned.
@@ -217,13 +239,16 @@ FP8BS_API int fp8bs_linear_bf16(const void* x, const void* w, const float* w_s, 
 
 /*
  * fp8bs_gemm_noalloc -- fp8bs_gemm_ws on a workspace that the library keeps in a static device
- * array (about 10.5 MB per device, reserved when the library's device code is loaded): no
- * memory is allocated by the caller or by the library at any time. The pages have no
+ * array (about 21 MB per device, sized for up to 160 SMs and reserved when the library's device
+ * code is loaded): no memory is allocated by the caller or by the library at any time. The pages have no
  * counterpart of this entry point: their fp8_gemm neither splits K nor uses scratch memory.
  *
  *   Arguments, results and accuracy as in fp8bs_gemm_ws.
  *   Calls on one device share the one workspace: they must not run at the same time (issue
- *   them on one stream, or order them).
+ *   them on one stream, or order them). After a call that recorded a device wait error, clear
+ *   the error with fp8bs_device_error(clear != 0), which also zeroes the workspace's counters,
+ *   before the next call. The workspace's address is looked up on the first call made with
+ *   each device current and kept for the life of the process (a device reset invalidates it).
  *   A device with more than 160 SMs (more than the static workspace covers) returns
  *   FP8BS_ERR_UNSUPPORTED_DEVICE without launching anything.
  */
@@ -262,6 +287,8 @@ FP8BS_API const char* fp8bs_status_string(int status);
  * on the current device. Every wait inside the library's kernels is bounded in time; a wait
  * that runs out sets a bit here (see FP8BS_DEVERR_*), abandons the kernel's remaining work
  * (its output is then undefined) and lets the kernel exit cleanly. Synchronises `stream`.
+ * With `clear`, the counters of fp8bs_gemm_noalloc's static workspace on this device are also
+ * zeroed (a call abandoned after a wait error may leave them nonzero).
  *   out [out] host pointer receiving the word (0 = no error since the last clear).
  */
 FP8BS_API int fp8bs_device_error(unsigned int* out, int clear, void* stream);

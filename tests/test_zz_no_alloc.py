@@ -23,27 +23,29 @@ def _clean_device_error():
     assert fp8bs.fp8bs_device_error(clear=True) == 0, "a kernel wait ran out"
 
 
-@pytest.mark.parametrize("M,N,K", [
-    (1100, 2500, 2048),    # 180 tiles shared between neighbouring CTAs, ragged edges
-    (2560, 2048, 2048),    # 152 tiles computed whole, then 168 shared
-    (2048, 1536, 7168),    # the MLA q projection
+@pytest.mark.parametrize("M,N,K,fmt", [
+    (1100, 2500, 2048, fp8bs.SCALE_UE8M0),  # 180 tiles shared between neighbouring CTAs
+    (2560, 2048, 2048, fp8bs.SCALE_UE8M0),  # 152 tiles computed whole, then 168 shared
+    (2048, 1536, 7168, fp8bs.SCALE_UE8M0),  # the MLA q projection
+    (2560, 2048, 2048, fp8bs.SCALE_FP32),   # fp32 scales: 220 tiles 192 wide, all shared
 ])
-def test_noalloc_matches_caller_workspace_on_two_calls_in_a_row(M, N, K):
+def test_noalloc_matches_caller_workspace_on_two_calls_in_a_row(M, N, K, fmt):
+    ue8m0 = fmt == fp8bs.SCALE_UE8M0
     x = synth.activations(M, K, seed=M + N, name="noallocA", outlier_frac=0.01)
-    a, a_s = oracle.act_quant(x, oracle.SCALE_UE8M0)
-    b, b_s = synth.weights(N, K, seed=N + K, name="noallocB", pow2=True)
+    a, a_s = oracle.act_quant(x, oracle.SCALE_UE8M0 if ue8m0 else oracle.SCALE_FP32)
+    b, b_s = synth.weights(N, K, seed=N + K, name="noallocB", pow2=ue8m0)
     A, AS, B, BS = dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s)
     ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
     st = torch.cuda.current_stream().cuda_stream
 
     ref = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
     fp8bs.fp8bs_gemm_ws(A.data_ptr(), AS.data_ptr(), B.data_ptr(), BS.data_ptr(), ref.data_ptr(),
-                        M, N, K, fp8bs.SCALE_UE8M0, 0, ws.data_ptr(), ws.numel(), st)
+                        M, N, K, fmt, 0, ws.data_ptr(), ws.numel(), st)
     outs = []
     for _ in range(2):
         c = torch.full((M, N), float("nan"), dtype=torch.bfloat16, device="cuda")
         fp8bs.fp8bs_gemm_noalloc(A.data_ptr(), AS.data_ptr(), B.data_ptr(), BS.data_ptr(),
-                                 c.data_ptr(), M, N, K, fp8bs.SCALE_UE8M0, 0, st)
+                                 c.data_ptr(), M, N, K, fmt, 0, st)
         outs.append(c)
     torch.cuda.synchronize()
     for i, c in enumerate(outs):
