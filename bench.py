@@ -249,6 +249,24 @@ class Gpu:
         self.fp8bs.fp8bs_linear_bf16(x.data_ptr(), w.data_ptr(), s.data_ptr(), y.data_ptr(), M, N,
                                      K, flags, self.sh)
 
+    def time_cycle(self, fn, items, rounds):
+        """Average device time (ms) of one fn(item) launch: `rounds` passes over `items`, all
+        launched back to back as one region between two events on the benchmark stream (behind
+        a GPU sleep, so that no launch waits on the host)."""
+        torch = self.torch
+        for it in items:
+            fn(it)
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e6 + rounds * len(items) * 1e5))
+        t0, t1 = self.event(), self.event()
+        t0.record()
+        for _ in range(rounds):
+            for it in items:
+                fn(it)
+        t1.record()
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / (rounds * len(items))
+
     def time_each(self, fn, reps, flush=True):
         """Device time (ms) of one fn() launch with a cold L2: `reps` launches back to back,
         each after an L2 flush, timed as one region between two events, minus a region of the
@@ -274,6 +292,15 @@ class Gpu:
         e[2].record()
         torch.cuda.synchronize()
         return (e[0].elapsed_time(e[1]) - e[1].elapsed_time(e[2])) / reps
+
+
+def copy_of_bytes(g: Gpu, total_bytes):
+    """A device-to-device copy that reads and writes total_bytes / 2 each (the same bytes in
+    total as the kernel it stands beside)."""
+    n = total_bytes // 2 // 16 * 16
+    src = g.torch.empty(n, dtype=g.torch.uint8, device="cuda")
+    dst = g.torch.empty(n, dtype=g.torch.uint8, device="cuda")
+    return lambda: dst.copy_(src)
 
 
 def decode_setup(g: Gpu, seed=0):
@@ -494,8 +521,53 @@ def secondary(g: Gpu, peaks, reps=20):
         s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
         ms = g.time_each(lambda: g.act_quant(x, y, s, M, K, fmt), reps)
         gbs = act_quant_bytes(M, K) / ms / 1e6
+        # A device copy moving the same number of bytes (half read, half written), timed the
+        # same way: what any kernel moving these bytes achieves at this size.
+        copy_ms = g.time_each(copy_of_bytes(g, act_quant_bytes(M, K)), reps)
         out[name] = {"M": M, "K": K, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
-                     "frac_hbm": round(gbs / hbm, 4)}
+                     "frac_hbm": round(gbs / hbm, 4), "copy_us": round(copy_ms * 1e3, 2),
+                     "frac_of_copy": round(copy_ms / ms, 4)}
+        del x, y, s
+
+    # act_quant at the decode sizes: one row block per M, each launch timed alone (cold L2)
+    for M in DECODE_MS:
+        x = g.bf16(synth.decode(M))
+        y = torch.empty((M, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((M, K_DIM // 128), dtype=torch.float32, device="cuda")
+        ms = g.time_each(lambda: g.act_quant(x, y, s, M, K_DIM, 0), reps)
+        out[f"act_quant_decode_M{M}"] = {"M": M, "K": K_DIM, "us": round(ms * 1e3, 2),
+                                         "GB/s": round(act_quant_bytes(M, K_DIM) / ms / 1e6, 1)}
+        del x, y, s
+
+    # decode GEMMs with few weight slabs (each slab's K loop split between the CTAs of a
+    # cluster): the MLP down-projection (N=7168, K=18432; four distinct 132 MB weights) and one
+    # MoE expert's up-projection (N=2048, K=7168; 32 distinct 14.7 MB weights). Launches cycle
+    # through the weights back to back, so no weight is in L2 when it is read again.
+    for name, N, K, n_w in (("decode_down_N7168_K18432", K_DIM, N_DIM, 4),
+                            ("decode_expert_N2048_K7168", synth.MOE_INTER, K_DIM, 32)):
+        b0, bs0 = synth.weights(N, K, 0, f"decode/{name}")
+        B0, S0 = g.e4m3(b0), g.f32(bs0)
+        del b0
+        ws = [(B0, S0)] + [
+            (torch.roll(B0.view(torch.uint8), shifts=i * 8, dims=0).contiguous()
+             .view(torch.float8_e4m3fn), torch.roll(S0, shifts=i, dims=0).contiguous())
+            for i in range(1, n_w)]
+        per_m = []
+        for M in DECODE_MS:
+            x = g.bf16(synth.activations(M, K, 0, f"decode/{name}/x", outlier_frac=0.01))
+            y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
+            s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+            c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            g.act_quant(x, y, s, M, K)
+            plan = g.fp8bs.fp8bs_gemm_plan(M, N, K, 0, False)
+            ms = g.time_cycle(lambda w: g.gemm_ex(y, s, w[0], w[1], c, M, N, K, 0,
+                                                  WEIGHTS_CONSTANT), ws, max(3, 400 // n_w))
+            gbs = gemm_bytes(M, N, K) / ms / 1e6
+            per_m.append({"M": M, "us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+                          "frac_hbm": round(gbs / hbm, 4), "ksplit": plan["ksplit"]})
+            del x, y, s, c
+        out[name] = {"N": N, "K": K, "weights": n_w, "per_M": per_m}
+        del ws, B0, S0
 
     # ue8m0 MLA projections (block-scaled MMA: the tensor cores apply the power-of-two scales)
     xa = synth.mla_acts()
@@ -670,6 +742,21 @@ def run_profile(case: str, launches: int, warmup: int):
         g.act_quant(x, y, s, M, K_DIM)
         fn = lambda: g.gemm_ex(y, s, B, S, c, M, N_DIM, K_DIM, 0,  # noqa: E731
                                WEIGHTS_CONSTANT)
+    elif case.startswith("expert") or case.startswith("down"):
+        # decode GEMMs with few weight slabs (split K): expert1..expert64 (N=2048, K=7168),
+        # down1..down64 (N=7168, K=18432)
+        expert = case.startswith("expert")
+        M = int(case[len("expert" if expert else "down"):] or 1)
+        N, K = (synth.MOE_INTER, K_DIM) if expert else (K_DIM, N_DIM)
+        b, bs = synth.weights(N, K, 0, "decode/profile")
+        B, S = g.e4m3(b), g.f32(bs)
+        x = g.bf16(synth.activations(M, K, 0, "decode/profile/x", outlier_frac=0.01))
+        y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((M, K // 128), dtype=torch.float32, device="cuda")
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        g.act_quant(x, y, s, M, K)
+        fn = lambda: g.gemm_ex(y, s, B, S, c, M, N, K, 0,  # noqa: E731
+                               WEIGHTS_CONSTANT)
     elif case in ("prefill_up", "prefill_down"):
         up = case == "prefill_up"
         N, K = (N_DIM, K_DIM) if up else (K_DIM, N_DIM)
@@ -791,7 +878,7 @@ def main(argv=None):
     ap.add_argument("--out-dir", default=os.path.join(ROOT, "bench_out"),
                     help="where the per-rank clock samples (clocks_rank<r>.csv) are written")
     ap.add_argument("--profile", metavar="CASE", default=None,
-                    help="run one kernel only (decode1..decode64, prefill_up, prefill_down, prefill_up_ue8m0, mla1536, mla576, linear1..linear4096, "
+                    help="run one kernel only (decode1..decode64, expert1..expert64, down1..down64, prefill_up, prefill_down, prefill_up_ue8m0, mla1536, mla576, linear1..linear4096, "
                          "act_quant, dequant, moe): warmup + steps launches, for ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
@@ -846,7 +933,11 @@ def main(argv=None):
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": 2 * len(DECODE_MS) * args.steps}
     if rank == 0 and world == 1 and not args.quick:
-        line["secondary"] = secondary(g, peaks)
+        sampler = ClockSampler(torch.cuda.current_device(),
+                               os.path.join(args.out_dir, "clocks_secondary.csv"))
+        with sampler:
+            line["secondary"] = secondary(g, peaks)
+        line["secondary"]["clocks"] = sampler.summary()
         line["cpu_baseline"] = cpu_baseline()
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -11,6 +11,8 @@ Raw entry points (same names and arguments as the C functions; pointers are ints
     fp8bs_gemm(a, a_s, b, b_s, c, M, N, K, scale_fmt, stream)
     fp8bs_gemm_ex(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, stream)
     fp8bs_gemm_plan(M, N, K, scale_fmt, with_workspace) -> dict
+    fp8bs_gemm_config(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, kernel, tile, ksplit,
+                      workspace, workspace_bytes, stream)
     fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt, stream)
     fp8bs_device_error(clear=True, stream=0) -> int
     fp8bs_probe_wait_timeout(timeout_ns, stream)
@@ -38,9 +40,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libfp8bs.so")
 GEMM_WEIGHTS_CONSTANT = 0x1
 GEMM_QUANT_IN_KERNEL = 0x2
-KERNEL_SWAPPED, KERNEL_PROMOTED, KERNEL_BLOCK_SCALED = 0, 1, 2
+KERNEL_SWAPPED, KERNEL_PROMOTED, KERNEL_BLOCK_SCALED, KERNEL_BLOCK_SCALED_PAIR = 0, 1, 2, 3
 EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_ex",
-           "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_plan", "fp8bs_gemm_noalloc",
+           "fp8bs_gemm_ws", "fp8bs_gemm_workspace_size", "fp8bs_gemm_plan", "fp8bs_gemm_config",
+           "fp8bs_gemm_noalloc",
            "fp8bs_act_quant_gemm", "fp8bs_linear_bf16",
            "fp8bs_gemm_grouped",
            "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
@@ -76,6 +79,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_gemm_workspace_size.argtypes = [ctypes.POINTER(ctypes.c_size_t)]
         ip = ctypes.POINTER(ctypes.c_int)
         lib.fp8bs_gemm_plan.argtypes = [i64, i64, i64, i32, i32, ip, ip, ip, ip]
+        lib.fp8bs_gemm_config.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i32, ctypes.c_uint,
+                                          i32, i32, i32, vp, ctypes.c_size_t, vp]
         lib.fp8bs_linear_bf16.argtypes = [vp, vp, vp, vp, i64, i64, i64, ctypes.c_uint, vp]
         lib.fp8bs_act_quant_gemm.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, i64, i32,
                                              ctypes.c_uint, vp, ctypes.c_size_t, vp]
@@ -154,6 +159,14 @@ def fp8bs_gemm_plan(M, N, K, scale_fmt=SCALE_FP32, with_workspace=True) -> dict:
                                                      *[ctypes.byref(o) for o in out]))
     return {"kernel": out[0].value, "tile": out[1].value, "ksplit": out[2].value,
             "stream_k": bool(out[3].value)}
+
+
+def fp8bs_gemm_config(a, a_s, b, b_s, c, M, N, K, scale_fmt=SCALE_FP32, flags=0,
+                      kernel=KERNEL_PROMOTED, tile=128, ksplit=1, workspace=0, workspace_bytes=0,
+                      stream=0) -> None:
+    _check("fp8bs_gemm_config", load().fp8bs_gemm_config(
+        a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, kernel, tile, ksplit, workspace,
+        workspace_bytes, stream))
 
 
 def fp8bs_gemm_grouped(a, a_s, b, b_s, c, row_offsets, groups, N, K, scale_fmt=SCALE_FP32,

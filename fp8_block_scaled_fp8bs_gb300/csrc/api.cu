@@ -3,6 +3,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <mutex>
 
@@ -176,21 +177,26 @@ fp8bs::StreamKArgs plan_stream_k_tn(int64_t tiles, int64_t num_kb, int sms, void
     return fp8bs::StreamKArgs{workspace, dp, 1};
 }
 
-// Relative time of one K block of a 128 x bn tile (the tile-width models of the two kernels).
+// Relative time of one K block of a 128 x bn tile (the tile-width models of the two kernels;
+// the block-scaled kernel's 64-wide tiles have two MMA issuers: 18.3 us for the MLA kv
+// projection as 144 such tiles against 24.1 us as 80 tiles 128 wide, both one round).
 int64_t width_cost(bool block_scaled, int bn) {
     switch (bn) {
         case 256: return block_scaled ? 134 : 141;
         case 192: return block_scaled ? 117 : 129;
         case 128: return 100;
-        default: return block_scaled ? 100 : 80;
+        default: return block_scaled ? 76 : 80;
     }
 }
 
 // Split K inside a cluster (StreamKArgs::ksplit) when the tiles are few: the tile width and
-// split with the lowest modelled time -- a CTA's share of the K blocks plus two K blocks for the
-// exchange of partials, at the width's K-block cost -- provided every cluster of the grid can
-// be resident at once. Taken only if it beats `cost_plain` (the whole-tile schedule) by 10 %;
-// otherwise ksplit = 1.
+// split with the lowest modelled time -- a CTA's share of the K blocks plus five K blocks for
+// the exchange of partials, at the width's K-block cost --
+// provided every cluster of the grid can be resident at once. Taken only if it beats
+// `cost_plain` (the whole-tile schedule) by 10 %; otherwise ksplit = 1. Measured on GB300: one
+// MoE expert's 300 rows (N=2048, K=7168, fp32 scales) take 29.8 us as 24 whole 256-wide tiles
+// and 16.7-17.4 us split four ways; the MLA kv projection (M=2048, N=576) is fastest as 144
+// whole 64-wide tiles (18.3 us against 19.7 us as 48 192-wide tiles split two ways).
 struct SplitPlan {
     int bn;
     int ksplit;
@@ -205,7 +211,7 @@ SplitPlan plan_split(bool block_scaled, int64_t m_tiles, int64_t N, int64_t num_
         const int64_t tiles = m_tiles * ceil_div(N, bn);
         for (int S = fp8bs::kMaxSplit; S > 1; --S) {
             if (tiles * S > sms || num_kb / S < 2) continue;
-            const int64_t cost = (ceil_div(num_kb, S) + 2) * width_cost(block_scaled, bn);
+            const int64_t cost = (ceil_div(num_kb, S) + 5) * width_cost(block_scaled, bn);
             if (cost >= best_cost) continue;
             const int fit = block_scaled ? fp8bs::max_split_clusters_bs(bn, S)
                                          : fp8bs::max_split_clusters_tn(bn, S);
@@ -242,6 +248,7 @@ struct GemmPlan {
     int tile;                  // MT (swapped) or BN (normal orientation)
     fp8bs::StreamKArgs ska;    // stream-K workspace or split K (normal orientation)
     int ksplit;                // CTAs per tile sharing its K loop in a cluster (1: none)
+    int pairs;                 // CTA pairs launched (FP8BS_KERNEL_BLOCK_SCALED_PAIR)
 };
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool block_scaled, void* workspace,
@@ -249,6 +256,7 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool block_scaled, void* wor
     GemmPlan p;
     p.ska = no_stream_k();
     p.ksplit = 1;
+    p.pairs = 0;
     if (M <= 128) {
         // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA (or
         // per cluster, with the K loop split).
@@ -268,6 +276,9 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool block_scaled, void* wor
     if (block_scaled) {
         p.ska = plan_stream_k_bs(m_tiles, N, K / 128, sms, workspace);
         BN = p.ska.workspace ? 128 : fp8bs::pick_tile_n_bs(m_tiles, N, sms);
+        // The CTA-pair kernel is not chosen here: measured on GB300 it runs 9-12 % slower than
+        // the one-CTA kernel (prefill up 412 against 378 us, the MLA q projection 30.5 against
+        // 27.2 us); fp8bs_gemm_config can select it.
     } else {
         BN = fp8bs::pick_tile_n(m_tiles, N, sms);
         p.ska = plan_stream_k_tn(m_tiles * ceil_div(N, BN), K / 128, sms, workspace);
@@ -288,10 +299,65 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool block_scaled, void* wor
     return p;
 }
 
-// fp8bs_gemm_ex and fp8bs_gemm_ws: checks, then the kernel for the shape (see fp8bs.h).
+// A caller-given configuration (fp8bs_gemm_config): kernel, tile and K split, checked against
+// what the kernels support for this shape. false: not supported.
+bool config_plan(const int cfg[3], int64_t M, int64_t N, int64_t K, bool block_scaled,
+                 void* workspace, int sms, GemmPlan* p) {
+    const int kind = cfg[0], tile = cfg[1], ks = cfg[2];
+    const int64_t num_kb = K / 128;
+    p->kind = kind;
+    p->tile = tile;
+    p->ska = no_stream_k();
+    p->ksplit = 1;
+    p->pairs = 0;
+    if (ks < 0 || ks > fp8bs::kMaxSplit || ks > num_kb) return false;
+    switch (kind) {
+        case FP8BS_KERNEL_SWAPPED:
+            if ((tile != 16 && tile != 32 && tile != 64 && tile != 128) || M > tile || ks == 0)
+                return false;
+            p->ksplit = ks;
+            return fp8bs::check_gemm_swapab(tile, static_cast<int>(K), ks);
+        case FP8BS_KERNEL_PROMOTED:
+        case FP8BS_KERNEL_BLOCK_SCALED: {
+            const bool bs = kind == FP8BS_KERNEL_BLOCK_SCALED;
+            if (bs && !block_scaled) return false;
+            if (tile != 64 && tile != 128 && tile != 192 && tile != 256) return false;
+            const int64_t tiles = ceil_div(M, 128) * ceil_div(N, tile);
+            if (ks == 0) {      // stream-K over the workspace
+                if (!workspace || (bs && tile != 128) || tiles < sms || num_kb < 2 ||
+                    !units_fit(tiles, num_kb))
+                    return false;
+                p->ska = fp8bs::StreamKArgs{workspace, dp_tiles_before_sharing(tiles, sms), 1};
+                return true;
+            }
+            if (ks > 1) {
+                const int fit = bs ? fp8bs::max_split_clusters_bs(tile, ks)
+                                   : fp8bs::max_split_clusters_tn(tile, ks);
+                if (fit < 1 || tiles * ks > INT32_MAX) return false;
+                p->ska = fp8bs::StreamKArgs{nullptr, 0, ks};
+                p->ksplit = ks;
+            }
+            return true;
+        }
+        case FP8BS_KERNEL_BLOCK_SCALED_PAIR: {
+            if (!block_scaled || ks != 1) return false;
+            if (tile != 128 && tile != 192 && tile != 256) return false;
+            const int64_t tiles = ceil_div(M, 256) * ceil_div(N, tile);
+            const int64_t cap = std::min<int64_t>(sms / 2, fp8bs::max_pair_clusters_bs(tile));
+            if (cap < 1) return false;
+            p->pairs = static_cast<int>(std::min<int64_t>(tiles, cap));
+            return true;
+        }
+        default:
+            return false;
+    }
+}
+
+// fp8bs_gemm_ex, fp8bs_gemm_ws and fp8bs_gemm_config: checks, then the kernel for the shape
+// (or the caller's configuration `cfg`, if given; see fp8bs.h).
 int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
               int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
-              void* workspace, size_t workspace_bytes, void* stream) {
+              void* workspace, size_t workspace_bytes, void* stream, const int* cfg = nullptr) {
     if ((flags & ~FP8BS_GEMM_WEIGHTS_CONSTANT) != 0) return FP8BS_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0 || K % FP8BS_BLOCK != 0) return FP8BS_ERR_INVALID_ARG;
     if (scale_fmt != FP8BS_SCALE_FP32 && scale_fmt != FP8BS_SCALE_UE8M0)
@@ -327,7 +393,13 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
     g.weights_constant = (flags & FP8BS_GEMM_WEIGHTS_CONSTANT) ? 1 : 0;
 
     const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
-    const GemmPlan p = plan_gemm(M, N, K, block_scaled, workspace, sms);
+    GemmPlan p;
+    if (cfg) {
+        if (!config_plan(cfg, M, N, K, block_scaled, workspace, sms, &p))
+            return FP8BS_ERR_INVALID_ARG;
+    } else {
+        p = plan_gemm(M, N, K, block_scaled, workspace, sms);
+    }
     CUtensorMap tmA, tmB;
     if (p.kind == FP8BS_KERNEL_SWAPPED) {
         if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, p.tile))
@@ -335,11 +407,16 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
         return status_of(
             fp8bs::launch_gemm_swapab(tmB, tmA, g, p.tile, fp8bs::FusedQuant{}, p.ksplit, st));
     }
+    if (p.kind == FP8BS_KERNEL_BLOCK_SCALED_PAIR) {
+        if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, p.tile / 2))
+            return FP8BS_ERR_CUDA;
+        return status_of(fp8bs::launch_gemm_bs_pair(tmA, tmB, g, p.tile, p.pairs, st));
+    }
     if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, p.tile)) return FP8BS_ERR_CUDA;
     const int64_t rows[2] = {0, M};
     fp8bs::GroupTable gt;
     fp8bs::fill_group_table(&gt, rows, 1, static_cast<int>(N), p.tile);
-    if (block_scaled)
+    if (p.kind == FP8BS_KERNEL_BLOCK_SCALED)
         return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, p.tile, sms, p.ska, st));
     return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, p.tile, sms, p.ska, st));
 }
@@ -504,6 +581,15 @@ int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b, const flo
     if (e == cudaErrorInvalidValue) return FP8BS_ERR_UNSUPPORTED_DEVICE;
     if (e != cudaSuccess) return FP8BS_ERR_CUDA;
     return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, ws, bytes, stream);
+}
+
+int fp8bs_gemm_config(const void* a, const float* a_s, const void* b, const float* b_s, void* c,
+                      int64_t M, int64_t N, int64_t K, int scale_fmt, unsigned int flags,
+                      int kernel, int tile, int ksplit, void* workspace, size_t workspace_bytes,
+                      void* stream) {
+    const int cfg[3] = {kernel, tile, ksplit};
+    return gemm_impl(a, a_s, b, b_s, c, M, N, K, scale_fmt, flags, workspace, workspace_bytes,
+                     stream, cfg);
 }
 
 int fp8bs_gemm_plan(int64_t M, int64_t N, int64_t K, int scale_fmt, int with_workspace,

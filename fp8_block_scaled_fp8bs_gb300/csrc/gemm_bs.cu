@@ -275,11 +275,6 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     const uint32_t wb = splat4(ue8m0_code(vb[i], pow2));
                     uint32_t wb2 = 0;
                     if constexpr (BN > 128) wb2 = splat4(ue8m0_code(vb2[i], pow2));
-                    if (kb + P < kb1) {                 // the scales of kb + P, in flight
-                        va[i] = __ldg(as_row + kb + P);
-                        vb[i] = __ldg(bs_row + kb + P);
-                        if constexpr (BN > 128) vb2[i] = __ldg(bs_row2 + kb + P);
-                    }
                     if (!warp_wait(&ring.empty[stage], phase ^ 1)) {
                         if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
                         ok = false;
@@ -300,6 +295,13 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&ring.full[stage]);
+                    // The scales of kb + P, requested only now: a release (the arrive) would
+                    // otherwise wait for them to return from memory.
+                    if (kb + P < kb1) {
+                        va[i] = __ldg(as_row + kb + P);
+                        vb[i] = __ldg(bs_row + kb + P);
+                        if constexpr (BN > 128) vb2[i] = __ldg(bs_row2 + kb + P);
+                    }
                     if (++stage == stages) {
                         stage = 0;
                         phase ^= 1;
@@ -531,6 +533,352 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     if (warp == ISSUER) tmem_dealloc(tmem_base, tmem_cols);
 }
 
+// ================================================================ CTA pairs
+//
+// The same GEMM on CTA pairs (cta_group::2): a cluster of two CTAs on neighbouring SMs computes
+// a 256 x BN tile. CTA r (cluster rank r) loads rows 128r .. 128r+127 of the A tile and rows
+// (BN/2)r .. (BN/2)(r+1)-1 of the B tile into its own shared memory, writes the scale factors
+// of its 128 rows of A and of all BN rows of B into its own TMEM, and receives its 128 rows of
+// the accumulator in its own TMEM; the even CTA issues the MMAs for both. Per SM this halves
+// the bytes of B that TMA writes to and the tensor cores read from shared memory in each K
+// block -- the one-CTA kernel moves 2 x (16 KB + BN x 128 B) per K block through one SM's
+// shared memory, more than it delivers at the MMA rate.
+//   - Both CTAs' TMA bytes complete the even CTA's `full` barrier of the stage; the even CTA's
+//     MMA commits arrive on the `empty` and `tfull` barriers of both CTAs at once; both CTAs'
+//     epilogue warps release a TMEM buffer on the even CTA's `tempty` barrier.
+//   - Scale factors travel in chunks of CHUNK K blocks through a ring of SLOTS TMEM slots per
+//     CTA: both CTAs' scale-factor warps fill a slot and arrive on the even CTA's `sf_full`,
+//     the MMA commit after the chunk's last K block frees it in both CTAs (`sf_empty`), and
+//     the writers run up to SLOTS - 1 chunks ahead of the MMAs. A hand-over between the SMs
+//     per K block (the one-CTA kernel's scheme) measured 2.3 x slower than the same pipeline
+//     without scale factors; per chunk it is paid once per CTA per CHUNK K blocks.
+//   - Whole tiles, one group; tiles ordered 256-row blocks fastest.
+template <int BN>
+struct PairCfg {
+    static_assert(BN == 128 || BN == 192 || BN == 256, "pair tile width");
+    static constexpr int SF_WARPS = 4;
+    static constexpr int EPI_WARPS = 4;
+    static constexpr int THREADS = 32 * (SF_WARPS + EPI_WARPS + 2);
+    static constexpr int B_HALF = (BN / 2) * BK;            // this CTA's half of the B tile
+    static constexpr int STAGE = A_TILE + B_HALF;
+    static constexpr int CHUNK = 8;                          // K blocks per scale-factor slot
+    static constexpr int SLOTS = 2;
+    static constexpr int SF_A = 4 * CHUNK;                   // A: 4 columns per K block
+    static constexpr int SF_SLOT = SF_A + 8 * CHUNK;         // then B: 8 columns per K block
+    static constexpr int NBUF = BN > 128 ? 1 : 2;
+    static constexpr int SF_COL0 = NBUF * BN;
+};
+
+template <int BN>
+__host__ __device__ constexpr int pair_stages() {
+    return (kSmemLimit - 1024 - ring_bytes(kMaxStages) - 64) / PairCfg<BN>::STAGE > kMaxStages
+               ? kMaxStages
+               : (kSmemLimit - 1024 - ring_bytes(kMaxStages) - 64) / PairCfg<BN>::STAGE;
+}
+
+template <int BN>
+__host__ __device__ constexpr int pair_smem() {
+    return 1024 + pair_stages<BN>() * PairCfg<BN>::STAGE + ring_bytes(pair_stages<BN>()) + 64;
+}
+
+template <int BN>
+__host__ __device__ constexpr uint32_t pair_tmem_cols() {
+    return tmem_cols_for(
+        static_cast<uint32_t>(PairCfg<BN>::SF_COL0 + PairCfg<BN>::SLOTS * PairCfg<BN>::SF_SLOT));
+}
+
+template <int BN>
+__global__ void __launch_bounds__(PairCfg<BN>::THREADS, 1)
+    gemm_bs_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const GemmArgs g) {
+    using Cfg = PairCfg<BN>;
+    constexpr int stages = pair_stages<BN>();
+    constexpr uint32_t tmem_cols = pair_tmem_cols<BN>();
+    static_assert(tmem_cols <= 512, "TMEM holds 512 columns");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = align_1024(smem_raw);
+    uint8_t* sA = smem;
+    uint8_t* sB = smem + stages * A_TILE;
+    const Ring ring = carve_ring(sB + stages * Cfg::B_HALF, stages);
+    // Scale-factor slots: [SLOTS] filled (even CTA: both CTAs' writers), [SLOTS] free.
+    uint64_t* sf_full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ring.full) +
+                                                    ring_bytes(stages));
+    uint64_t* sf_empty = sf_full + Cfg::SLOTS;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const bool leader = rank == 0;
+    const int pair = blockIdx.x >> 1;
+    const int num_pairs = gridDim.x >> 1;
+    const int num_kb = g.K / BK;
+    const int m_pairs = (g.M + 2 * BM - 1) / (2 * BM);
+    const int num_tiles = m_pairs * ((g.N + BN - 1) / BN);
+    const int nb_count = (g.N + 127) / 128;
+    constexpr int PRODUCER = Cfg::SF_WARPS + Cfg::EPI_WARPS;
+    constexpr int ISSUER = PRODUCER + 1;
+
+    grid_dependency_wait();
+    grid_launch_dependents();
+    if (threadIdx.x == 0) {
+        // full: the leader's producer (and both CTAs' TMA bytes); tempty: the epilogue warps of
+        // both CTAs; sf_full: the scale-factor warps of both CTAs.
+        init_ring(ring, stages, 2 * Cfg::EPI_WARPS, 1);
+        for (int i = 0; i < Cfg::SLOTS; ++i) {
+            mbar_init(&sf_full[i], 2 * Cfg::SF_WARPS);
+            mbar_init(&sf_empty[i], 1);
+        }
+        fence_barrier_init();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == ISSUER) tmem_alloc_pair(ring.tmem_holder, tmem_cols);
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // both CTAs' barriers are initialised before either signals the other
+    tc_fence_after();
+    const uint32_t tmem_base = *ring.tmem_holder;
+
+    if (warp == PRODUCER) {
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+                // This CTA's rows of A and of B; a box that would start past the end of the
+                // matrix (ragged last tiles) is loaded in range instead: the rows it feeds are
+                // never stored, and the byte count stays the same.
+                const int m0 = min((tile % m_pairs) * (2 * BM) + static_cast<int>(rank) * BM,
+                                   g.M - 1);
+                const int nb0 = min((tile / m_pairs) * BN + static_cast<int>(rank) * (BN / 2),
+                                    g.N - 1);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    if (!mbar_wait(&ring.empty[stage], phase ^ 1)) {
+                        record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    if (leader) mbar_arrive_expect_tx(&ring.full[stage], 2 * Cfg::STAGE);
+                    const uint32_t full0 = mapa_shared(smem_addr(&ring.full[stage]), 0);
+                    tma_load_2d_pair(sA + stage * A_TILE, &tmA, full0, kb * BK, m0);
+                    tma_load_2d_pair(sB + stage * Cfg::B_HALF, &tmB, full0, kb * BK, nb0);
+                    ++issued;
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                }
+            }
+            if (!ok) {
+                if (leader) {
+                    drain_tma(ring, stages, issued);
+                } else {
+                    // This CTA's copies complete on the leader's barriers: give copies still in
+                    // flight time to land before the CTA may exit.
+                    const uint64_t t0 = global_timer_ns();
+                    while (global_timer_ns() - t0 < 200000ull) {
+                    }
+                }
+            }
+        }
+    } else if (warp == ISSUER) {
+        if (lane == 0 && leader) {
+            constexpr uint32_t idesc = idesc_e4m3_block_scaled(2 * BM, BN);
+            int stage = 0, buf = 0, slot = 0;
+            uint32_t phase = 0, tphase = 0, sphase = 0;
+            bool ok = true;
+            for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+                if (!mbar_wait_cluster(&ring.tempty[buf], tphase ^ 1)) {
+                    record_error(FP8BS_DEVERR_MMA_WAIT);
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * BN);
+                for (int kb = 0; kb < num_kb; ++kb) {
+                    const int j = kb % Cfg::CHUNK;
+                    if ((j == 0 && !mbar_wait_cluster(&sf_full[slot], sphase)) ||
+                        !mbar_wait(&ring.full[stage], phase)) {
+                        record_error(FP8BS_DEVERR_MMA_WAIT);
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a_addr = smem_addr(sA + stage * A_TILE);
+                    const uint32_t b_addr = smem_addr(sB + stage * Cfg::B_HALF);
+                    const uint32_t sf = tmem_base +
+                                        static_cast<uint32_t>(Cfg::SF_COL0 + slot * Cfg::SF_SLOT);
+#pragma unroll
+                    for (int jj = 0; jj < BK / MMA_K; ++jj)
+                        mma_f8_block_scaled_pair(d_tmem, smem_desc_k_sw128(a_addr + jj * MMA_K),
+                                                 smem_desc_k_sw128(b_addr + jj * MMA_K), idesc,
+                                                 sf + 4 * j, sf + Cfg::SF_A + 8 * j,
+                                                 (kb > 0 || jj > 0) ? 1u : 0u);
+                    mma_commit_pair(&ring.empty[stage]);
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    if (j == Cfg::CHUNK - 1 || kb == num_kb - 1) {
+                        mma_commit_pair(&sf_empty[slot]);     // the slot is free in both CTAs
+                        if (++slot == Cfg::SLOTS) {
+                            slot = 0;
+                            sphase ^= 1;
+                        }
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair(&ring.tfull[buf]);
+                if (Cfg::NBUF == 2) buf ^= 1;
+                if (buf == 0) tphase ^= 1;
+            }
+            // Make sure nothing issued is still running before TMEM is freed.
+            mma_commit_pair(ring.drain);
+            if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
+        }
+    } else if (warp < Cfg::SF_WARPS) {
+        // Scale-factor writers: warp w owns TMEM lanes 32w .. 32w+31 of this CTA's slots, i.e.
+        // rows 32w .. 32w+31 of its 128 rows of the tile; every lane writes the exponents of
+        // all BN rows of B (the tensor core of each CTA reads them from its own TMEM). Per K
+        // block j of a chunk: A exponent in columns 4j .. 4j+3; B in SF_A + 8j .. +7, column c
+        // for tile rows 32c .. 32c+31 (the second 128-row block of B from column 2 or 4 on).
+        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t sf_full0 = mapa_shared(smem_addr(sf_full), 0);
+        int slot = 0;
+        uint32_t sphase = 0;
+        bool ok = true, pow2 = true;
+        for (int tile = pair; ok && tile < num_tiles; tile += num_pairs) {
+            const int m0 = (tile % m_pairs) * (2 * BM) + static_cast<int>(rank) * BM;
+            const int n0 = (tile / m_pairs) * BN;
+            const int row = min(m0 + warp * 32 + lane, g.M - 1);
+            const float* as_row = g.a_s + static_cast<int64_t>(row) * num_kb;
+            const float* bs_row = g.b_s + static_cast<int64_t>(n0 / 128) * num_kb;
+            const float* bs_row2 = BN > 128 && n0 / 128 + 1 < nb_count ? bs_row + num_kb : bs_row;
+            const bool b_shift = BN > 128 && (n0 & 127) != 0;
+            for (int kc = 0; kc < num_kb; kc += Cfg::CHUNK) {
+                uint32_t wa[Cfg::CHUNK], wb[Cfg::CHUNK], wb2[Cfg::CHUNK];
+#pragma unroll
+                for (int i = 0; i < Cfg::CHUNK; ++i) {
+                    wa[i] = wb[i] = wb2[i] = 0;
+                    if (kc + i < num_kb) {
+                        wa[i] = splat4(ue8m0_code(__ldg(as_row + kc + i), pow2));
+                        wb[i] = splat4(ue8m0_code(__ldg(bs_row + kc + i), pow2));
+                        wb2[i] = BN > 128 ? splat4(ue8m0_code(__ldg(bs_row2 + kc + i), pow2))
+                                          : wb[i];
+                    }
+                }
+                if (!warp_wait(&sf_empty[slot], sphase ^ 1)) {
+                    if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t taddr = tmem_base + lane_base +
+                                       static_cast<uint32_t>(Cfg::SF_COL0 + slot * Cfg::SF_SLOT);
+                static_assert(Cfg::CHUNK == 8, "one 32-column A store, two 32-column B stores");
+                uint32_t v[32];
+#pragma unroll
+                for (int i = 0; i < Cfg::CHUNK; ++i)
+                    v[4 * i] = v[4 * i + 1] = v[4 * i + 2] = v[4 * i + 3] = wa[i];
+                tmem_st_32cols(taddr, v);
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int k = 4 * h + i;
+                        const uint32_t wx = b_shift ? wb2[k] : wb[k];
+                        v[8 * i + 0] = wb[k];
+                        v[8 * i + 1] = wb[k];
+                        v[8 * i + 2] = wx;
+                        v[8 * i + 3] = wx;
+                        v[8 * i + 4] = v[8 * i + 5] = v[8 * i + 6] = v[8 * i + 7] = wb2[k];
+                    }
+                    tmem_st_32cols(taddr + Cfg::SF_A + 32 * h, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sf_full0 + static_cast<uint32_t>(slot * 8));
+                if (++slot == Cfg::SLOTS) {
+                    slot = 0;
+                    sphase ^= 1;
+                }
+            }
+        }
+        if (!__all_sync(0xffffffffu, pow2) && lane == 0) record_error(FP8BS_DEVERR_SCALE_NOT_POW2);
+    } else if (warp < Cfg::SF_WARPS + Cfg::EPI_WARPS) {
+        // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (this CTA's rows of the same
+        // numbers), 32 columns at a time with the next chunk's load in flight, and hands the
+        // buffer back to the leader after the last load.
+        const int quarter = warp & 3;
+        const int row_in_tile = quarter * 32 + lane;
+        const bool vec = (g.N & 7) == 0;
+        int buf = 0;
+        uint32_t tphase = 0;
+        for (int tile = pair; tile < num_tiles; tile += num_pairs) {
+            const int m0 = (tile % m_pairs) * (2 * BM) + static_cast<int>(rank) * BM;
+            const int n0 = (tile / m_pairs) * BN;
+            if (!warp_wait(&ring.tfull[buf], tphase)) {
+                if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
+                break;
+            }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                                   static_cast<uint32_t>(buf * BN);
+            const int row = m0 + row_in_tile;
+            const bool store = row < g.M;
+            __nv_bfloat16* crow =
+                static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(row) * g.N + n0;
+            const int valid = min(BN, g.N - n0);
+            float va[32], vb[32];
+            tmem_ld_32cols(taddr, va);
+            tmem_wait_ld_32(va);
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c) {
+                float* cur = (c & 1) ? vb : va;
+                float* nxt = (c & 1) ? va : vb;
+                if (c + 1 < BN / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+                if (c + 1 == BN / 32) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0)
+                        mbar_arrive_cluster(mapa_shared(smem_addr(&ring.tempty[buf]), 0));
+                }
+                if (store) store_row_bf16<32>(crow + 32 * c, cur, valid - 32 * c, vec);
+                if (c + 1 < BN / 32) tmem_wait_ld_32(nxt);
+            }
+            if (Cfg::NBUF == 2) buf ^= 1;
+            if (buf == 0) tphase ^= 1;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();      // no CTA leaves while the other may still signal it or use its TMEM
+    tc_fence_after();
+    if (warp == ISSUER) tmem_dealloc_pair(tmem_base, tmem_cols);
+}
+
+template <int BN>
+cudaError_t launch_bs_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
+                           int pairs, cudaStream_t stream) {
+    using Cfg = PairCfg<BN>;
+    cudaError_t e = set_smem(gemm_bs_pair_kernel<BN>, pair_smem<BN>());
+    if (e != cudaSuccess) return e;
+    return launch_pdl_cluster(gemm_bs_pair_kernel<BN>, dim3(2 * pairs), Cfg::THREADS,
+                              pair_smem<BN>(), stream, 2, tmA, tmB, g);
+}
+
+template <int BN>
+int pair_clusters() {
+    if (set_smem(gemm_bs_pair_kernel<BN>, pair_smem<BN>()) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return max_active_clusters(reinterpret_cast<const void*>(gemm_bs_pair_kernel<BN>),
+                               PairCfg<BN>::THREADS, pair_smem<BN>(), 2);
+}
+
 // Stages and dynamic shared memory: with a stream-K workspace one partial tile (and its
 // barrier) is kept in shared memory, at two stages' cost.
 template <int BN>
@@ -587,12 +935,12 @@ int split_clusters_bs(int S) {
 }  // namespace
 
 // Tile width by rounds of tiles over the SMs times the measured time of one K block at that
-// width (~886 clk at 256, ~660 at 128 and about the same at 64, at prefill shapes; 192 taken
-// between them): wider tiles carry fewer operand bytes per MAC but leave more SMs idle when
-// tiles are few.
+// width (~886 clk at 256, ~660 at 128 at prefill shapes; 192 taken between them; 64, with its
+// two MMA issuers, 0.76 of 128 on the MLA kv projection): wider tiles carry fewer operand
+// bytes per MAC but leave more SMs idle when tiles are few.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
-    static const int kWidth[4] = {256, 192, 64, 128};   // on a tie the narrower of 64 and 128
-    static const int kCost[4] = {134, 117, 100, 100};
+    static const int kWidth[4] = {256, 192, 64, 128};
+    static const int kCost[4] = {134, 117, 76, 100};
     int best = 128;
     int64_t best_cost = INT64_MAX;
     for (int i = 0; i < 4; ++i) {
@@ -615,6 +963,25 @@ cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const
         case 192: return launch_bs<192>(tmA, tmB, g, gt, num_sms, ska, stream);
         case 256: return launch_bs<256>(tmA, tmB, g, gt, num_sms, ska, stream);
         default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t launch_gemm_bs_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                const GemmArgs& g, int BN, int pairs, cudaStream_t stream) {
+    switch (BN) {
+        case 128: return launch_bs_pair<128>(tmA, tmB, g, pairs, stream);
+        case 192: return launch_bs_pair<192>(tmA, tmB, g, pairs, stream);
+        case 256: return launch_bs_pair<256>(tmA, tmB, g, pairs, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int max_pair_clusters_bs(int BN) {
+    switch (BN) {
+        case 128: return pair_clusters<128>();
+        case 192: return pair_clusters<192>();
+        case 256: return pair_clusters<256>();
+        default: return 0;
     }
 }
 

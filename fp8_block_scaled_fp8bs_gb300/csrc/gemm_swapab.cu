@@ -68,10 +68,17 @@ __device__ __forceinline__ bool spin_until_at_least(const int* p, int target) {
     return true;
 }
 
-// Receive area of the split-K exchange (at the start of the stage memory, free once every CTA
-// of the cluster has finished its K loop): S slots of `wm` rows of C x 128 columns, fp32.
+// Split-K exchange: CTA q of the cluster adds up rows [q*wm, (q+1)*wm) of C, wm a multiple of
+// 4 (so that four consecutive rows travel as one float4); its receive area (at the start of the
+// stage memory, free once every CTA of the cluster has finished its K loop) holds S slots of
+// 128 columns x wm rows, column-major with a row pitch of p4 float4 (p4 odd: the float4 stores
+// of eight consecutive columns fall in distinct bank groups).
+__host__ __device__ constexpr int swap_rows_per_rank(int rows, int S) {
+    return ((rows + S - 1) / S + 3) / 4 * 4;
+}
+__host__ __device__ constexpr int swap_pitch4(int wm) { return (wm / 4) | 1; }
 __host__ __device__ constexpr int swap_recv_bytes(int MT, int S) {
-    return S * ((MT + S - 1) / S) * BM * 4;
+    return S * BM * swap_pitch4(swap_rows_per_rank(MT, S)) * 16;
 }
 
 template <int MT, bool FUSED>
@@ -156,6 +163,14 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 for (int i = 4 * lane; i < count; i += 4 * 32) cp_async_16(sRaw + i, as_rows + i);
             } else {
                 for (int i = lane; i < count; i += 32) cp_async_4(sRaw + i, as_rows + i);
+            }
+        } else if ((reinterpret_cast<uintptr_t>(as_rows) & 15) == 0 &&
+                   ((num_kb | kb_lo | nkb) & 3) == 0) {
+            // This CTA's K blocks of each row, 16 bytes at a time (every segment aligned).
+            for (int i = 4 * lane; i < scale_rows * nkb; i += 4 * 32) {
+                const int j = i / nkb;
+                cp_async_16(sRaw + i,
+                            as_rows + static_cast<int64_t>(j) * num_kb + kb_lo + i - j * nkb);
             }
         } else {
             // This CTA's K blocks of each row.
@@ -438,38 +453,49 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                         c[static_cast<int64_t>(m0 + j) * g.N + n] = __float2bfloat16_rn(acc[j]);
             }
         } else {
-            // Split K: row j of C (j < scale_rows) is added up by CTA j / wm of the cluster,
-            // which receives this CTA's partial of it in slot `rank` of its receive area
-            // ([slot][wm][128] fp32 at the start of the stage memory).
+            // Split K: rows j .. j+3 of C (j < scale_rows, j % 4 == 0) are added up by CTA
+            // j / wm of the cluster, which receives this CTA's partial of them as one float4
+            // in slot `rank` of its receive area (rows past M hold zeros).
             const int t = quarter * 32 + lane;
-            const int wm = (scale_rows + S - 1) / S;
+            const int wm = swap_rows_per_rank(scale_rows, S);
+            const int p4 = swap_pitch4(wm);
             const int rank = static_cast<int>(cluster_ctarank());
             const uint32_t recv = smem_addr(smem);
             cluster_sync();               // every CTA of the cluster is done with its stages
             if (ok) {
 #pragma unroll
-                for (int j = 0; j < MT; ++j) {
+                for (int j = 0; j < MT; j += 4) {
                     if (j < scale_rows) {
                         const int q = j / wm;
-                        const uint32_t off =
-                            static_cast<uint32_t>(((rank * wm + j - q * wm) * BM + t) * 4);
-                        st_shared_cluster_f32(mapa_shared(recv + off, static_cast<uint32_t>(q)),
-                                              acc[j]);
+                        const uint32_t off = static_cast<uint32_t>(
+                            ((rank * BM + t) * p4 + (j - q * wm) / 4) * 16);
+                        st_shared_cluster_f4(mapa_shared(recv + off, static_cast<uint32_t>(q)),
+                                             make_float4(acc[j], acc[j + 1], acc[j + 2],
+                                                         acc[j + 3]));
                     }
                 }
             }
             cluster_sync();               // every partial has landed
-            const float* rv = reinterpret_cast<const float*>(smem);
-            const int j_end = min(scale_rows, (rank + 1) * wm);
-            for (int j = rank * wm; ok && j < j_end; ++j) {
-                float v = 0.0f;
+            const float4* rv = reinterpret_cast<const float4*>(smem);
+            const int j0 = rank * wm;
+            const int j_end = min(scale_rows, j0 + wm);
+            for (int j = j0; ok && j < j_end; j += 4) {
+                float v[4];
                 for (int r = 0; r < S; ++r) {
-                    const float p = rv[(r * wm + j - rank * wm) * BM + t];
-                    v = r == 0 ? p : v + p;
+                    const float4 p = rv[(r * BM + t) * p4 + (j - j0) / 4];
+                    v[0] = r == 0 ? p.x : v[0] + p.x;
+                    v[1] = r == 0 ? p.y : v[1] + p.y;
+                    v[2] = r == 0 ? p.z : v[2] + p.z;
+                    v[3] = r == 0 ? p.w : v[3] + p.w;
                 }
-                if (n < g.N)
-                    static_cast<__nv_bfloat16*>(g.c)[static_cast<int64_t>(m0 + j) * g.N + n] =
-                        __float2bfloat16_rn(v);
+                if (n < g.N) {
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (j + i < j_end)
+                            static_cast<__nv_bfloat16*>(g.c)[static_cast<int64_t>(m0 + j + i) *
+                                                                 g.N + n] =
+                                __float2bfloat16_rn(v[i]);
+                }
             }
         }
     }
@@ -551,6 +577,24 @@ cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const Ge
 }
 
 }  // namespace
+
+template <int MT>
+bool check_swap(int K, int S) {
+    int st = 0, sm = 0;
+    const int num_kb = K / BK;
+    if (S < 1 || S > num_kb || !swap_smem<MT, false>((num_kb + S - 1) / S, &st, &sm)) return false;
+    return S == 1 || swap_recv_bytes(MT, S) <= st * SwapCfg<MT, false>::STAGE;
+}
+
+bool check_gemm_swapab(int MT, int K, int ksplit) {
+    switch (MT) {
+        case 16: return check_swap<16>(K, ksplit);
+        case 32: return check_swap<32>(K, ksplit);
+        case 64: return check_swap<64>(K, ksplit);
+        case 128: return check_swap<128>(K, ksplit);
+        default: return false;
+    }
+}
 
 int plan_gemm_swapab(int MT, bool fused, int M, int N, int K, int num_sms) {
     if (fused) {

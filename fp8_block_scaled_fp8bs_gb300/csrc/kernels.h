@@ -119,6 +119,14 @@ int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms);
 cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmArgs& g,
                            const GroupTable& gt, int BN, int num_sms, const StreamKArgs& ska,
                            cudaStream_t stream);
+// Block-scaled GEMM on CTA pairs (cta_group::2): tiles of 256 rows of A x BN (128, 192 or 256)
+// columns of B, each computed by a cluster of two CTAs; one group, whole tiles, `pairs`
+// clusters persistent over the tiles. tmA: box {128, 128} over A; tmB: box {128, BN/2} over B.
+// max_pair_clusters_bs: how many such clusters can be resident at once (0: query failed).
+cudaError_t launch_gemm_bs_pair(const CUtensorMap& tmA, const CUtensorMap& tmB,
+                                const GemmArgs& g, int BN, int pairs, cudaStream_t stream);
+int max_pair_clusters_bs(int BN);
+
 // The library's static stream-K workspace on the current device (no allocation); fails with
 // cudaErrorInvalidValue on a device with more SMs than it covers.
 cudaError_t bs_static_workspace(int num_sms, void** ws, size_t* bytes);
@@ -143,6 +151,8 @@ struct FusedQuant {
 // shared memory. plan_gemm_swapab gives the split for a problem (1: none; 0: this kernel cannot
 // take K, whose activation scales would not fit in shared memory).
 int plan_gemm_swapab(int MT, bool fused, int M, int N, int K, int num_sms);
+// Whether the quantised-input kernel can run with MT rows, this K and a split of ksplit.
+bool check_gemm_swapab(int MT, int K, int ksplit);
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
                                const GemmArgs& g, int MT, const FusedQuant& fq, int ksplit,
                                cudaStream_t stream);

@@ -135,6 +135,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
+// The same at cluster scope: for barriers that other CTAs of the cluster arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
+    const uint32_t a = smem_addr(bar);
+    if (mbar_try_wait_cluster(a, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait_cluster(a, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// Arrive on an mbarrier of any CTA of the cluster (address from mapa_shared).
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
 // ------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -204,6 +236,19 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
     return p;
 }
 
+// 2-D tiled load into this CTA's shared memory whose completion is counted on an mbarrier of
+// the CTA pair (address from mapa_shared): the loads of both CTAs of a cta_group::2 MMA complete
+// on the even CTA's barrier.
+__device__ __forceinline__ void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map,
+                                                 uint32_t bar_cluster_addr, int32_t c0,
+                                                 int32_t c1) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile"
+        ".mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_addr(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_cluster_addr), "r"(c0), "r"(c1)
+        : "memory");
+}
+
 // ------------------------------------------------------------------------- tcgen05
 
 // Allocate `ncols` TMEM columns (power of two, 32..512); the base address lands in *holder.
@@ -256,6 +301,49 @@ __device__ __forceinline__ void mma_f8_block_scaled(uint32_t d_tmem, uint64_t a_
         : "memory");
 }
 
+// ---- CTA pairs (cta_group::2): two CTAs of a cluster on neighbouring SMs compute one 256-row
+// MMA tile; each holds its 128 rows of A, half of B and its 128 rows of D (and the scale
+// factors for them) in its own shared memory and TMEM. The even CTA issues the MMAs.
+
+// TMEM allocation of the pair: one warp of each CTA executes it with the same count.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* holder, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(holder)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+// D (+)= (A * 2^sfa) * (B * 2^sfb)^T over the pair: M = 256 rows (128 per CTA), issued by the
+// even CTA; the same TMEM and shared-memory offsets in both CTAs.
+__device__ __forceinline__ void mma_f8_block_scaled_pair(uint32_t d_tmem, uint64_t a_desc,
+                                                         uint64_t b_desc, uint32_t idesc,
+                                                         uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on the mbarrier at this shared-memory offset in both CTAs of the pair when every
+// tcgen05 operation issued so far by this thread completes.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %1;" ::"r"(smem_addr(bar)),
+        "h"(static_cast<uint16_t>(0x3))
+        : "memory");
+}
+
 // Instruction descriptor for kind::mxf8f6f4 with block scaling: D = fp32, A = B = e4m3, both
 // K-major, ue8m0 scale factors (scale-factor byte selectors left at 0), shape M x N.
 __host__ __device__ constexpr uint32_t idesc_e4m3_block_scaled(uint32_t M, uint32_t N) {
@@ -273,6 +361,17 @@ __device__ __forceinline__ void tmem_st_4cols(uint32_t taddr, uint32_t w0, uint3
     asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
                  "r"(w0), "r"(w1), "r"(w2), "r"(w3)
                  : "memory");
+}
+
+// Write 16 consecutive 32-bit TMEM columns of the warp's 32 lanes (thread t: lane base + t).
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+        "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]),
+        "r"(v[15])
+        : "memory");
 }
 
 // Write 32 consecutive 32-bit TMEM columns of the warp's 32 lanes (thread t: lane base + t).

@@ -167,8 +167,9 @@ FP8BS_API int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, cons
  *
  *   M, N, K > 0 with K % 128 == 0; scale_fmt as in fp8bs_gemm.
  *   kernel   [out] FP8BS_KERNEL_SWAPPED (M <= 128: 128-row weight slabs on the MMA's M side),
- *                  FP8BS_KERNEL_PROMOTED (fp32 scales applied by CUDA cores per K block) or
- *                  FP8BS_KERNEL_BLOCK_SCALED (ue8m0 scales applied by the tensor cores).
+ *                  FP8BS_KERNEL_PROMOTED (fp32 scales applied by CUDA cores per K block),
+ *                  FP8BS_KERNEL_BLOCK_SCALED (ue8m0 scales applied by the tensor cores) or
+ *                  FP8BS_KERNEL_BLOCK_SCALED_PAIR (the same on pairs of SMs, 256-row tiles).
  *   tile     [out] rows of A per CTA (swapped) or columns of B per tile (otherwise).
  *   ksplit   [out] CTAs of one thread-block cluster that share each tile's K loop (1: none).
  *   stream_k [out] 1 if tiles share K loops through the workspace (stream-K), else 0.
@@ -176,8 +177,32 @@ FP8BS_API int fp8bs_gemm_ws(const void* a, const float* a_s, const void* b, cons
 #define FP8BS_KERNEL_SWAPPED 0
 #define FP8BS_KERNEL_PROMOTED 1
 #define FP8BS_KERNEL_BLOCK_SCALED 2
+#define FP8BS_KERNEL_BLOCK_SCALED_PAIR 3
 FP8BS_API int fp8bs_gemm_plan(int64_t M, int64_t N, int64_t K, int scale_fmt, int with_workspace,
                               int* kernel, int* tile, int* ksplit, int* stream_k);
+
+/*
+ * fp8bs_gemm_config -- fp8bs_gemm_ws with the launch configuration given by the caller, in the
+ * vocabulary of fp8bs_gemm_plan, instead of chosen from the shape: for callers that tune their
+ * own shapes (the pages' fp8_gemm autotunes over tile configurations, "DeepSeek-V3
+ * Administrator & Developer Guide", §6.5 and §8.5.3) and for tests that cover every kernel
+ * schedule. Results and accuracy as in fp8bs_gemm.
+ *
+ *   kernel  FP8BS_KERNEL_SWAPPED      tile = rows of A per CTA, 16, 32, 64 or 128, and >= M.
+ *           FP8BS_KERNEL_PROMOTED     tile = 64, 128, 192 or 256 columns (any scale_fmt).
+ *           FP8BS_KERNEL_BLOCK_SCALED tile = 64, 128, 192 or 256 (scale_fmt UE8M0).
+ *           FP8BS_KERNEL_BLOCK_SCALED_PAIR  tile = 128, 192 or 256 (UE8M0, ksplit 1).
+ *   ksplit  1: whole tiles; 2 .. 8 (and at most K/128): each tile's K loop split between that
+ *           many CTAs of a cluster; 0 (normal orientation only; tile 128 for BLOCK_SCALED):
+ *           stream-K over `workspace`, which is then required, for shapes with at least as
+ *           many tiles as SMs.
+ *   Other arguments as in fp8bs_gemm_ws. A configuration the kernels do not support for the
+ *   shape returns FP8BS_ERR_INVALID_ARG and launches nothing.
+ */
+FP8BS_API int fp8bs_gemm_config(const void* a, const float* a_s, const void* b, const float* b_s,
+                                void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
+                                unsigned int flags, int kernel, int tile, int ksplit,
+                                void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * fp8bs_gemm_workspace_size -- bytes of workspace fp8bs_gemm_ws uses on the current device: the

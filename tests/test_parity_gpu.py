@@ -15,7 +15,7 @@ import fp8_block_scaled_fp8bs_gb300 as fp8bs
 import oracle
 import synth
 from parity_util import (assert_gemm_close, dev_bf16, dev_e4m3, dev_f32, host_bf16_bits,
-                         host_bf16_f64, host_codes, tile_samples)
+                         host_bf16_f64, host_codes, lines_and_tiles)
 
 pytestmark = pytest.mark.gpu
 
@@ -229,16 +229,15 @@ def pipeline_check(x_bits, b, b_s, fmt, what, per_tile=2, weights_constant=False
     y, s = fp8bs.act_quant(xt, fmt)          # the GEMM may start while this one finishes
     c = fp8bs.fp8_gemm(y, s, bt, bst, fmt, weights_constant=weights_constant)
     torch.cuda.synchronize()
-    mi, ni = tile_samples(M, N, per_tile, seed=M + N)
+    mi, ni = lines_and_tiles(M, N, per_tile, seed=M + N)
     rows = np.unique(mi)
     a_ref, as_ref = oracle.act_quant(x_bits[rows], FMTS[fmt])
     assert_quant_equal(host_codes(y)[rows], s.cpu().numpy()[rows], a_ref, as_ref, what)
     # the oracle's GEMM on its own codes of the sampled rows
-    row_of = {r: i for i, r in enumerate(rows)}
-    local = np.array([row_of[m] for m in mi], dtype=np.int64)
+    local = np.searchsorted(rows, mi).astype(np.int64)
     ref = oracle.gemm_at(a_ref, as_ref, b, b_s, local, ni)
     got = host_bf16_f64(c[torch.from_numpy(mi).cuda(), torch.from_numpy(ni).cuda()])
-    return assert_gemm_close(got, ref, what)
+    return assert_gemm_close(got, ref, what, c_full=c)
 
 
 @pytest.mark.parametrize("weights_constant", [False, True])
@@ -311,14 +310,13 @@ def test_moe_experts_full_size():
         if hi == lo:
             continue
         b, b_s = weights[e]
-        mi, ni = tile_samples(hi - lo, synth.MOE_INTER, 1, seed=e)
+        mi, ni = lines_and_tiles(hi - lo, synth.MOE_INTER, 1, seed=e, n_rows=1, n_cols=1)
         rows_e = np.unique(mi)
         a_ref, as_ref = oracle.act_quant(x[lo + rows_e])
         assert_quant_equal(y_h[lo + rows_e], s_h[lo + rows_e], a_ref, as_ref, f"expert {e}")
-        row_of = {r: i for i, r in enumerate(rows_e)}
-        ref = oracle.gemm_at(a_ref, as_ref, b, b_s, np.array([row_of[m] for m in mi]), ni)
+        ref = oracle.gemm_at(a_ref, as_ref, b, b_s, np.searchsorted(rows_e, mi), ni)
         got = host_bf16_f64(outs[e])[mi, ni]
-        assert_gemm_close(got, ref, f"expert {e} (M_e={hi - lo})")
+        assert_gemm_close(got, ref, f"expert {e} (M_e={hi - lo})", c_full=outs[e])
 
 
 def grouped_check(counts, N, K, seed, what, per_tile=None, fmt="fp32"):
@@ -334,9 +332,10 @@ def grouped_check(counts, N, K, seed, what, per_tile=None, fmt="fp32"):
           for e in range(len(counts))]
     b = np.stack([w for w, _ in ws])
     b_s = np.stack([s for _, s in ws])
-    c = fp8bs.fp8_gemm_grouped(dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), offs, fmt)
+    c_dev = fp8bs.fp8_gemm_grouped(dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), offs,
+                                   fmt)
     torch.cuda.synchronize()
-    c = host_bf16_f64(c)
+    c = host_bf16_f64(c_dev)
     for e in range(len(counts)):
         lo, hi = offs[e], offs[e + 1]
         if hi == lo:
@@ -345,9 +344,9 @@ def grouped_check(counts, N, K, seed, what, per_tile=None, fmt="fp32"):
             ref = oracle.gemm(a[lo:hi], a_s[lo:hi], b[e], b_s[e])
             assert_gemm_close(c[lo:hi], ref, f"{what} group {e}")
         else:
-            mi, ni = tile_samples(hi - lo, N, per_tile, seed=e)
+            mi, ni = lines_and_tiles(hi - lo, N, per_tile, seed=e, n_rows=1, n_cols=1)
             ref = oracle.gemm_at(a[lo:hi], a_s[lo:hi], b[e], b_s[e], mi, ni)
-            assert_gemm_close(c[lo:hi][mi, ni], ref, f"{what} group {e}")
+            assert_gemm_close(c[lo:hi][mi, ni], ref, f"{what} group {e}", c_full=c[lo:hi])
 
 
 @pytest.mark.parametrize("counts,N,K", [
@@ -432,9 +431,9 @@ def test_gemm_ue8m0_per_row_and_block_exponents(M, N, K):
     if M * N <= 384 * 384:
         assert_gemm_close(c, oracle.gemm(a, a_s, b, b_s), "ue8m0 exponent pattern")
     else:
-        mi, ni = tile_samples(M, N, 2, seed=K)
+        mi, ni = lines_and_tiles(M, N, 2, seed=K)
         assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni),
-                          "ue8m0 exponent pattern (sampled)")
+                          "ue8m0 exponent pattern (sampled)", c_full=c)
 
 
 def test_gemm_ue8m0_extreme_exponents():
@@ -467,8 +466,22 @@ def test_gemm_grouped_ue8m0_block_scaled(counts, N, K):
 
 
 def run_gemm_ws(a_codes, a_s, b_codes, b_s, ws, fmt="ue8m0"):
-    c = fp8bs.fp8_gemm(dev_e4m3(a_codes), dev_f32(a_s), dev_e4m3(b_codes), dev_f32(b_s), fmt,
-                       workspace=ws)
+    """With a workspace and at least as many 128 x 128 tiles as SMs: the block-scaled kernel's
+    stream-K schedule, selected explicitly (the automatic plan prefers wider whole tiles for
+    these shapes); otherwise the automatic plan."""
+    M, K = a_codes.shape
+    N = b_codes.shape[0]
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    if ws is not None and fmt == "ue8m0" and -(-M // 128) * -(-N // 128) >= sms:
+        c = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        A, AS, B, BS = dev_e4m3(a_codes), dev_f32(a_s), dev_e4m3(b_codes), dev_f32(b_s)
+        fp8bs.fp8bs_gemm_config(A.data_ptr(), AS.data_ptr(), B.data_ptr(), BS.data_ptr(),
+                                c.data_ptr(), M, N, K, fp8bs.SCALE_UE8M0, 0,
+                                fp8bs.KERNEL_BLOCK_SCALED, 128, 0, ws.data_ptr(), ws.numel(),
+                                torch.cuda.current_stream().cuda_stream)
+    else:
+        c = fp8bs.fp8_gemm(dev_e4m3(a_codes), dev_f32(a_s), dev_e4m3(b_codes), dev_f32(b_s),
+                           fmt, workspace=ws)
     torch.cuda.synchronize()
     return host_bf16_f64(c)
 
@@ -495,10 +508,10 @@ def test_gemm_ue8m0_stream_k_against_oracle(M, N, K, full):
         assert_gemm_close(c1, ref, f"stream-K {M}x{N}x{K}")
         assert_gemm_close(c0, ref, f"no workspace {M}x{N}x{K}")
     else:
-        mi, ni = tile_samples(M, N, 1, seed=M + N)
+        mi, ni = lines_and_tiles(M, N, 1, seed=M + N)
         ref = oracle.gemm_at(a, a_s, b, b_s, mi, ni)
-        assert_gemm_close(c1[mi, ni], ref, f"stream-K {M}x{N}x{K}")
-        assert_gemm_close(c0[mi, ni], ref, f"no workspace {M}x{N}x{K}")
+        assert_gemm_close(c1[mi, ni], ref, f"stream-K {M}x{N}x{K}", c_full=c1)
+        assert_gemm_close(c0[mi, ni], ref, f"no workspace {M}x{N}x{K}", c_full=c0)
 
 
 def test_gemm_ue8m0_stream_k_after_whole_tiles():
@@ -507,8 +520,9 @@ def test_gemm_ue8m0_stream_k_after_whole_tiles():
     a, a_s, b, b_s = pow2_case(M, N, K, 23)
     ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
     c = run_gemm_ws(a, a_s, b, b_s, ws)
-    mi, ni = tile_samples(M, N, 2, seed=5)
-    assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni), "ue8m0 hybrid stream-K")
+    mi, ni = lines_and_tiles(M, N, 2, seed=5)
+    assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni), "ue8m0 hybrid stream-K",
+                      c_full=c)
 
 
 def test_gemm_ue8m0_stream_k_workspace_reused_across_shapes():
@@ -569,9 +583,9 @@ def test_act_quant_gemm_matches_separate_calls(fmt, M, N, K):
     # and against the oracle on the codes it produced itself
     a_ref, as_ref = oracle.act_quant(x, FMTS[fmt])
     assert_quant_equal(host_codes(y1), s1.cpu().numpy(), a_ref, as_ref, f"aqg {M}x{K}")
-    mi, ni = tile_samples(M, N, 2, seed=K)
+    mi, ni = lines_and_tiles(M, N, 2, seed=K)
     ref = oracle.gemm_at(a_ref, as_ref, b, b_s, mi, ni)
-    assert_gemm_close(host_bf16_f64(c1)[mi, ni], ref, f"aqg {M}x{N}x{K}")
+    assert_gemm_close(host_bf16_f64(c1)[mi, ni], ref, f"aqg {M}x{N}x{K}", c_full=c1)
 
 
 def test_act_quant_gemm_without_workspace():

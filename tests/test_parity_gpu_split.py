@@ -16,7 +16,7 @@ import torch
 import fp8_block_scaled_fp8bs_gb300 as fp8bs
 import oracle
 import synth
-from parity_util import (assert_gemm_close, dev_e4m3, dev_f32, host_bf16_f64, tile_samples)
+from parity_util import assert_gemm_close, dev_e4m3, dev_f32, host_bf16_f64, lines_and_tiles
 
 pytestmark = pytest.mark.gpu
 
@@ -54,18 +54,6 @@ def check_plan(M, N, K, fmt, kernel, tile=None, min_split=2):
         assert p["tile"] == tile, p
     assert p["ksplit"] >= min_split, p
     return p
-
-
-def rows_cols_and_tiles(M, N, seed, n_rows=2, n_cols=2):
-    """Whole rows and whole columns (first, last and random ones) plus samples in every tile."""
-    rng = np.random.default_rng(seed)
-    rows = np.unique(np.r_[0, M - 1, rng.integers(0, M, n_rows)])
-    cols = np.unique(np.r_[0, N - 1, rng.integers(0, N, n_cols)])
-    mi = [np.repeat(rows, N), np.tile(np.arange(N), len(rows))]
-    ni = [np.repeat(np.arange(M), len(cols)), np.tile(cols, M)]
-    tm, tn = tile_samples(M, N, 2, seed=seed)
-    return (np.concatenate([mi[0], ni[0], tm]).astype(np.int64),
-            np.concatenate([mi[1], ni[1], tn]).astype(np.int64))
 
 
 # ------------------------------------------------------------------ decode orientation (M <= 128)
@@ -125,10 +113,10 @@ def test_decode_without_split_unchanged_at_full_width():
 
 @pytest.mark.parametrize("M,N,K", [
     (300, 2048, 7168),     # one MoE expert's rows: 24 tiles 256 wide on 152 SMs
-    (129, 2048, 2048),     # two row tiles, the second one row high
-    (513, 1000, 1024),     # ragged columns
+    (129, 2048, 4096),     # two row tiles, the second one row high
+    (257, 1000, 4096),     # ragged columns, three row tiles
     (200, 97, 4096),       # one tile narrower than the narrowest width
-    (640, 1536, 4096),     # 30 tiles 256 wide
+    (300, 1536, 4096),
 ])
 def test_fp32_split_k_full_compare(M, N, K):
     check_plan(M, N, K, "fp32", "promoted")
@@ -139,9 +127,9 @@ def test_fp32_split_k_full_compare(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [
-    (2048, 576, 7168),     # the MLA kv projection: 48 tiles 192 wide, three CTAs each
+    (512, 576, 7168),      # twelve 192-wide tiles, eight CTAs each
     (300, 576, 2048),
-    (129, 1000, 1024),
+    (129, 1000, 4096),
     (1000, 64, 4096),      # eight 64-wide tiles (two MMA issuers per CTA)
 ])
 def test_ue8m0_split_k_full_compare(M, N, K):
@@ -152,14 +140,15 @@ def test_ue8m0_split_k_full_compare(M, N, K):
     assert_gemm_close(host_bf16_f64(c1), oracle.gemm(a, a_s, b, b_s), f"ue8m0 split {M}x{N}x{K}")
 
 
-def test_mla_kv_projection_uses_192_wide_split_tiles():
-    """The ue8m0 MLA kv projection (M=2048, N=576, K=7168) with and without a workspace: 192-wide
-    tiles (576 = 3 x 192), each shared by the CTAs of a cluster (as many as the device can
-    place for all 48 tiles at once)."""
+def test_mla_projection_plans():
+    """The ue8m0 MLA projections (M=2048, K=7168) fill the SMs with whole tiles, with or without
+    a workspace: the kv projection (N=576) as 144 tiles 64 wide, the q projection (N=1536) as
+    128 tiles 192 wide (1536 = 8 x 192)."""
     for ws in (False, True):
-        p = fp8bs.fp8bs_gemm_plan(2048, 576, synth.DIM, fp8bs.SCALE_UE8M0, ws)
-        assert p["kernel"] == fp8bs.KERNEL_BLOCK_SCALED and p["tile"] == 192, p
-        assert p["ksplit"] >= 2 and not p["stream_k"], p
+        for N, tile in ((576, 64), (1536, 192)):
+            p = fp8bs.fp8bs_gemm_plan(2048, N, synth.DIM, fp8bs.SCALE_UE8M0, ws)
+            assert p == {"kernel": fp8bs.KERNEL_BLOCK_SCALED, "tile": tile, "ksplit": 1,
+                         "stream_k": False}, (N, ws, p)
 
 
 def random_codes(rng, rows, cols):
@@ -169,8 +158,9 @@ def random_codes(rng, rows, cols):
 
 
 @pytest.mark.parametrize("M,N,K,split", [
-    (2048, 576, 2048, True),     # 192-wide tiles at n0 = 0, 192, 384, split K
+    (512, 576, 7168, True),      # 192-wide tiles at n0 = 0, 192, 384, split K
     (2048, 1536, 640, False),    # 192-wide whole tiles at every n0 up to 1344
+    (2560, 1152, 768, False),
 ])
 def test_ue8m0_192_wide_tiles_per_row_and_block_exponents(M, N, K, split):
     """Every row of A and every 128-row block of B carries its own exponent in every K block. A
@@ -200,6 +190,8 @@ def test_mla_full_size_rows_and_columns(N):
     a, a_s = oracle.act_quant(x, oracle.SCALE_UE8M0)
     b, b_s = synth.weights(N, K, seed=0, name=f"mla/B{N}", pow2=True)
     ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
-    c = host_bf16_f64(run(a, a_s, b, b_s, "ue8m0", workspace=ws))
-    mi, ni = rows_cols_and_tiles(M, N, seed=N)
-    assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni), f"MLA N={N}")
+    c_dev = run(a, a_s, b, b_s, "ue8m0", workspace=ws)
+    c = host_bf16_f64(c_dev)
+    mi, ni = lines_and_tiles(M, N, 2, seed=N)
+    assert_gemm_close(c[mi, ni], oracle.gemm_at(a, a_s, b, b_s, mi, ni), f"MLA N={N}",
+                      c_full=c_dev)
