@@ -46,7 +46,8 @@ EXPORTS = ("fp8bs_act_quant", "fp8bs_weight_dequant", "fp8bs_gemm", "fp8bs_gemm_
            "fp8bs_gemm_noalloc",
            "fp8bs_act_quant_gemm", "fp8bs_linear_bf16",
            "fp8bs_gemm_grouped",
-           "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout")
+           "fp8bs_status_string", "fp8bs_device_error", "fp8bs_probe_wait_timeout",
+           "fp8bs_probe_occupy")
 
 _lock = threading.Lock()
 _lib = None
@@ -92,6 +93,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
         lib.fp8bs_status_string.restype = ctypes.c_char_p
         lib.fp8bs_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint), i32, vp]
         lib.fp8bs_probe_wait_timeout.argtypes = [ctypes.c_uint64, vp]
+        lib.fp8bs_probe_occupy.argtypes = [i32, ctypes.c_uint64, vp]
         for name in EXPORTS:
             getattr(lib, name).restype = getattr(lib, name).restype or i32
         lib.fp8bs_status_string.restype = ctypes.c_char_p
@@ -185,6 +187,10 @@ def fp8bs_device_error(clear: bool = True, stream=0) -> int:
 
 def fp8bs_probe_wait_timeout(timeout_ns: int, stream=0) -> None:
     _check("fp8bs_probe_wait_timeout", load().fp8bs_probe_wait_timeout(timeout_ns, stream))
+
+
+def fp8bs_probe_occupy(ctas: int, duration_ns: int, stream=0) -> None:
+    _check("fp8bs_probe_occupy", load().fp8bs_probe_occupy(ctas, duration_ns, stream))
 
 
 # ----------------------------------------------------------------------- tensor helpers

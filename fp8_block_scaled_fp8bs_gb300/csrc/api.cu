@@ -679,6 +679,15 @@ int fp8bs_device_error(unsigned int* out, int clear, void* stream) {
     return status_of(fp8bs::read_device_error(out, clear != 0, static_cast<cudaStream_t>(stream)));
 }
 
+int fp8bs_probe_occupy(int ctas, uint64_t duration_ns, void* stream) {
+    if (ctas < 1 || ctas > 1024) return FP8BS_ERR_INVALID_ARG;
+    if (duration_ns > 5000000000ull) duration_ns = 5000000000ull;
+    int sms = 0;
+    if (int st = check_device(&sms)) return st;
+    return status_of(fp8bs::launch_probe_occupy(ctas, duration_ns,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 int fp8bs_probe_wait_timeout(uint64_t timeout_ns, void* stream) {
     if (timeout_ns < 1000000ull) timeout_ns = 1000000ull;
     if (timeout_ns > 2000000000ull) timeout_ns = 2000000000ull;

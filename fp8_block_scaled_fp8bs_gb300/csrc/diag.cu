@@ -16,7 +16,27 @@ __global__ void probe_wait_kernel(uint64_t timeout_ns) {
     }
 }
 
+// Holds its SM (it claims most of the SM's shared memory) until duration_ns have passed.
+__global__ void probe_occupy_kernel(uint64_t duration_ns) {
+    extern __shared__ uint8_t held[];
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        volatile uint8_t* p = held;
+        while (global_timer_ns() - t0 < duration_ns) p[0] = 1;
+    }
+}
+
+constexpr int kOccupySmem = 200 * 1024;
+
 }  // namespace
+
+cudaError_t launch_probe_occupy(int ctas, uint64_t duration_ns, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(probe_occupy_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kOccupySmem);
+    if (e != cudaSuccess) return e;
+    probe_occupy_kernel<<<ctas, 32, kOccupySmem, stream>>>(duration_ns);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream) {
     probe_wait_kernel<<<1, 32, 0, stream>>>(timeout_ns);

@@ -866,7 +866,7 @@ cudaError_t launch_bs_pair(const CUtensorMap& tmA, const CUtensorMap& tmB, const
     cudaError_t e = set_smem(gemm_bs_pair_kernel<BN>, pair_smem<BN>());
     if (e != cudaSuccess) return e;
     return launch_pdl_cluster(gemm_bs_pair_kernel<BN>, dim3(2 * pairs), Cfg::THREADS,
-                              pair_smem<BN>(), stream, 2, tmA, tmB, g);
+                              pair_smem<BN>(), stream, 2, false, tmA, tmB, g);
 }
 
 template <int BN>
@@ -916,8 +916,16 @@ cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     if (tiles == 0) return cudaSuccess;
     StreamK sk = {nullptr, nullptr, 0, 1};
     const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
-    return launch_pdl_cluster(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
-                              tmA, tmB, g, gt, stages, sk);
+    e = launch_pdl_cluster(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
+                           stream_k, tmA, tmB, g, gt, stages, sk);
+    if (e == cudaSuccess || !stream_k) return e;
+    // The runtime could not place every CTA of the stream-K grid at once (fewer SMs available
+    // to this context than the plan assumed): whole tiles instead, which need no co-residency.
+    cudaGetLastError();
+    const StreamK whole = {nullptr, nullptr, 0, 1};
+    return launch_pdl_cluster(gemm_bs_kernel<BN>, tiles < num_sms ? tiles : num_sms,
+                              Cfg::THREADS, bs_smem<BN>(false), stream, 1, false, tmA, tmB, g,
+                              gt, bs_stages<BN>(false), whole);
 }
 
 template <int BN>

@@ -572,8 +572,8 @@ cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const Ge
         return cudaErrorInvalidValue;
     if (S > 1 && swap_recv_bytes(MT, S) > stages * Cfg::STAGE) return cudaErrorInvalidValue;
     const dim3 grid(((g.N + BM - 1) / BM) * S, (g.M + MT - 1) / MT);
-    return launch_pdl_cluster(kernel, grid, Cfg::THREADS, smem, stream, S, tmB, tmA, g, stages,
-                              fq, S);
+    return launch_pdl_cluster(kernel, grid, Cfg::THREADS, smem, stream, S, false, tmB, tmA, g,
+                              stages, fq, S);
 }
 
 }  // namespace

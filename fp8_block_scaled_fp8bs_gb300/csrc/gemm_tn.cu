@@ -420,8 +420,17 @@ cudaError_t launch_tn(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     if (tiles == 0) return cudaSuccess;
     StreamK sk = {nullptr, nullptr, 0, 1};
     const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
-    return launch_pdl_cluster(gemm_tn_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
-                              tmA, tmB, g, gt, stages, sk);
+    const bool stream_k = sk.parts != nullptr;
+    e = launch_pdl_cluster(gemm_tn_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
+                           stream_k, tmA, tmB, g, gt, stages, sk);
+    if (e == cudaSuccess || !stream_k) return e;
+    // The runtime could not place every CTA of the stream-K grid at once (fewer SMs available
+    // to this context than the plan assumed): whole tiles instead, which need no co-residency.
+    cudaGetLastError();
+    const StreamK whole = {nullptr, nullptr, 0, 1};
+    return launch_pdl_cluster(gemm_tn_kernel<BN>, tiles < num_sms ? tiles : num_sms,
+                              Cfg::THREADS, smem, stream, 1, false, tmA, tmB, g, gt, stages,
+                              whole);
 }
 
 template <int BN>

@@ -12,31 +12,42 @@ namespace fp8bs {
 // Launch with programmatic stream serialisation (see grid_dependency_wait in ptx.cuh): the
 // launch may begin while the previous kernel on the stream is finishing.
 // With cluster_x > 1 the grid is launched as clusters of cluster_x consecutive CTAs along x
-// (grid.x must be a multiple of it).
+// (grid.x must be a multiple of it). With `cooperative` the launch is a cooperative one: the
+// runtime places every CTA of the grid at once (or refuses the launch), which the stream-K
+// schedule relies on -- a tile's owner waits for partials from CTAs with larger indices.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                               cudaStream_t stream, int cluster_x, Args&&... args) {
+                               cudaStream_t stream, int cluster_x, bool cooperative,
+                               Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = static_cast<unsigned>(cluster_x);
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
+    cudaLaunchAttribute attr[3];
+    int n = 0;
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n++].val.programmaticStreamSerializationAllowed = 1;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attr[n].val.clusterDim.y = 1;
+        attr[n++].val.clusterDim.z = 1;
+    }
+    if (cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n++].val.cooperative = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = cluster_x > 1 ? 2 : 1;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                        cudaStream_t stream, Args&&... args) {
-    return launch_pdl_cluster(kernel, grid, block, smem, stream, 1, static_cast<Args&&>(args)...);
+    return launch_pdl_cluster(kernel, grid, block, smem, stream, 1, false,
+                              static_cast<Args&&>(args)...);
 }
 
 // Split K inside a cluster: at most this many CTAs share a tile (the portable cluster size).
@@ -166,6 +177,10 @@ cudaError_t launch_linear_bf16_swap(const CUtensorMap& tmW, const CUtensorMap& t
 
 // Diagnostic kernel: one wait on a barrier nothing signals (see fp8bs_probe_wait_timeout).
 cudaError_t launch_probe_wait(uint64_t timeout_ns, cudaStream_t stream);
+
+// Diagnostic kernel: `ctas` CTAs that each take a whole SM (most of its shared memory) and
+// return after `duration_ns` (see fp8bs_probe_occupy).
+cudaError_t launch_probe_occupy(int ctas, uint64_t duration_ns, cudaStream_t stream);
 
 // The device error word of the library (read/clear; synchronises `stream`): the OR of the
 // words of the kernel files, each read (and cleared) by its own function below.

@@ -137,12 +137,15 @@ FP8BS_API int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, cons
 
 /*
  * fp8bs_gemm_ws -- fp8bs_gemm_ex with a device workspace, which lets the library share the K
- * loop of an output tile between SMs (stream-K) when whole tiles would leave SMs idle. Used
- * for FP8BS_SCALE_UE8M0 with M > 128 (the block-scaled MMA) when the tiles do not fill the
- * SMs evenly, e.g. the MLA projections M=2048, K=7168, N=1536 or 576; otherwise the call runs
- * as fp8bs_gemm_ex. The partial sums of a shared tile are added in K order, so results do not
- * depend on timing. ("DeepSeek-V3 Administrator & Developer Guide", §8.5.3, computed as in
- * fp8bs_gemm; the pages' kernel has no split of K.)
+ * loop of an output tile between SMs (stream-K) when the tiles do not fill the SMs evenly
+ * (M > 128, at least as many tiles as SMs, e.g. the prefill up-projection with fp32 scales);
+ * otherwise the call runs as fp8bs_gemm_ex. The partial sums of a shared tile are added in a
+ * fixed order, so results do not depend on timing. A stream-K grid is launched cooperatively
+ * (the runtime places all its CTAs at once); where the runtime cannot, the call computes whole
+ * tiles instead. ("DeepSeek-V3 Administrator & Developer Guide", §8.5.3, computed as in
+ * fp8bs_gemm; the pages' kernel has no split of K.) Every call, with or without a workspace,
+ * may also split a tile's K loop between the CTAs of a thread-block cluster when the tiles are
+ * few (fp8bs_gemm_plan shows the choice); that needs no workspace.
  *
  *   workspace        device memory of at least fp8bs_gemm_workspace_size bytes, 16-byte
  *                    aligned, owned by the caller. It must hold zeros before its first use;
@@ -333,6 +336,15 @@ FP8BS_API int fp8bs_device_error(unsigned int* out, int clear, void* stream);
  * fp8bs_device_error.
  */
 FP8BS_API int fp8bs_probe_wait_timeout(uint64_t timeout_ns, void* stream);
+
+/*
+ * fp8bs_probe_occupy -- diagnostic: launch `ctas` (1 .. 1024) CTAs that each hold one SM (they
+ * claim most of its shared memory) and return after duration_ns (at most 5 s). Enqueued only.
+ * With it a caller can run a GEMM while another stream holds some of the SMs: a stream-K
+ * launch (fp8bs_gemm_ws) is a cooperative launch whose CTAs the runtime places all at once, so
+ * its tiles' owners never wait on contributors that have no SM.
+ */
+FP8BS_API int fp8bs_probe_occupy(int ctas, uint64_t duration_ns, void* stream);
 
 #ifdef __cplusplus
 }

@@ -682,3 +682,36 @@ def test_bounded_wait_reports_instead_of_hanging():
     a, a_s = oracle.act_quant(t["x"])
     b, b_s = t["b"]
     assert_gemm_close(run_gemm(a, a_s, b, b_s), oracle.gemm(a, a_s, b, b_s), "after probe")
+
+
+def test_stream_k_while_another_stream_holds_sms():
+    """A stream-K GEMM launched while a kernel on another stream holds half the SMs for longer
+    than any wait inside the library may last (2.2 s against 2 s): the stream-K grid is a
+    cooperative launch, so its CTAs are placed together once the SMs are free, and no tile's
+    owner waits on a contributor that has no SM. C is bit-identical to an uncontended call and
+    no wait runs out."""
+    M, N, K = 2560, 2304, 1024          # 220 tiles 192 wide, all shared (fp32 scales)
+    assert fp8bs.fp8bs_gemm_plan(M, N, K, fp8bs.SCALE_FP32, True)["stream_k"]
+    x = synth.activations(M, K, seed=31, name="occA", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x)
+    b, b_s = synth.weights(N, K, seed=32, name="occB")
+    A, AS, B, BS = dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s)
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda")
+    ref = fp8bs.fp8_gemm(A, AS, B, BS, "fp32", workspace=ws)
+    whole = torch.empty_like(ref)
+    fp8bs.fp8bs_gemm_config(A.data_ptr(), AS.data_ptr(), B.data_ptr(), BS.data_ptr(),
+                            whole.data_ptr(), M, N, K, fp8bs.SCALE_FP32, 0,
+                            fp8bs.KERNEL_PROMOTED, 192, 1, 0, 0,
+                            torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    # the shared tiles add their partials in another order than whole tiles: the reference
+    # really ran the stream-K schedule
+    assert not torch.equal(whole.view(torch.int16), ref.view(torch.int16))
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    other = torch.cuda.Stream()
+    fp8bs.fp8bs_probe_occupy(sms // 2, 2_200_000_000, other.cuda_stream)
+    c = fp8bs.fp8_gemm(A, AS, B, BS, "fp32", workspace=ws)
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_error(clear=False) == 0
+    assert torch.equal(c.view(torch.int16), ref.view(torch.int16))
+    assert_gemm_close(host_bf16_f64(c), oracle.gemm(a, a_s, b, b_s), "stream-K under contention")
