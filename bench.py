@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # kernel (gemm_swapab_kernel), from ncu captures of its M=1 and M=64 launches (their mean),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "380089e60e1f3fad", "per_launch_mb": (134.90 + 135.37) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "40cac2d4a873b553", "per_launch_mb": (135.03 + 135.39) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -789,6 +789,12 @@ def run_profile(case: str, launches: int, warmup: int):
         c = torch.empty((2048, N), dtype=torch.bfloat16, device="cuda")
         g.act_quant(x, y, s, 2048, K_DIM, 1)
         fn = lambda: g.gemm_ws(y, s, B, S, c, 2048, N, K_DIM, 1)  # noqa: E731
+    elif case == "act_quant_mla":
+        # the ue8m0 MLA input, 2048 x 7168
+        x = g.bf16(synth.mla_acts())
+        y = torch.empty((2048, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((2048, K_DIM // 128), dtype=torch.float32, device="cuda")
+        fn = lambda: g.act_quant(x, y, s, 2048, K_DIM, 1)  # noqa: E731
     elif case == "act_quant":
         rows, _ = synth.moe_routing(0)
         x = g.bf16(synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows])
@@ -879,7 +885,7 @@ def main(argv=None):
                     help="where the per-rank clock samples (clocks_rank<r>.csv) are written")
     ap.add_argument("--profile", metavar="CASE", default=None,
                     help="run one kernel only (decode1..decode64, expert1..expert64, down1..down64, prefill_up, prefill_down, prefill_up_ue8m0, mla1536, mla576, linear1..linear4096, "
-                         "act_quant, dequant, moe): warmup + steps launches, for ncu")
+                         "act_quant, act_quant_mla, dequant, moe): warmup + steps launches, for ncu")
     args = ap.parse_args(argv)
     if args.warmup < 3 and not args.profile:
         ap.error("--warmup must be at least 3")
