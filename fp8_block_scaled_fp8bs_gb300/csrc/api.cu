@@ -261,8 +261,8 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, bool block_scaled, void* wor
         // Few rows of A (decode): weights on the MMA's M side, one 128-row slab per CTA (or
         // per cluster, with the K loop split).
         const int MT = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
-        const int S = fp8bs::plan_gemm_swapab(MT, false, static_cast<int>(M), static_cast<int>(N),
-                                              static_cast<int>(K), sms);
+        const int S = fp8bs::plan_gemm_swapab(MT, false, static_cast<int>((M + MT - 1) / MT),
+                                              static_cast<int>(N), static_cast<int>(K), sms);
         if (S > 0) {
             p.kind = FP8BS_KERNEL_SWAPPED;
             p.tile = MT;
@@ -404,8 +404,11 @@ int gemm_impl(const void* a, const float* a_s, const void* b, const float* b_s, 
     if (p.kind == FP8BS_KERNEL_SWAPPED) {
         if (!make_map(&tmB, b, N, K, 128) || !make_map(&tmA, a, M, K, p.tile))
             return FP8BS_ERR_CUDA;
-        return status_of(
-            fp8bs::launch_gemm_swapab(tmB, tmA, g, p.tile, fp8bs::FusedQuant{}, p.ksplit, st));
+        const int64_t rows[2] = {0, M};
+        fp8bs::GroupTable gt;
+        fp8bs::fill_row_tiles(&gt, rows, 1, p.tile);
+        return status_of(fp8bs::launch_gemm_swapab(tmB, tmA, g, gt, p.tile, fp8bs::FusedQuant{},
+                                                   p.ksplit, false, st));
     }
     if (p.kind == FP8BS_KERNEL_BLOCK_SCALED_PAIR) {
         if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N, K, p.tile / 2))
@@ -529,12 +532,16 @@ int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b, const 
         fq.ue8m0 = ue8m0 ? 1 : 0;
         // Only where the separate GEMM would not split its K loop either: the one kernel
         // promotes every K block in order, and C must equal that of the separate calls.
-        if (fp8bs::plan_gemm_swapab(MT, false, g.M, g.N, g.K, sms) == 1 &&
-            fp8bs::plan_gemm_swapab(MT, true, g.M, g.N, g.K, sms) == 1) {
+        const int row_tiles = (g.M + MT - 1) / MT;
+        if (fp8bs::plan_gemm_swapab(MT, false, row_tiles, g.N, g.K, sms) == 1 &&
+            fp8bs::plan_gemm_swapab(MT, true, row_tiles, g.N, g.K, sms) == 1) {
             CUtensorMap tmA, tmB;
             if (!make_map(&tmB, b, N, K, 128) || !make_map_bf16(&tmA, x, M, K, MT))
                 return FP8BS_ERR_CUDA;
-            return status_of(fp8bs::launch_gemm_swapab(tmB, tmA, g, MT, fq, 1, st));
+            const int64_t rows[2] = {0, M};
+            fp8bs::GroupTable gt;
+            fp8bs::fill_row_tiles(&gt, rows, 1, MT);
+            return status_of(fp8bs::launch_gemm_swapab(tmB, tmA, g, gt, MT, fq, 1, false, st));
         }
         // K too long to stage the scales, or a split K loop: two launches below.
     }
@@ -656,20 +663,74 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     g.N = static_cast<int>(N);
     g.K = static_cast<int>(K);
     g.weights_constant = 0;
-    int64_t m_tiles_total = 0;
-    for (int64_t i = 0; i < groups; ++i)
-        m_tiles_total += (row_offsets[i + 1] - row_offsets[i] + 127) / 128;
+    // Groups of at most 64 rows run in the swapped orientation (their weights on the MMA's M
+    // side, their few rows on its N side, as at decode), the others as 128-row tiles. With both
+    // kinds, the small groups' launch follows the other one without waiting for it (the two
+    // write disjoint rows of C): its CTAs take the SMs the first launch's last round leaves
+    // idle.
+    int64_t small_max = 0, small_count = 0;
+    for (int64_t i = 0; i < groups; ++i) {
+        const int64_t rows = row_offsets[i + 1] - row_offsets[i];
+        if (rows > 0 && rows <= 64) {
+            small_max = std::max(small_max, rows);
+            ++small_count;
+        }
+    }
+    const int MT = small_max <= 16 ? 16 : small_max <= 32 ? 32 : 64;
+    int S = 0;
+    if (small_count > 0)      // 0: K too long for the swapped kernel, every group as tiles
+        S = fp8bs::plan_gemm_swapab(MT, false, static_cast<int>(small_count), g.N, g.K, sms);
+    const int64_t small_rows = S > 0 ? 64 : 0;
+    auto is_small = [&](int64_t rows) { return rows > 0 && rows <= small_rows; };
+
     const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
-    const int BN = block_scaled ? fp8bs::pick_tile_n_bs(m_tiles_total, N, sms)
-                                : fp8bs::pick_tile_n(m_tiles_total, N, sms);
-    fp8bs::GroupTable gt;
-    fp8bs::fill_group_table(&gt, row_offsets, static_cast<int>(groups), g.N, BN);
-    CUtensorMap tmA, tmB;
-    if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
-        return FP8BS_ERR_CUDA;
-    if (block_scaled)
-        return status_of(fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, no_stream_k(), st));
-    return status_of(fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, no_stream_k(), st));
+    int64_t m_tiles_total = 0;
+    for (int64_t i = 0; i < groups; ++i) {
+        const int64_t rows = row_offsets[i + 1] - row_offsets[i];
+        if (!is_small(rows)) m_tiles_total += (rows + 127) / 128;
+    }
+    bool launched = false;
+    if (m_tiles_total > 0) {
+        // The group table keeps every group's rows; the small groups contribute no tiles.
+        const int BN = block_scaled ? fp8bs::pick_tile_n_bs(m_tiles_total, N, sms)
+                                    : fp8bs::pick_tile_n(m_tiles_total, N, sms);
+        const int n_tiles = static_cast<int>(ceil_div(N, BN));
+        fp8bs::GroupTable gt;
+        gt.num_groups = static_cast<int>(groups);
+        gt.row_off[0] = 0;
+        gt.tile_off[0] = 0;
+        for (int64_t i = 0; i < groups; ++i) {
+            const int64_t rows = row_offsets[i + 1] - row_offsets[i];
+            gt.row_off[i + 1] = static_cast<int>(row_offsets[i + 1]);
+            gt.tile_off[i + 1] =
+                gt.tile_off[i] + (is_small(rows) ? 0 : static_cast<int>((rows + 127) / 128)) * n_tiles;
+        }
+        CUtensorMap tmA, tmB;
+        if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
+            return FP8BS_ERR_CUDA;
+        const cudaError_t e =
+            block_scaled ? fp8bs::launch_gemm_bs(tmA, tmB, g, gt, BN, sms, no_stream_k(), st)
+                         : fp8bs::launch_gemm_tn(tmA, tmB, g, gt, BN, sms, no_stream_k(), st);
+        if (e != cudaSuccess) return FP8BS_ERR_CUDA;
+        launched = true;
+    }
+    if (small_count > 0 && S > 0) {
+        fp8bs::GroupTable gt;
+        gt.num_groups = static_cast<int>(groups);
+        gt.row_off[0] = 0;
+        gt.tile_off[0] = 0;
+        for (int64_t i = 0; i < groups; ++i) {
+            gt.row_off[i + 1] = static_cast<int>(row_offsets[i + 1]);
+            gt.tile_off[i + 1] =
+                gt.tile_off[i] + (is_small(row_offsets[i + 1] - row_offsets[i]) ? 1 : 0);
+        }
+        CUtensorMap tmA, tmB;
+        if (!make_map(&tmB, b, N * groups, K, 128) || !make_map(&tmA, a, M, K, MT))
+            return FP8BS_ERR_CUDA;
+        return status_of(fp8bs::launch_gemm_swapab(tmB, tmA, g, gt, MT, fp8bs::FusedQuant{}, S,
+                                                   launched, st));
+    }
+    return FP8BS_OK;
 }
 
 int fp8bs_device_error(unsigned int* out, int clear, void* stream) {

@@ -85,7 +85,8 @@ template <int MT, bool FUSED>
 __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     gemm_swapab_kernel(const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmA, const GemmArgs g,
-                       const int stages, const FusedQuant fq, const int ksplit) {
+                       const __grid_constant__ GroupTable gt, const int stages,
+                       const FusedQuant fq, const int ksplit, const int early) {
     using Cfg = SwapCfg<MT, FUSED>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -109,7 +110,13 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int n0 = slab * BM;
-    const int m0 = blockIdx.y * MT;
+    // Group and rows of this CTA: blockIdx.y counts the MT-row tiles of all groups, group by
+    // group; group grp owns rows row_off[grp] .. row_off[grp+1]-1 of A, a_s and C, rows
+    // grp*N .. of the stacked B and scale rows grp*ceil(N/128) .. of the stacked b_s.
+    int grp = 0;
+    while (static_cast<int>(blockIdx.y) >= gt.tile_off[grp + 1]) ++grp;
+    const int m0 = gt.row_off[grp] + (static_cast<int>(blockIdx.y) - gt.tile_off[grp]) * MT;
+    const int b_row = grp * g.N + n0;                    // row of the stacked B
 
     // Prologue order: barriers; (weights declared constant: the whole weight ring, before
     // waiting for earlier kernels); wait; scales; TMEM; block sync; activations (and weights).
@@ -120,9 +127,10 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     // contiguous) are requested by the promotion threads before the block synchronises, and the
     // weight stream only starts after it: the scales then return at unloaded latency instead of
     // queueing behind megabytes of weights.
-    const int scale_rows = min(MT, g.M - m0);
+    const int scale_rows = min(MT, gt.row_off[grp + 1] - m0);
     const float* as_rows = g.a_s + static_cast<int64_t>(m0) * num_kb;
-    const float* bs_row = g.b_s + static_cast<int64_t>(slab) * num_kb + kb_lo;
+    const float* bs_row =
+        g.b_s + (static_cast<int64_t>(grp) * ((g.N + BM - 1) / BM) + slab) * num_kb + kb_lo;
     // Quantised input: the scale warp counts here the K blocks of sAs it has filled.
     int* sScaleDone = reinterpret_cast<int*>(ring.tmem_holder + 1);
     if (threadIdx.x == 0) {
@@ -139,7 +147,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         if (g.weights_constant) {
             for (int i = 0; i < prefill; ++i) {
                 mbar_arrive_expect_tx(&ring.full[i], Cfg::TX_BYTES);
-                tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], (kb_lo + i) * BK, n0,
+                tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], (kb_lo + i) * BK, b_row,
                                  stream);
             }
         }
@@ -147,7 +155,10 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     if constexpr (FUSED) {
         for (int i = threadIdx.x; i < num_kb; i += Cfg::THREADS) sReady[i] = 0;
     }
-    grid_dependency_wait();
+    // `early`: this launch reads nothing the kernel just before it writes (the second of two
+    // launches over disjoint groups), so it starts its work at once and waits for that kernel
+    // only before exiting -- its own completion then still implies the other's.
+    if (!early) grid_dependency_wait();
     grid_launch_dependents();
     if (FUSED && warp >= 2 && warp < 2 + Cfg::EPI_WARPS) {
         const int t = threadIdx.x - 64;
@@ -196,7 +207,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             const int kb = kb_lo + i;
             if (!g.weights_constant) {
                 mbar_arrive_expect_tx(&ring.full[i], Cfg::TX_BYTES);
-                tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], kb * BK, n0, stream);
+                tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], kb * BK, b_row, stream);
             }
             tma_load_2d_hint(sAct + i * ACT_TILE, &tmA, &ring.full[i], kb * BK, m0, keep);
         }
@@ -215,7 +226,8 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                     break;
                 }
                 mbar_arrive_expect_tx(&ring.full[stage], Cfg::TX_BYTES);
-                tma_load_2d_hint(sW + stage * A_TILE, &tmB, &ring.full[stage], kb * BK, n0, stream);
+                tma_load_2d_hint(sW + stage * A_TILE, &tmB, &ring.full[stage], kb * BK, b_row,
+                                 stream);
                 tma_load_2d_hint(sAct + stage * ACT_TILE, &tmA, &ring.full[stage], kb * BK, m0,
                                  keep);
                 ++issued;
@@ -285,7 +297,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         const int sub = lane >> 3;                        // row within the warp's four
         const int chunk = lane & 7;
         const bool writer = blockIdx.x == 0;              // first slab: also write y and s
-        const int rows = min(MT, g.M - m0);               // rows of x; the rest stay zero
+        const int rows = scale_rows;                      // rows of x; the rest stay zero
         constexpr int PASSES = MT / 16;
         // Rows past M are zero codes in every stage (written once, never overwritten).
         for (int i = threadIdx.x - Cfg::Q_WARP0 * 32; i < stages * MT * 8; i += Cfg::Q_WARPS * 32) {
@@ -396,36 +408,41 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             auto scales4 = [&](int i) {
                 float4 a4 = *reinterpret_cast<const float4*>(as_kb + i);
                 if constexpr (FUSED) {   // rows past M: zero, as when staged
-                    a4.x = m0 + i < g.M ? a4.x * sb : 0.0f;
-                    a4.y = m0 + i + 1 < g.M ? a4.y * sb : 0.0f;
-                    a4.z = m0 + i + 2 < g.M ? a4.z * sb : 0.0f;
-                    a4.w = m0 + i + 3 < g.M ? a4.w * sb : 0.0f;
+                    a4.x = i < scale_rows ? a4.x * sb : 0.0f;
+                    a4.y = i + 1 < scale_rows ? a4.y * sb : 0.0f;
+                    a4.z = i + 2 < scale_rows ? a4.z * sb : 0.0f;
+                    a4.w = i + 3 < scale_rows ? a4.w * sb : 0.0f;
                 }
                 return a4;
             };
             if constexpr (MT >= 32) {
-                // Chunks of 32 columns, the next load in flight while one is folded in.
+                // Chunks of 32 columns, the next load in flight while one is folded in; only
+                // the chunks that hold rows of this CTA (a group of a grouped launch may have
+                // fewer rows than MT).
                 constexpr int NCH = MT / 32;
+                const int nch = (scale_rows + 31) >> 5;
                 float va[32], vb[32];
                 tmem_ld_32cols(taddr, va);
                 tmem_wait_ld_32(va);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
-                    float* cur = (c & 1) ? vb : va;
-                    float* nxt = (c & 1) ? va : vb;
-                    if (c + 1 < NCH) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
-                    if (c + 1 == NCH) {
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&ring.tempty[buf]);
-                    }
+                    if (c < nch) {
+                        float* cur = (c & 1) ? vb : va;
+                        float* nxt = (c & 1) ? va : vb;
+                        if (c + 1 < nch) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+                        if (c + 1 == nch) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                        }
 #pragma unroll
-                    for (int i = 0; i < 32; i += 4) {
-                        const float4 a4 = scales4(c * 32 + i);
-                        fma2_into(acc + c * 32 + i, cur[i + 0], cur[i + 1], a4.x, a4.y);
-                        fma2_into(acc + c * 32 + i + 2, cur[i + 2], cur[i + 3], a4.z, a4.w);
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 a4 = scales4(c * 32 + i);
+                            fma2_into(acc + c * 32 + i, cur[i + 0], cur[i + 1], a4.x, a4.y);
+                            fma2_into(acc + c * 32 + i + 2, cur[i + 2], cur[i + 3], a4.z, a4.w);
+                        }
+                        if (c + 1 < nch) tmem_wait_ld_32(nxt);
                     }
-                    if (c + 1 < NCH) tmem_wait_ld_32(nxt);
                 }
             } else {
                 float v[16];
@@ -449,7 +466,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 __nv_bfloat16* c = static_cast<__nv_bfloat16*>(g.c);
 #pragma unroll
                 for (int j = 0; j < MT; ++j)
-                    if (m0 + j < g.M)
+                    if (j < scale_rows)
                         c[static_cast<int64_t>(m0 + j) * g.N + n] = __float2bfloat16_rn(acc[j]);
             }
         } else {
@@ -510,6 +527,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     if (warp == 1) tmem_dealloc(tmem_base, Cfg::TMEM_COLS);
+    if (early && threadIdx.x == 0) grid_dependency_wait();
 }
 
 // Stages and dynamic shared-memory bytes of a launch whose CTAs take nkb K blocks each.
@@ -530,28 +548,28 @@ bool swap_smem(int nkb, int* stages_out, int* smem_out) {
 // Fewest K blocks per CTA worth a split of the K loop.
 constexpr int kMinSplitKb = 4;
 
-// CTAs per slab for this launch: the largest S (up to kMaxSplit) for which every CTA of the
-// grid is resident at once, as whole clusters, with at least kMinSplitKb K blocks each; 1 for
-// no split; 0 if the kernel cannot take this K (the activation scales do not fit).
+// CTAs per slab for a launch over `row_tiles` MT-row tiles: the largest S (up to kMaxSplit) for
+// which every CTA of the grid is resident at once, as whole clusters, with at least kMinSplitKb
+// K blocks each; 1 for no split; 0 if the kernel cannot take this K (the activation scales do
+// not fit).
 template <int MT, bool FUSED>
-int plan_swap(int M, int N, int K, int num_sms) {
+int plan_swap(int row_tiles, int N, int K, int num_sms) {
     using Cfg = SwapCfg<MT, FUSED>;
     auto kernel = gemm_swapab_kernel<MT, FUSED>;
     const int num_kb = K / BK;
     const int slabs = (N + BM - 1) / BM;
-    const int m_tiles = (M + MT - 1) / MT;
     if (set_smem(kernel, kSmemLimit) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
     for (int c = FUSED ? 1 : kMaxSplit; c > 1; --c) {
         int st = 0, sm = 0;
-        if (static_cast<int64_t>(slabs) * m_tiles * c > num_sms || num_kb / c < kMinSplitKb ||
+        if (static_cast<int64_t>(slabs) * row_tiles * c > num_sms || num_kb / c < kMinSplitKb ||
             !swap_smem<MT, FUSED>((num_kb + c - 1) / c, &st, &sm) ||
             swap_recv_bytes(MT, c) > st * Cfg::STAGE)
             continue;
         if (max_active_clusters(reinterpret_cast<const void*>(kernel), Cfg::THREADS, sm, c) <
-            static_cast<int64_t>(slabs) * m_tiles)
+            static_cast<int64_t>(slabs) * row_tiles)
             continue;
         return c;
     }
@@ -561,22 +579,24 @@ int plan_swap(int M, int N, int K, int num_sms) {
 
 template <int MT, bool FUSED>
 cudaError_t launch_swap(const CUtensorMap& tmB, const CUtensorMap& tmA, const GemmArgs& g,
-                        const FusedQuant& fq, int S, cudaStream_t stream) {
+                        const GroupTable& gt, const FusedQuant& fq, int S, bool early,
+                        cudaStream_t stream) {
     using Cfg = SwapCfg<MT, FUSED>;
     auto kernel = gemm_swapab_kernel<MT, FUSED>;
     cudaError_t e = set_smem(kernel, kSmemLimit);
     if (e != cudaSuccess) return e;
     const int num_kb = g.K / BK;
     int stages = 0, smem = 0;
-    if (S < 1 || (FUSED && S != 1) || !swap_smem<MT, FUSED>((num_kb + S - 1) / S, &stages, &smem))
+    if (S < 1 || (FUSED && (S != 1 || gt.num_groups != 1)) ||
+        !swap_smem<MT, FUSED>((num_kb + S - 1) / S, &stages, &smem))
         return cudaErrorInvalidValue;
     if (S > 1 && swap_recv_bytes(MT, S) > stages * Cfg::STAGE) return cudaErrorInvalidValue;
-    const dim3 grid(((g.N + BM - 1) / BM) * S, (g.M + MT - 1) / MT);
-    return launch_pdl_cluster(kernel, grid, Cfg::THREADS, smem, stream, S, false, tmB, tmA, g,
-                              stages, fq, S);
+    const int row_tiles = gt.tile_off[gt.num_groups];
+    if (row_tiles == 0) return cudaSuccess;
+    const dim3 grid(((g.N + BM - 1) / BM) * S, row_tiles);
+    return launch_pdl_cluster(kernel, grid, Cfg::THREADS, smem, stream, S, false, tmB, tmA, g, gt,
+                              stages, fq, S, early ? 1 : 0);
 }
-
-}  // namespace
 
 template <int MT>
 bool check_swap(int K, int S) {
@@ -585,6 +605,8 @@ bool check_swap(int K, int S) {
     if (S < 1 || S > num_kb || !swap_smem<MT, false>((num_kb + S - 1) / S, &st, &sm)) return false;
     return S == 1 || swap_recv_bytes(MT, S) <= st * SwapCfg<MT, false>::STAGE;
 }
+
+}  // namespace
 
 bool check_gemm_swapab(int MT, int K, int ksplit) {
     switch (MT) {
@@ -596,40 +618,52 @@ bool check_gemm_swapab(int MT, int K, int ksplit) {
     }
 }
 
-int plan_gemm_swapab(int MT, bool fused, int M, int N, int K, int num_sms) {
+int plan_gemm_swapab(int MT, bool fused, int row_tiles, int N, int K, int num_sms) {
     if (fused) {
         switch (MT) {
-            case 16: return plan_swap<16, true>(M, N, K, num_sms);
-            case 32: return plan_swap<32, true>(M, N, K, num_sms);
-            case 64: return plan_swap<64, true>(M, N, K, num_sms);
+            case 16: return plan_swap<16, true>(row_tiles, N, K, num_sms);
+            case 32: return plan_swap<32, true>(row_tiles, N, K, num_sms);
+            case 64: return plan_swap<64, true>(row_tiles, N, K, num_sms);
             default: return 0;
         }
     }
     switch (MT) {
-        case 16: return plan_swap<16, false>(M, N, K, num_sms);
-        case 32: return plan_swap<32, false>(M, N, K, num_sms);
-        case 64: return plan_swap<64, false>(M, N, K, num_sms);
-        case 128: return plan_swap<128, false>(M, N, K, num_sms);
+        case 16: return plan_swap<16, false>(row_tiles, N, K, num_sms);
+        case 32: return plan_swap<32, false>(row_tiles, N, K, num_sms);
+        case 64: return plan_swap<64, false>(row_tiles, N, K, num_sms);
+        case 128: return plan_swap<128, false>(row_tiles, N, K, num_sms);
         default: return 0;
     }
 }
 
+void fill_row_tiles(GroupTable* gt, const int64_t* row_off, int groups, int MT) {
+    gt->num_groups = groups;
+    gt->row_off[0] = static_cast<int>(row_off[0]);
+    gt->tile_off[0] = 0;
+    for (int i = 0; i < groups; ++i) {
+        const int rows = static_cast<int>(row_off[i + 1] - row_off[i]);
+        gt->row_off[i + 1] = static_cast<int>(row_off[i + 1]);
+        gt->tile_off[i + 1] = gt->tile_off[i] + (rows + MT - 1) / MT;
+    }
+}
+
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
-                               const GemmArgs& g, int MT, const FusedQuant& fq, int ksplit,
+                               const GemmArgs& g, const GroupTable& gt, int MT,
+                               const FusedQuant& fq, int ksplit, bool early,
                                cudaStream_t stream) {
     if (fq.x) {
         switch (MT) {
-            case 16: return launch_swap<16, true>(tmB, tmA, g, fq, ksplit, stream);
-            case 32: return launch_swap<32, true>(tmB, tmA, g, fq, ksplit, stream);
-            case 64: return launch_swap<64, true>(tmB, tmA, g, fq, ksplit, stream);
+            case 16: return launch_swap<16, true>(tmB, tmA, g, gt, fq, ksplit, early, stream);
+            case 32: return launch_swap<32, true>(tmB, tmA, g, gt, fq, ksplit, early, stream);
+            case 64: return launch_swap<64, true>(tmB, tmA, g, gt, fq, ksplit, early, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (MT) {
-        case 16: return launch_swap<16, false>(tmB, tmA, g, fq, ksplit, stream);
-        case 32: return launch_swap<32, false>(tmB, tmA, g, fq, ksplit, stream);
-        case 64: return launch_swap<64, false>(tmB, tmA, g, fq, ksplit, stream);
-        case 128: return launch_swap<128, false>(tmB, tmA, g, fq, ksplit, stream);
+        case 16: return launch_swap<16, false>(tmB, tmA, g, gt, fq, ksplit, early, stream);
+        case 32: return launch_swap<32, false>(tmB, tmA, g, gt, fq, ksplit, early, stream);
+        case 64: return launch_swap<64, false>(tmB, tmA, g, gt, fq, ksplit, early, stream);
+        case 128: return launch_swap<128, false>(tmB, tmA, g, gt, fq, ksplit, early, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -157,15 +157,21 @@ struct FusedQuant {
 // Swapped orientation for few rows of A: 128-row slabs of B on the MMA's M side, MT rows of A
 // on its N side. tmB: box {128, 128} over B [N,K]; tmA: box {128, MT} over A [M,K] (with
 // FusedQuant: a bf16 map over x, box {128, MT}, no swizzle).
-// ksplit > 1 (quantised input only): the K loop of each 128-row slab is split between the
-// ksplit CTAs of a cluster, whose fp32 partials are added in rank order through distributed
-// shared memory. plan_gemm_swapab gives the split for a problem (1: none; 0: this kernel cannot
-// take K, whose activation scales would not fit in shared memory).
-int plan_gemm_swapab(int MT, bool fused, int M, int N, int K, int num_sms);
+// Groups: the launch covers the MT-row tiles of every group of `gt` (tile_off counts row
+// tiles, see fill_row_tiles); group i's rows take the stacked B's rows i*N .. and b_s's scale
+// rows i*ceil(N/128) .. (a plain GEMM is one group). ksplit > 1 (quantised input only): the K
+// loop of each 128-row slab is split between the ksplit CTAs of a cluster, whose fp32 partials
+// are added in rank order through distributed shared memory. early: the launch reads nothing
+// the kernel before it on the stream writes, so it starts at once and waits for that kernel
+// only before it exits. plan_gemm_swapab gives the split for `row_tiles` tiles (1: none; 0:
+// this kernel cannot take K, whose activation scales would not fit in shared memory).
+int plan_gemm_swapab(int MT, bool fused, int row_tiles, int N, int K, int num_sms);
 // Whether the quantised-input kernel can run with MT rows, this K and a split of ksplit.
 bool check_gemm_swapab(int MT, int K, int ksplit);
+void fill_row_tiles(GroupTable* gt, const int64_t* row_off, int groups, int MT);
 cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
-                               const GemmArgs& g, int MT, const FusedQuant& fq, int ksplit,
+                               const GemmArgs& g, const GroupTable& gt, int MT,
+                               const FusedQuant& fq, int ksplit, bool early,
                                cudaStream_t stream);
 
 // bf16 path, decode orientation (M <= 64, MT = 16, 32 or 64): y bf16 [M, N] = x . W'^T with W'

@@ -301,7 +301,11 @@ FP8BS_API int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b,
  *   groups      0 .. 256.  N >= 0, K >= 0 with K % 128 == 0.  scale_fmt as in fp8bs_gemm
  *               (with FP8BS_SCALE_UE8M0 every group runs on the block-scaled MMA).
  *
- * Results and accuracy are those of fp8bs_gemm on each group's rows.
+ * Results and accuracy are those of fp8bs_gemm on each group's rows. Groups of at most 64
+ * rows are computed in the swapped orientation (their weights on the MMA's M side, as for
+ * decode-sized M); the others as 128-row tiles. With both kinds the call enqueues two kernels,
+ * and the second starts without waiting for the first (they write disjoint rows of c) but
+ * completes only after it, so work enqueued after the call sees all of c.
  */
 FP8BS_API int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const float* b_s,
                                  void* c, const int64_t* row_offsets, int64_t groups, int64_t N,

@@ -186,3 +186,33 @@ def test_act_quant_gemm_argument_checks(lib, args, expect):
 ])
 def test_linear_bf16_argument_checks(lib, args, expect):
     assert lib.fp8bs_linear_bf16(*args, None) == expect
+
+
+def test_gemm_plan_argument_checks(lib):
+    """fp8bs_gemm_plan checks its arguments before looking at the device."""
+    out = [ctypes.c_int(0) for _ in range(4)]
+    refs = [ctypes.byref(o) for o in out]
+    assert lib.fp8bs_gemm_plan(8, 256, 200, 0, 1, *refs) == INVALID       # K % 128
+    assert lib.fp8bs_gemm_plan(0, 256, 256, 0, 1, *refs) == INVALID       # empty shape
+    assert lib.fp8bs_gemm_plan(8, 256, 256, 3, 1, *refs) == INVALID       # bad scale_fmt
+    assert lib.fp8bs_gemm_plan(8, 256, 256, 0, 1, None, *refs[1:]) == INVALID
+    import torch
+    if not torch.cuda.is_available():
+        assert lib.fp8bs_gemm_plan(8, 256, 256, 0, 1, *refs) in (CUDA, UNSUPPORTED)
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((A16, B16, C16, B16, C16, 8, 256, 200, 0, 0, 1, 128, 1), INVALID),      # K % 128
+    ((A16, B16, C16, B16, C16, 8, 256, 256, 0, 0x2, 1, 128, 1), INVALID),    # unknown flag
+    ((A16 + 8, B16, C16, B16, C16, 300, 256, 256, 0, 0, 1, 128, 1), MISALIGNED),
+    ((None, None, None, None, None, 0, 256, 256, 0, 0, 1, 128, 1), OK),      # empty: no-op
+])
+def test_gemm_config_argument_checks(lib, args, expect):
+    """fp8bs_gemm_config checks the arguments it shares with fp8bs_gemm_ws first; the
+    configuration itself is checked against the device's kernels (GPU tests)."""
+    assert lib.fp8bs_gemm_config(*args, None, 0, None) == expect
+
+
+def test_probe_occupy_argument_checks(lib):
+    assert lib.fp8bs_probe_occupy(0, 1000, None) == INVALID
+    assert lib.fp8bs_probe_occupy(2000, 1000, None) == INVALID

@@ -359,6 +359,19 @@ def test_gemm_grouped_against_oracle(counts, N, K):
     grouped_check(counts, N, K, seed=sum(counts) + N, what=f"grouped {counts}")
 
 
+@pytest.mark.parametrize("counts,N,K,fmt", [
+    ([1, 8, 32, 64], 2048, 7168, "fp32"),      # decode-sized groups: one swapped launch
+    ([3, 17, 40], 1000, 2048, "fp32"),         # ragged N, the K loop split in clusters
+    ([0, 5, 0, 64, 2], 576, 1024, "ue8m0"),
+    ([200, 3, 0, 64, 130, 1], 384, 512, "fp32"),  # both launches: tiles, then swapped groups
+])
+def test_gemm_grouped_small_groups(counts, N, K, fmt):
+    """Groups of at most 64 rows run in the swapped orientation (with other groups: as a
+    second launch that starts without waiting for the first); every element against the
+    oracle."""
+    grouped_check(counts, N, K, seed=sum(counts) + N + 3, what=f"grouped small {counts}", fmt=fmt)
+
+
 def test_gemm_grouped_moe_full_size():
     """The MoE workload (1024 tokens x 8 slots over 32 experts, N=2048, K=7168) in one call."""
     rows, counts = synth.moe_routing(0)
