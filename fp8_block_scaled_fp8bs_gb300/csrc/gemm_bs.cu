@@ -73,6 +73,11 @@ struct BsCfg {
     static constexpr int ACC = ISSUERS * BN;          // TMEM columns of one buffer
     static constexpr int SF_COL0 = NBUF * ACC;
     static constexpr int PART = BM * BN * 4;          // one fp32 partial tile (stream-K)
+    // Shared-memory scratch of the epilogue's coalesced stores of whole 192- and 256-wide tiles,
+    // 4 KB per epilogue warp. Narrower tiles store rows directly: at BN = 128 the stages fill
+    // shared memory, and at BN = 64 a lane's 128-byte row is one whole line anyway (the MLA kv
+    // projection measured 17.5 us direct, 19.0 us through the scratch).
+    static constexpr int SCRATCH = BN > 128 ? EPI_WARPS * 4096 : 0;
 };
 
 template <int BN>
@@ -110,11 +115,12 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     uint8_t* sA = smem;
     uint8_t* sB = smem + stages * A_TILE;
     const bool stream_k = sk.parts != nullptr;
-    // Stream-K only: the first contributor's partial of the tile this CTA owns, copied in while
-    // the owner's own piece still runs (after the stages, 1024-byte aligned), and the barrier
-    // counting its bytes (after the ring).
-    float4* sPart = reinterpret_cast<float4*>(sB + stages * Cfg::B_TILE);
-    const Ring ring = carve_ring(sB + stages * Cfg::B_TILE + (stream_k ? Cfg::PART : 0), stages);
+    // The epilogue's store scratch (after the stages). Stream-K only: the first contributor's
+    // partial of the tile this CTA owns, copied in while the owner's own piece still runs
+    // (1024-byte aligned), and the barrier counting its bytes (after the ring).
+    uint8_t* sScratch = sB + stages * Cfg::B_TILE;
+    float4* sPart = reinterpret_cast<float4*>(sScratch + Cfg::SCRATCH);
+    const Ring ring = carve_ring(sScratch + Cfg::SCRATCH + (stream_k ? Cfg::PART : 0), stages);
     uint64_t* part_bar = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(ring.full) +
                                                      ring_bytes(stages));
 
@@ -398,24 +404,17 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                 static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(row) * g.N + t.n0;
             const int valid = min(BN, g.N - t.n0);
             const bool vec = (g.N & 7) == 0;
+            uint8_t* scratch = Cfg::SCRATCH > 0 ? sScratch + quarter * 4096 : nullptr;
+            const WarpRows wr{static_cast<__nv_bfloat16*>(g.c), g.N, t.m0 + quarter * 32,
+                              t.row_end, t.n0};
 
             if (kb0 == 0 && kb1 == num_kb) {
                 if constexpr (BN > 128) {
-                    // A whole 256-wide tile (one buffer): 32 columns at a time, the next
-                    // chunk's load in flight while one is stored; the buffer goes back after
-                    // the last load.
-                    float va[32], vb[32];
-                    tmem_ld_32cols(taddr, va);
-                    tmem_wait_ld_32(va);
-#pragma unroll
-                    for (int c = 0; c < BN / 32; ++c) {
-                        float* cur = (c & 1) ? vb : va;
-                        float* nxt = (c & 1) ? va : vb;
-                        if (c + 1 < BN / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
-                        if (store) store_row_bf16<32>(crow + 32 * c, cur, valid - 32 * c, vec);
-                        if (c + 1 < BN / 32) tmem_wait_ld_32(nxt);
-                    }
-                    release_tmem(&ring.tempty[buf], lane);
+                    // A whole 192- or 256-wide tile: the row into registers as bf16 pairs, the
+                    // buffer back (at BN = 256 the only one: the next tile's MMAs wait for it),
+                    // then store. Storing between the loads held the buffer ~9K clk per tile.
+                    drain_row_bf16<BN>(taddr, crow, store, valid, vec, scratch, wr, lane,
+                                       [&] { release_tmem(&ring.tempty[buf], lane); });
                 } else {
                     // A whole tile: the accumulator into registers, the buffer back, then store.
                     float acc[BN];
@@ -436,7 +435,14 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                         }
                     }
                     release_tmem(&ring.tempty[buf], lane);
-                    if (store) store_row_bf16<BN>(crow, acc, valid, vec);
+                    if (Cfg::SCRATCH > 0 && vec) {
+                        uint32_t pk[BN / 2];
+#pragma unroll
+                        for (int i = 0; i < BN / 2; ++i) pk[i] = pack_bf16x2(acc[2 * i], acc[2 * i + 1]);
+                        store_rows_coalesced<BN>(scratch, pk, wr, lane);
+                    } else if (store) {
+                        store_row_bf16<BN>(crow, acc, valid, vec);
+                    }
                 }
             } else if (kb0 > 0) {
                 // A piece that does not start its tile: publish the partial in this CTA's slot,
@@ -808,8 +814,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::THREADS, 1)
         if (!__all_sync(0xffffffffu, pow2) && lane == 0) record_error(FP8BS_DEVERR_SCALE_NOT_POW2);
     } else if (warp < Cfg::SF_WARPS + Cfg::EPI_WARPS) {
         // Epilogue: warp w reads TMEM lanes 32*(w%4) .. +31 (this CTA's rows of the same
-        // numbers), 32 columns at a time with the next chunk's load in flight, and hands the
-        // buffer back to the leader after the last load.
+        // numbers) and hands the buffer back to the leader once it has read it all.
         const int quarter = warp & 3;
         const int row_in_tile = quarter * 32 + lane;
         const bool vec = (g.N & 7) == 0;
@@ -830,23 +835,11 @@ __global__ void __launch_bounds__(PairCfg<BN>::THREADS, 1)
             __nv_bfloat16* crow =
                 static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(row) * g.N + n0;
             const int valid = min(BN, g.N - n0);
-            float va[32], vb[32];
-            tmem_ld_32cols(taddr, va);
-            tmem_wait_ld_32(va);
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c) {
-                float* cur = (c & 1) ? vb : va;
-                float* nxt = (c & 1) ? va : vb;
-                if (c + 1 < BN / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
-                if (c + 1 == BN / 32) {
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0)
-                        mbar_arrive_cluster(mapa_shared(smem_addr(&ring.tempty[buf]), 0));
-                }
-                if (store) store_row_bf16<32>(crow + 32 * c, cur, valid - 32 * c, vec);
-                if (c + 1 < BN / 32) tmem_wait_ld_32(nxt);
-            }
+            drain_row_bf16<BN>(taddr, crow, store, valid, vec, nullptr, WarpRows{}, lane, [&] {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&ring.tempty[buf]), 0));
+            });
             if (Cfg::NBUF == 2) buf ^= 1;
             if (buf == 0) tphase ^= 1;
         }
@@ -883,16 +876,16 @@ int pair_clusters() {
 // barrier) is kept in shared memory, at two stages' cost.
 template <int BN>
 constexpr int bs_stages(bool stream_k) {
-    return (kSmemLimit - 1024 - ring_bytes(kMaxStages) -
+    return (kSmemLimit - 1024 - ring_bytes(kMaxStages) - BsCfg<BN>::SCRATCH -
             (stream_k ? BsCfg<BN>::PART + 16 : 0)) / BsCfg<BN>::STAGE > kMaxStages
                ? kMaxStages
-               : (kSmemLimit - 1024 - ring_bytes(kMaxStages) -
+               : (kSmemLimit - 1024 - ring_bytes(kMaxStages) - BsCfg<BN>::SCRATCH -
                   (stream_k ? BsCfg<BN>::PART + 16 : 0)) / BsCfg<BN>::STAGE;
 }
 
 template <int BN>
 constexpr int bs_smem(bool stream_k) {
-    return 1024 + bs_stages<BN>(stream_k) * BsCfg<BN>::STAGE +
+    return 1024 + bs_stages<BN>(stream_k) * BsCfg<BN>::STAGE + BsCfg<BN>::SCRATCH +
            (stream_k ? BsCfg<BN>::PART + 16 : 0) + ring_bytes(bs_stages<BN>(stream_k));
 }
 

@@ -170,6 +170,113 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* crow, const float*
     }
 }
 
+// Read BN accumulator columns of this thread's TMEM lane as packed bf16 pairs (the rounding of
+// store_row_bf16; column 2i in the low half of pk[i]), 16 columns per load (the packed row
+// takes BN/2 registers). Holding the row in registers lets the epilogue hand a single
+// accumulator buffer back before its global stores, which are scattered over 32 rows per warp
+// instruction and take several times as long as the loads.
+template <int BN>
+__device__ __forceinline__ void tmem_row_bf16(uint32_t taddr, uint32_t* pk) {
+#pragma unroll
+    for (int c = 0; c < BN / 16; ++c) {
+        float v[16];
+        tmem_ld_16cols(taddr + 16 * c, v);
+        tmem_wait_ld_16(v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) pk[8 * c + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+    }
+}
+
+// store_row_bf16's 16-byte stores (N % 8 == 0) for a row packed by tmem_row_bf16.
+template <int CW>
+__device__ __forceinline__ void store_row_packed(__nv_bfloat16* crow, const uint32_t* pk,
+                                                 int valid) {
+#pragma unroll
+    for (int j = 0; j < CW / 8; ++j)
+        if (8 * j < valid)
+            *reinterpret_cast<uint4*>(crow + 8 * j) =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+}
+
+// Where a warp's 32 output rows go: rows row0 .. row0+31 of C (leading dimension N) from column
+// n0, rows at or past row_end not stored.
+struct WarpRows {
+    __nv_bfloat16* c;
+    int64_t N;
+    int row0, row_end, n0;
+};
+
+// The 16-byte stores of a warp's 32 rows (lane l holds CW columns of row l as packed bf16 pairs)
+// through a shared-memory scratch of the warp (32 x CH x 2 bytes), CH = 64 or 32 columns at a
+// time: each lane writes its row's piece of the chunk (16-byte piece k of row r at position
+// k ^ (r & 7), or k ^ ((r >> 1) & 3) for 64-byte rows, so that the eight lanes of a shared-memory
+// phase hit distinct banks), then CH/8 lanes store each row's piece, 32/(CH/8) rows per
+// instruction. Row-per-lane stores touch 32 rows per instruction: measured on GB300 they held
+// the memory pipeline long enough to cost ~15 % of the ue8m0 prefill GEMM (385 against 329 us
+// with the stores left out).
+template <int CW, int CH = 64>
+__device__ __forceinline__ void store_rows_coalesced(uint8_t* scratch, const uint32_t* pk,
+                                                     const WarpRows& w, int lane) {
+    static_assert(CH == 32 || CH == 64, "chunk width");
+    static_assert(CW % CH == 0, "whole chunks");
+    constexpr int KCH = CH / 8;           // 16-byte pieces per row of a chunk
+    constexpr int RPI = 32 / KCH;         // rows per store instruction
+    const auto pos = [](int r, int k) { return CH == 64 ? (k ^ (r & 7)) : (k ^ ((r >> 1) & 3)); };
+    const int sub = lane % KCH;
+#pragma unroll
+    for (int q = 0; q < CW / CH; ++q) {
+#pragma unroll
+        for (int k = 0; k < KCH; ++k) {
+            const uint32_t* src = pk + (CH / 2) * q + 4 * k;
+            *reinterpret_cast<uint4*>(scratch + lane * (2 * CH) + pos(lane, k) * 16) =
+                make_uint4(src[0], src[1], src[2], src[3]);
+        }
+        __syncwarp();
+        const int col = w.n0 + CH * q + 8 * sub;
+#pragma unroll
+        for (int i = 0; i < KCH; ++i) {
+            const int r = RPI * i + lane / KCH;
+            const uint4 v =
+                *reinterpret_cast<const uint4*>(scratch + r * (2 * CH) + pos(r, sub) * 16);
+            if (w.row0 + r < w.row_end && col < w.N)
+                *reinterpret_cast<uint4*>(w.c + static_cast<int64_t>(w.row0 + r) * w.N + col) = v;
+        }
+        __syncwarp();
+    }
+}
+
+// The epilogue of a whole BN-column tile from one TMEM buffer: with 16-byte stores, the row
+// into registers, `release` (the buffer back to the MMA issuer), then the stores (through the
+// warp's scratch when it has one); otherwise (element stores, N % 8 != 0) 32 columns at a time
+// with the next chunk's load in flight and `release` after the last load.
+template <int BN, typename Release>
+__device__ __forceinline__ void drain_row_bf16(uint32_t taddr, __nv_bfloat16* crow, bool store,
+                                               int valid, bool vec, uint8_t* scratch,
+                                               const WarpRows& w, int lane, Release release) {
+    if (vec) {
+        uint32_t pk[BN / 2];
+        tmem_row_bf16<BN>(taddr, pk);
+        release();
+        if (scratch != nullptr)
+            store_rows_coalesced<BN>(scratch, pk, w, lane);
+        else if (store)
+            store_row_packed<BN>(crow, pk, valid);
+        return;
+    }
+    float va[32], vb[32];
+    tmem_ld_32cols(taddr, va);
+    tmem_wait_ld_32(va);
+#pragma unroll
+    for (int c = 0; c < BN / 32; ++c) {
+        float* cur = (c & 1) ? vb : va;
+        float* nxt = (c & 1) ? va : vb;
+        if (c + 1 < BN / 32) tmem_ld_32cols(taddr + 32 * (c + 1), nxt);
+        if (c + 1 == BN / 32) release();
+        if (store) store_row_bf16<32>(crow + 32 * c, cur, valid - 32 * c, false);
+        if (c + 1 < BN / 32) tmem_wait_ld_32(nxt);
+    }
+}
+
 constexpr int kSmemLimit = 227 * 1024;
 constexpr int kMaxStages = 8;
 
