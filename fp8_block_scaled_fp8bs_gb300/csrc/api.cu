@@ -177,9 +177,12 @@ fp8bs::StreamKArgs plan_stream_k_tn(int64_t tiles, int64_t num_kb, int sms, void
     return fp8bs::StreamKArgs{workspace, dp, 1};
 }
 
-// Relative time of one K block of a 128 x bn tile (the tile-width models of the two kernels;
-// the block-scaled kernel's 64-wide tiles have two MMA issuers: 18.3 us for the MLA kv
-// projection as 144 such tiles against 24.1 us as 80 tiles 128 wide, both one round).
+// Relative time of one K block of a 128 x bn tile in the split schedule below (the tile-width
+// models of the two kernels; the block-scaled kernel's 64-wide tiles have two MMA issuers:
+// 18.3 us for the MLA kv projection as 144 such tiles against 24.1 us as 80 tiles 128 wide,
+// both one round). The block-scaled 192-wide tile keeps 117 here although its two issuers make
+// whole tiles cheaper (104 in pick_tile_n_bs): split two ways, the MLA kv projection measured
+// 18.75 us against 17.6 us as whole 64-wide tiles, which 104 would not predict.
 int64_t width_cost(bool block_scaled, int bn) {
     switch (bn) {
         case 256: return block_scaled ? 134 : 141;

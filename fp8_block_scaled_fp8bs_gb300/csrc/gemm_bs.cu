@@ -56,9 +56,12 @@ struct BsCfg {
     static_assert(BN == 64 || BN == 128 || BN == 192 || BN == 256, "tile width");
     static constexpr int SF_WARPS = 4;
     static constexpr int EPI_WARPS = 4;
-    // MMA issuers: two at BN = 64, taking a tile's K blocks in turn into accumulators of their
-    // own. Wider tiles keep one: two buffers of two accumulators would not fit in TMEM.
-    static constexpr int ISSUERS = BN <= 64 ? 2 : 1;
+    // MMA issuers: two at BN = 64 and 192, taking a tile's K blocks in turn into accumulators
+    // of their own (one thread issuing alone advances one K block per ~650-770 clk at these
+    // widths whatever N is; the MLA q projection, 128 tiles of 192, went from 26.6 to 23.2 us).
+    // 128 keeps one (two buffers of two accumulators would not fit in TMEM, and one buffer
+    // loses the epilogue overlap its many-round shapes need); 256 has no room for a second.
+    static constexpr int ISSUERS = (BN <= 64 || BN == 192) ? 2 : 1;
     static constexpr int THREADS = 32 * (SF_WARPS + EPI_WARPS + 1 + ISSUERS);
     static constexpr int B_TILE = BN * BK;
     static constexpr int STAGE = A_TILE + B_TILE;
@@ -67,9 +70,10 @@ struct BsCfg {
     // the slot covers tile rows 32c .. 32c+31).
     static constexpr int SF_B_COLS = BN > 128 ? 8 : 4;
     static constexpr int SF_COLS = 4 + SF_B_COLS;
-    // Accumulators: two BN-column buffers (the epilogue of one tile overlaps the next), or at
-    // BN = 256 one (two would fill TMEM and leave no room for scale factors).
-    static constexpr int NBUF = BN > 192 ? 1 : 2;
+    // Accumulators: two buffers of ISSUERS x BN columns (the epilogue of one tile overlaps the
+    // next), or one where two would leave no TMEM for the scale factors (BN = 256, and 192
+    // with its two issuers).
+    static constexpr int NBUF = BN > 128 ? 1 : 2;
     static constexpr int ACC = ISSUERS * BN;          // TMEM columns of one buffer
     static constexpr int SF_COL0 = NBUF * ACC;
     static constexpr int PART = BM * BN * 4;          // one fp32 partial tile (stream-K)
@@ -413,7 +417,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     // A whole 192- or 256-wide tile: the row into registers as bf16 pairs, the
                     // buffer back (at BN = 256 the only one: the next tile's MMAs wait for it),
                     // then store. Storing between the loads held the buffer ~9K clk per tile.
-                    drain_row_bf16<BN>(taddr, crow, store, valid, vec, scratch, wr, lane,
+                    drain_row_bf16<BN>(taddr, crow, store, valid, vec, two, scratch, wr, lane,
                                        [&] { release_tmem(&ring.tempty[buf], lane); });
                 } else {
                     // A whole tile: the accumulator into registers, the buffer back, then store.
@@ -835,7 +839,7 @@ __global__ void __launch_bounds__(PairCfg<BN>::THREADS, 1)
             __nv_bfloat16* crow =
                 static_cast<__nv_bfloat16*>(g.c) + static_cast<int64_t>(row) * g.N + n0;
             const int valid = min(BN, g.N - n0);
-            drain_row_bf16<BN>(taddr, crow, store, valid, vec, nullptr, WarpRows{}, lane, [&] {
+            drain_row_bf16<BN>(taddr, crow, store, valid, vec, false, nullptr, WarpRows{}, lane, [&] {
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_addr(&ring.tempty[buf]), 0));
@@ -936,12 +940,13 @@ int split_clusters_bs(int S) {
 }  // namespace
 
 // Tile width by rounds of tiles over the SMs times the measured time of one K block at that
-// width (~886 clk at 256, ~660 at 128 at prefill shapes; 192 taken between them; 64, with its
-// two MMA issuers, 0.76 of 128 on the MLA kv projection): wider tiles carry fewer operand
-// bytes per MAC but leave more SMs idle when tiles are few.
+// width relative to 128 (256: 134; 192 with its two MMA issuers: 104, from the prefill
+// up-projection at 192 (353 us, 21 rounds) against 256 (346 us, 16 rounds); 64, also with two
+// issuers: 76, from the MLA kv projection): wider tiles carry fewer operand bytes per MAC but
+// leave more SMs idle when tiles are few.
 int pick_tile_n_bs(int64_t m_tiles_total, int64_t N, int num_sms) {
     static const int kWidth[4] = {256, 192, 64, 128};
-    static const int kCost[4] = {134, 117, 76, 100};
+    static const int kCost[4] = {134, 104, 76, 100};
     int best = 128;
     int64_t best_cost = INT64_MAX;
     for (int i = 0; i < 4; ++i) {

@@ -172,16 +172,24 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* crow, const float*
 
 // Read BN accumulator columns of this thread's TMEM lane as packed bf16 pairs (the rounding of
 // store_row_bf16; column 2i in the low half of pk[i]), 16 columns per load (the packed row
-// takes BN/2 registers). Holding the row in registers lets the epilogue hand a single
-// accumulator buffer back before its global stores, which are scattered over 32 rows per warp
-// instruction and take several times as long as the loads.
+// takes BN/2 registers); with `two`, the sum of two accumulators BN columns apart (two MMA
+// issuers). Holding the row in registers lets the epilogue hand a single accumulator buffer
+// back before its global stores, which are scattered over 32 rows per warp instruction and
+// take several times as long as the loads.
 template <int BN>
-__device__ __forceinline__ void tmem_row_bf16(uint32_t taddr, uint32_t* pk) {
+__device__ __forceinline__ void tmem_row_bf16(uint32_t taddr, uint32_t* pk, bool two) {
 #pragma unroll
     for (int c = 0; c < BN / 16; ++c) {
         float v[16];
         tmem_ld_16cols(taddr + 16 * c, v);
         tmem_wait_ld_16(v);
+        if (two) {
+            float u[16];
+            tmem_ld_16cols(taddr + BN + 16 * c, u);
+            tmem_wait_ld_16(u);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] += u[i];
+        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) pk[8 * c + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
     }
@@ -245,22 +253,38 @@ __device__ __forceinline__ void store_rows_coalesced(uint8_t* scratch, const uin
     }
 }
 
-// The epilogue of a whole BN-column tile from one TMEM buffer: with 16-byte stores, the row
-// into registers, `release` (the buffer back to the MMA issuer), then the stores (through the
-// warp's scratch when it has one); otherwise (element stores, N % 8 != 0) 32 columns at a time
-// with the next chunk's load in flight and `release` after the last load.
+// The epilogue of a whole BN-column tile from one TMEM buffer (with `two`, the sum of the two
+// issuers' accumulators): with 16-byte stores, the row into registers, `release` (the buffer
+// back to the MMA issuer), then the stores (through the warp's scratch when it has one);
+// otherwise (element stores, N % 8 != 0) 32 columns at a time with the next chunk's load in
+// flight and `release` after the last load.
 template <int BN, typename Release>
 __device__ __forceinline__ void drain_row_bf16(uint32_t taddr, __nv_bfloat16* crow, bool store,
-                                               int valid, bool vec, uint8_t* scratch,
+                                               int valid, bool vec, bool two, uint8_t* scratch,
                                                const WarpRows& w, int lane, Release release) {
     if (vec) {
         uint32_t pk[BN / 2];
-        tmem_row_bf16<BN>(taddr, pk);
+        tmem_row_bf16<BN>(taddr, pk, two);
         release();
         if (scratch != nullptr)
             store_rows_coalesced<BN>(scratch, pk, w, lane);
         else if (store)
             store_row_packed<BN>(crow, pk, valid);
+        return;
+    }
+    if (two) {
+#pragma unroll
+        for (int c = 0; c < BN / 32; ++c) {
+            float v[32], u[32];
+            tmem_ld_32cols(taddr + 32 * c, v);
+            tmem_ld_32cols(taddr + BN + 32 * c, u);
+            tmem_wait_ld_32(v);
+            tmem_wait_ld_32(u);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] += u[i];
+            if (c + 1 == BN / 32) release();
+            if (store) store_row_bf16<32>(crow + 32 * c, v, valid - 32 * c, false);
+        }
         return;
     }
     float va[32], vb[32];

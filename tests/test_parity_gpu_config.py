@@ -76,6 +76,9 @@ CONFIGS = [
     (B, 192, 2, UE8M0, 300, 1000, 1024, False),
     (B, 256, 8, UE8M0, 300, 1000, 1024, False),
     (B, 128, 0, UE8M0, 1100, 2500, 2048, True),     # stream-K: 180 tiles, ragged both ways
+    (B, 192, 1, UE8M0, 300, 1003, 1024, False),    # N % 8 != 0: element stores, two issuers
+    (B, 192, 3, UE8M0, 300, 1003, 1024, False),
+    (B, 256, 1, UE8M0, 300, 1003, 1024, False),
     (PAIR, 128, 1, UE8M0, 600, 1000, 640, False),   # the last pair's second CTA past M
     (PAIR, 192, 1, UE8M0, 600, 1000, 640, False),
     (PAIR, 256, 1, UE8M0, 600, 1000, 640, False),
