@@ -14,12 +14,13 @@
 //   warps 4 .. 7   epilogue: read the finished accumulator, round to bf16, store
 //   warp 8         TMA producer
 //   warp 9         MMA issuer (allocates and frees TMEM)
-//   warp 10        BN = 64 only: a second MMA issuer. The two take a tile's K blocks in turn,
-//                  each into its own accumulator; the epilogue adds the two. One thread
-//                  issuing alone waits for its MMAs to drain at every barrier wait, which at
-//                  this width costs more than the MMAs themselves (MLA N = 576: 22.2 us with
-//                  one issuer, 17.9-18.3 us with two).
-// TMEM: two accumulator buffers (BN columns per issuer), then per stage 8 columns of scale
+//   warp 10        BN = 64 and 192: a second MMA issuer. The two take a tile's K blocks in
+//                  turn, each into its own accumulator; the epilogue adds the two. One thread
+//                  issuing alone advances one K block per ~650-770 clk at these widths,
+//                  more than the MMAs take (MLA N = 576: 22.2 us with one issuer, 17.9-18.3 us
+//                  with two; N = 1536 at 192: 26.6 and 23.2 us).
+// TMEM: accumulator buffers of BN columns per issuer (two, or one at BN > 128), then per stage
+// 8 or 12 columns of scale
 // factors (4 for A, 4 or 8 for B). A stage's full barrier completes when its TMA bytes have
 // landed AND the four scale-factor warps have written its slot; the MMA's commit to the
 // stage's empty barrier frees both.
@@ -59,8 +60,9 @@ struct BsCfg {
     // MMA issuers: two at BN = 64 and 192, taking a tile's K blocks in turn into accumulators
     // of their own (one thread issuing alone advances one K block per ~650-770 clk at these
     // widths whatever N is; the MLA q projection, 128 tiles of 192, went from 26.6 to 23.2 us).
-    // 128 keeps one (two buffers of two accumulators would not fit in TMEM, and one buffer
-    // loses the epilogue overlap its many-round shapes need); 256 has no room for a second.
+    // A third at 64 changed nothing (MLA kv projection 17.7 us either way). 128 keeps one (two
+    // buffers of two accumulators would not fit in TMEM, and one buffer loses the epilogue
+    // overlap its many-round shapes need); 256 has no room for a second.
     static constexpr int ISSUERS = (BN <= 64 || BN == 192) ? 2 : 1;
     static constexpr int THREADS = 32 * (SF_WARPS + EPI_WARPS + 1 + ISSUERS);
     static constexpr int B_TILE = BN * BK;
@@ -106,6 +108,22 @@ __device__ __forceinline__ void release_tmem(uint64_t* tempty, int lane) {
     tc_fence_before();
     __syncwarp();
     if (lane == 0) mbar_arrive(tempty);
+}
+
+// With several MMA issuers (issuer i's accumulator BN columns after issuer 0's): add to v the
+// 32 columns at `taddr` of the accumulators of issuers 1 .. nacc-1, in issuer order.
+template <int BN, int ISSUERS>
+__device__ __forceinline__ void add_issuer_accs(uint32_t taddr, int nacc, float* v) {
+#pragma unroll
+    for (int i = 1; i < ISSUERS; ++i) {
+        if (i < nacc) {
+            float t[32];
+            tmem_ld_32cols(taddr + static_cast<uint32_t>(i * BN), t);
+            tmem_wait_ld_32(t);
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] += t[k];
+        }
+    }
 }
 
 template <int BN>
@@ -367,8 +385,9 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * Cfg::ACC);
-            // the second issuer's accumulator (BN columns on) holds K blocks kb0 + 1, kb0 + 3..
-            const bool two = Cfg::ISSUERS > 1 && kb1 - kb0 > 1;
+            // Issuer i's accumulator (i x BN columns on) holds K blocks kb0 + i, kb0 + i +
+            // ISSUERS, ...: the first nacc issuers received some.
+            const int nacc = min(Cfg::ISSUERS, kb1 - kb0);
             if (split) {
                 // Split K: once every CTA of the cluster is past its K loop (its stage memory
                 // free), send each slice of the accumulator to the CTA that adds that slice up;
@@ -381,15 +400,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     float v[32];
                     tmem_ld_32cols(taddr + 32 * c, v);
                     tmem_wait_ld_32(v);
-                    if constexpr (Cfg::ISSUERS > 1) {
-                        if (two) {
-                            float u[32];
-                            tmem_ld_32cols(taddr + BN + 32 * c, u);
-                            tmem_wait_ld_32(u);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += u[i];
-                        }
-                    }
+                    add_issuer_accs<BN, Cfg::ISSUERS>(taddr + 32 * c, nacc, v);
 #pragma unroll
                     for (int j = 0; j < 8; ++j)
                         split_push4(sp, row_in_tile, 32 * c + 4 * j,
@@ -417,7 +428,8 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     // A whole 192- or 256-wide tile: the row into registers as bf16 pairs, the
                     // buffer back (at BN = 256 the only one: the next tile's MMAs wait for it),
                     // then store. Storing between the loads held the buffer ~9K clk per tile.
-                    drain_row_bf16<BN>(taddr, crow, store, valid, vec, two, scratch, wr, lane,
+                    static_assert(BN <= 128 || Cfg::ISSUERS <= 2, "the wide epilogue adds two");
+                    drain_row_bf16<BN>(taddr, crow, store, valid, vec, nacc > 1, scratch, wr, lane,
                                        [&] { release_tmem(&ring.tempty[buf], lane); });
                 } else {
                     // A whole tile: the accumulator into registers, the buffer back, then store.
@@ -426,18 +438,9 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     for (int c = 0; c < BN / 32; ++c) tmem_ld_32cols(taddr + 32 * c, acc + 32 * c);
 #pragma unroll
                     for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(acc + 32 * c);
-                    if constexpr (Cfg::ISSUERS > 1) {
-                        if (two) {
-                            float t[BN];
 #pragma unroll
-                            for (int c = 0; c < BN / 32; ++c)
-                                tmem_ld_32cols(taddr + BN + 32 * c, t + 32 * c);
-#pragma unroll
-                            for (int c = 0; c < BN / 32; ++c) tmem_wait_ld_32(t + 32 * c);
-#pragma unroll
-                            for (int i = 0; i < BN; ++i) acc[i] += t[i];
-                        }
-                    }
+                    for (int c = 0; c < BN / 32; ++c)
+                        add_issuer_accs<BN, Cfg::ISSUERS>(taddr + 32 * c, nacc, acc + 32 * c);
                     release_tmem(&ring.tempty[buf], lane);
                     if (Cfg::SCRATCH > 0 && vec) {
                         uint32_t pk[BN / 2];
@@ -457,15 +460,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     float v[32];
                     tmem_ld_32cols(taddr + 32 * c, v);
                     tmem_wait_ld_32(v);
-                    if constexpr (Cfg::ISSUERS > 1) {
-                        if (two) {
-                            float t[32];
-                            tmem_ld_32cols(taddr + BN + 32 * c, t);
-                            tmem_wait_ld_32(t);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += t[i];
-                        }
-                    }
+                    add_issuer_accs<BN, Cfg::ISSUERS>(taddr + 32 * c, nacc, v);
 #pragma unroll
                     for (int q = 0; q < 8; ++q)
                         __stcg(slot + (8 * c + q) * BM + row_in_tile,
@@ -488,15 +483,7 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
                     float v[32];
                     tmem_ld_32cols(taddr + 32 * c, v);
                     tmem_wait_ld_32(v);
-                    if constexpr (Cfg::ISSUERS > 1) {
-                        if (two) {
-                            float t[32];
-                            tmem_ld_32cols(taddr + BN + 32 * c, t);
-                            tmem_wait_ld_32(t);
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += t[i];
-                        }
-                    }
+                    add_issuer_accs<BN, Cfg::ISSUERS>(taddr + 32 * c, nacc, v);
                     if (have) {
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
