@@ -472,6 +472,8 @@ def test_gemm_ue8m0_reports_a_scale_that_is_not_a_power_of_two():
     ([0, 130, 5, 0, 257, 1], 384, 256),
     ([64] * 8, 576, 512),
     ([300, 0, 200], 2048, 256),
+    ([600, 0, 700, 650, 100], 1536, 256),    # 192-wide tiles (two issuers, one buffer); the
+                                             # coalesced stores stop at each group's last row
 ])
 def test_gemm_grouped_ue8m0_block_scaled(counts, N, K):
     grouped_check(counts, N, K, seed=sum(counts) + N + 1, what=f"grouped ue8m0 {counts}",

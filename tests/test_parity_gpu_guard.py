@@ -100,6 +100,8 @@ GEMM_CASES = [
     (2560, 2304, 1024, 0, True),    # promoted, stream-K (192-wide tiles)
     (1100, 4736, 256, 0, False),    # promoted, 256-wide tiles
     (2600, 3900, 384, 1, False),    # block-scaled, 256-wide tiles, ragged both ways
+    (2600, 4096, 384, 1, False),    # block-scaled, 256-wide tiles, stores through the scratch
+    (2000, 1536, 640, 1, False),    # block-scaled, 192-wide tiles (two issuers), scratch stores
     (1100, 2500, 2048, 1, True),    # block-scaled, stream-K
     (512, 576, 7168, 1, False),     # block-scaled, 192-wide tiles, split K
     (2048, 1300, 640, 1, False),    # block-scaled, 192-wide whole tiles, N tail
@@ -119,14 +121,18 @@ def test_gemm_guard_bands(M, N, K, fmt, with_ws):
     c.check(f"gemm {M}x{N}x{K} fmt={fmt} workspace={with_ws}")
 
 
-@pytest.mark.parametrize("fmt", [0, 1])
-def test_grouped_gemm_guard_bands(fmt):
-    counts = [0, 130, 5, 0, 257, 1]
-    N, K = 384, 256
+@pytest.mark.parametrize("fmt,counts,N", [
+    (0, [0, 130, 5, 0, 257, 1], 384),
+    (1, [0, 130, 5, 0, 257, 1], 384),
+    (1, [600, 0, 700, 650, 100], 1536),      # 192-wide tiles, stores through the scratch
+])
+def test_grouped_gemm_guard_bands(fmt, counts, N):
+    K = 256
     offs = np.r_[0, np.cumsum(counts)]
     T = int(offs[-1])
     A, AS, _, _ = gemm_inputs(T, N, K, fmt, seed=3)
-    ws = [synth.weights(N, K, seed=10 + e, name="guardG", pow2=fmt == 1) for e in range(6)]
+    ws = [synth.weights(N, K, seed=10 + e, name="guardG", pow2=fmt == 1)
+          for e in range(len(counts))]
     B = dev_e4m3(np.stack([w for w, _ in ws]))
     BS = dev_f32(np.stack([s for _, s in ws]))
     c = Guarded((T, N), torch.bfloat16)
