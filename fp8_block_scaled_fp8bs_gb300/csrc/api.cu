@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <vector>
 #include <cstdint>
 #include <mutex>
 
@@ -670,27 +671,52 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     // side, their few rows on its N side, as at decode), the others as 128-row tiles. With both
     // kinds, the small groups' launch follows the other one without waiting for it (the two
     // write disjoint rows of C): its CTAs take the SMs the first launch's last round leaves
-    // idle.
-    int64_t small_max = 0, small_count = 0;
+    // idle. The small groups' launch takes one CTA per 128-row weight slab of each group: where
+    // that is a little more than one wave (10 MoE experts x 16 slabs on 152 SMs took 48 us for
+    // 147 MB of weights), its largest groups join the tiles instead, provided they add no round
+    // to the tile launch.
+    const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
+    const int64_t slabs = ceil_div(N, 128);
+    auto tile_rounds = [&](int64_t m_tiles) {
+        if (m_tiles == 0) return static_cast<int64_t>(0);
+        const int bn = block_scaled ? fp8bs::pick_tile_n_bs(m_tiles, N, sms)
+                                    : fp8bs::pick_tile_n(m_tiles, N, sms);
+        return ceil_div(m_tiles * ceil_div(N, bn), sms);
+    };
+    std::vector<int64_t> cand;                     // groups of 1 .. 64 rows, fewest rows first
+    int64_t m_big = 0;
     for (int64_t i = 0; i < groups; ++i) {
         const int64_t rows = row_offsets[i + 1] - row_offsets[i];
-        if (rows > 0 && rows <= 64) {
-            small_max = std::max(small_max, rows);
-            ++small_count;
-        }
+        if (rows > 0 && rows <= 64)
+            cand.push_back(i);
+        else
+            m_big += (rows + 127) / 128;
     }
+    std::stable_sort(cand.begin(), cand.end(), [&](int64_t x, int64_t y) {
+        return row_offsets[x + 1] - row_offsets[x] < row_offsets[y + 1] - row_offsets[y];
+    });
+    int64_t keep = static_cast<int64_t>(cand.size());
+    if (m_big > 0 && keep * slabs > sms && keep * slabs < 2 * static_cast<int64_t>(sms)) {
+        const int64_t fit = sms / slabs;
+        if (tile_rounds(m_big + (keep - fit)) <= tile_rounds(m_big)) keep = fit;
+    }
+    int64_t small_max = 0;
+    for (int64_t j = 0; j < keep; ++j)
+        small_max = std::max(small_max, row_offsets[cand[j] + 1] - row_offsets[cand[j]]);
+    const int64_t small_count = keep;
     const int MT = small_max <= 16 ? 16 : small_max <= 32 ? 32 : 64;
     int S = 0;
     if (small_count > 0)      // 0: K too long for the swapped kernel, every group as tiles
         S = fp8bs::plan_gemm_swapab(MT, false, static_cast<int>(small_count), g.N, g.K, sms);
-    const int64_t small_rows = S > 0 ? 64 : 0;
-    auto is_small = [&](int64_t rows) { return rows > 0 && rows <= small_rows; };
+    std::vector<char> small(static_cast<size_t>(groups), 0);
+    if (S > 0)
+        for (int64_t j = 0; j < keep; ++j) small[static_cast<size_t>(cand[j])] = 1;
+    auto is_small = [&](int64_t i) { return small[static_cast<size_t>(i)] != 0; };
 
-    const bool block_scaled = scale_fmt == FP8BS_SCALE_UE8M0;
     int64_t m_tiles_total = 0;
     for (int64_t i = 0; i < groups; ++i) {
         const int64_t rows = row_offsets[i + 1] - row_offsets[i];
-        if (!is_small(rows)) m_tiles_total += (rows + 127) / 128;
+        if (!is_small(i)) m_tiles_total += (rows + 127) / 128;
     }
     bool launched = false;
     if (m_tiles_total > 0) {
@@ -706,7 +732,7 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
             const int64_t rows = row_offsets[i + 1] - row_offsets[i];
             gt.row_off[i + 1] = static_cast<int>(row_offsets[i + 1]);
             gt.tile_off[i + 1] =
-                gt.tile_off[i] + (is_small(rows) ? 0 : static_cast<int>((rows + 127) / 128)) * n_tiles;
+                gt.tile_off[i] + (is_small(i) ? 0 : static_cast<int>((rows + 127) / 128)) * n_tiles;
         }
         CUtensorMap tmA, tmB;
         if (!make_map(&tmA, a, M, K, 128) || !make_map(&tmB, b, N * groups, K, BN))
@@ -725,7 +751,7 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
         for (int64_t i = 0; i < groups; ++i) {
             gt.row_off[i + 1] = static_cast<int>(row_offsets[i + 1]);
             gt.tile_off[i + 1] =
-                gt.tile_off[i] + (is_small(row_offsets[i + 1] - row_offsets[i]) ? 1 : 0);
+                gt.tile_off[i] + (is_small(i) ? 1 : 0);
         }
         CUtensorMap tmA, tmB;
         if (!make_map(&tmB, b, N * groups, K, 128) || !make_map(&tmA, a, M, K, MT))

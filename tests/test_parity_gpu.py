@@ -364,6 +364,10 @@ def test_gemm_grouped_against_oracle(counts, N, K):
     ([3, 17, 40], 1000, 2048, "fp32"),         # ragged N, the K loop split in clusters
     ([0, 5, 0, 64, 2], 576, 1024, "ue8m0"),
     ([200, 3, 0, 64, 130, 1], 384, 512, "fp32"),  # both launches: tiles, then swapped groups
+    # ten small groups x 16 weight slabs would be 160 CTAs on 152 SMs: the largest small group
+    # (64 rows) joins the tiles as one padded tile, the other nine stay in the swapped launch
+    ([300, 40, 3, 17, 64, 1, 9, 33, 50, 12, 28], 2048, 256, "fp32"),
+    ([300, 40, 3, 17, 64, 1, 9, 33, 50, 12, 28], 2048, 256, "ue8m0"),
 ])
 def test_gemm_grouped_small_groups(counts, N, K, fmt):
     """Groups of at most 64 rows run in the swapped orientation (with other groups: as a
