@@ -1,0 +1,122 @@
+"""Seeded random shapes through the public entry points, every output element against the oracle.
+
+The hand-picked parity cases pin each schedule on shapes chosen to reach it; here a fixed seed
+draws M, N, K, the scale format and whether a stream-K workspace is passed, and the library's
+own plan decides the kernel, tile width, K split or stream-K for each draw (the plan is printed
+in the failure message). Shapes are kept small enough (at most ~2e8 multiply-adds each) for
+the oracle to finish in about a second. act_quant and weight_dequant are compared bit for bit,
+the GEMMs within the bound of "DeepSeek-V3 Administrator & Developer Guide" §8.5.3's fp32
+accumulation (parity_util.assert_gemm_close), and two calls in a row must agree bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import fp8_block_scaled_fp8bs_gb300 as fp8bs
+import oracle
+import synth
+from parity_util import assert_gemm_close, dev_bf16, dev_e4m3, dev_f32, host_bf16_f64
+
+pytestmark = pytest.mark.gpu
+
+FMTS = {"fp32": oracle.SCALE_FP32, "ue8m0": oracle.SCALE_UE8M0}
+
+
+@pytest.fixture(autouse=True)
+def _clean_device_error():
+    fp8bs.fp8bs_device_error(clear=True)
+    yield
+    torch.cuda.synchronize()
+    assert fp8bs.fp8bs_device_error(clear=True) == 0, "a kernel wait ran out"
+
+
+def draw_gemm(i):
+    """Case i: M from decode-sized to a few row tiles, N ragged or a multiple of 8, K a multiple
+    of 128, capped so that M * N * K <= 2e8."""
+    rng = np.random.default_rng(1000 + i)
+    M = int(rng.choice([int(rng.integers(1, 129)), int(rng.integers(129, 1300))]))
+    N = int(rng.integers(1, 2600))
+    if rng.random() < 0.5:
+        N = max(8, N // 8 * 8)
+    K = 128 * int(rng.integers(1, 30))
+    while M * N * K > 2e8:
+        if K > 128:
+            K = 128 * max(1, K // 256)
+        else:
+            N = max(1, N // 2)
+    fmt = "ue8m0" if rng.random() < 0.5 else "fp32"
+    with_ws = bool(rng.random() < 0.5)
+    return M, N, K, fmt, with_ws
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_gemm_random_shapes(i):
+    M, N, K, fmt, with_ws = draw_gemm(i)
+    x = synth.activations(M, K, seed=i, name="fuzzA", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x, FMTS[fmt])
+    b, b_s = synth.weights(N, K, seed=i + 7, name="fuzzB", pow2=fmt == "ue8m0")
+    ws = torch.zeros(fp8bs.fp8bs_gemm_workspace_size(), dtype=torch.uint8, device="cuda") \
+        if with_ws else None
+    plan = fp8bs.fp8bs_gemm_plan(M, N, K, fp8bs._fmt(fmt), with_ws)
+    A, AS, B, BS = dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s)
+    c1 = fp8bs.fp8_gemm(A, AS, B, BS, fmt, workspace=ws)
+    c2 = fp8bs.fp8_gemm(A, AS, B, BS, fmt, workspace=ws)
+    torch.cuda.synchronize()
+    what = f"case {i}: {M}x{N}x{K} {fmt} workspace={with_ws} plan={plan}"
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16)), f"{what}: two calls differ"
+    assert_gemm_close(host_bf16_f64(c1), oracle.gemm(a, a_s, b, b_s), what)
+
+
+@pytest.mark.parametrize("i", range(8))
+def test_grouped_random_shapes(i):
+    """Random group sizes (empty, decode-sized, a few tiles), N and K: both of the grouped
+    call's launches, and the choice between them, on shapes drawn at random."""
+    rng = np.random.default_rng(2000 + i)
+    G = int(rng.integers(1, 12))
+    counts = [int(rng.choice([0, int(rng.integers(1, 65)), int(rng.integers(65, 400))]))
+              for _ in range(G)]
+    N = int(rng.choice([int(rng.integers(1, 700)), 8 * int(rng.integers(1, 200))]))
+    K = 128 * int(rng.integers(1, 8))
+    fmt = "ue8m0" if rng.random() < 0.5 else "fp32"
+    offs = np.r_[0, np.cumsum(counts)]
+    T = int(offs[-1])
+    if T == 0:
+        counts[0] = 1
+        offs = np.r_[0, np.cumsum(counts)]
+        T = 1
+    x = synth.activations(T, K, seed=i, name="fuzzG", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x, FMTS[fmt])
+    ws = [synth.weights(N, K, seed=i + 1 + e, name="fuzzGB", pow2=fmt == "ue8m0")
+          for e in range(G)]
+    b = np.stack([w for w, _ in ws])
+    b_s = np.stack([s for _, s in ws])
+    c = host_bf16_f64(fp8bs.fp8_gemm_grouped(dev_e4m3(a), dev_f32(a_s), dev_e4m3(b),
+                                             dev_f32(b_s), offs, fmt))
+    torch.cuda.synchronize()
+    for e in range(G):
+        lo, hi = offs[e], offs[e + 1]
+        if hi > lo:
+            assert_gemm_close(c[lo:hi], oracle.gemm(a[lo:hi], a_s[lo:hi], b[e], b_s[e]),
+                              f"case {i}: group {e} of {counts}, N={N} K={K} {fmt}")
+
+
+@pytest.mark.parametrize("i", range(12))
+def test_act_quant_and_dequant_random_shapes(i):
+    rng = np.random.default_rng(3000 + i)
+    M = int(rng.integers(1, 3000))
+    K = 128 * int(rng.integers(1, 40))
+    fmt = "ue8m0" if rng.random() < 0.5 else "fp32"
+    x = synth.activations(M, K, seed=i, name="fuzzQ", outlier_frac=0.02)
+    y, s = fp8bs.act_quant(dev_bf16(x), fmt)
+    torch.cuda.synchronize()
+    y_ref, s_ref = oracle.act_quant(x, FMTS[fmt])
+    assert np.array_equal(y.view(torch.uint8).cpu().numpy(), y_ref), f"case {i}: codes {M}x{K}"
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_ref.view(np.uint32)), \
+        f"case {i}: scales {M}x{K}"
+    N = int(rng.integers(1, 1500))
+    Kw = int(rng.integers(1, 1500))
+    w, w_s = synth.weights(N, Kw, seed=i + 3, name="fuzzW")
+    d = fp8bs.weight_dequant(dev_e4m3(w), dev_f32(w_s))
+    torch.cuda.synchronize()
+    assert np.array_equal(d.view(torch.int16).cpu().numpy().view(np.uint16),
+                          oracle.weight_dequant(w, w_s)), f"case {i}: weight_dequant {N}x{Kw}"
