@@ -20,10 +20,9 @@
 //                  more than the MMAs take (MLA N = 576: 22.2 us with one issuer, 17.9-18.3 us
 //                  with two; N = 1536 at 192: 26.6 and 23.2 us).
 // TMEM: accumulator buffers of BN columns per issuer (two, or one at BN > 128), then per stage
-// 8 or 12 columns of scale
-// factors (4 for A, 4 or 8 for B). A stage's full barrier completes when its TMA bytes have
-// landed AND the four scale-factor warps have written its slot; the MMA's commit to the
-// stage's empty barrier frees both.
+// 8 or 12 columns of scale factors (4 for A, 4 or 8 for B). A stage's full barrier completes
+// when its TMA bytes have landed AND the four scale-factor warps have written its slot; the
+// MMA's commit to the stage's empty barrier frees both.
 //
 // Scale-factor placement. The tensor core takes the exponent of row m of A from lane m,
 // column m/32 of the A slot, and the exponent of row n of B (for output rows of lane quarter q)
