@@ -4,7 +4,6 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
-#include <vector>
 #include <cstdint>
 #include <mutex>
 
@@ -683,19 +682,19 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
                                     : fp8bs::pick_tile_n(m_tiles, N, sms);
         return ceil_div(m_tiles * ceil_div(N, bn), sms);
     };
-    std::vector<int64_t> cand;                     // groups of 1 .. 64 rows, fewest rows first
-    int64_t m_big = 0;
+    int64_t cand[fp8bs::kMaxGroups];               // groups of 1 .. 64 rows, fewest rows first
+    int64_t n_cand = 0, m_big = 0;
     for (int64_t i = 0; i < groups; ++i) {
         const int64_t rows = row_offsets[i + 1] - row_offsets[i];
         if (rows > 0 && rows <= 64)
-            cand.push_back(i);
+            cand[n_cand++] = i;
         else
             m_big += (rows + 127) / 128;
     }
-    std::stable_sort(cand.begin(), cand.end(), [&](int64_t x, int64_t y) {
+    std::stable_sort(cand, cand + n_cand, [&](int64_t x, int64_t y) {
         return row_offsets[x + 1] - row_offsets[x] < row_offsets[y + 1] - row_offsets[y];
     });
-    int64_t keep = static_cast<int64_t>(cand.size());
+    int64_t keep = n_cand;
     if (m_big > 0 && keep * slabs > sms && keep * slabs < 2 * static_cast<int64_t>(sms)) {
         const int64_t fit = sms / slabs;
         if (tile_rounds(m_big + (keep - fit)) <= tile_rounds(m_big)) keep = fit;
@@ -708,10 +707,10 @@ int fp8bs_gemm_grouped(const void* a, const float* a_s, const void* b, const flo
     int S = 0;
     if (small_count > 0)      // 0: K too long for the swapped kernel, every group as tiles
         S = fp8bs::plan_gemm_swapab(MT, false, static_cast<int>(small_count), g.N, g.K, sms);
-    std::vector<char> small(static_cast<size_t>(groups), 0);
+    bool small[fp8bs::kMaxGroups] = {};
     if (S > 0)
-        for (int64_t j = 0; j < keep; ++j) small[static_cast<size_t>(cand[j])] = 1;
-    auto is_small = [&](int64_t i) { return small[static_cast<size_t>(i)] != 0; };
+        for (int64_t j = 0; j < keep; ++j) small[cand[j]] = true;
+    auto is_small = [&](int64_t i) { return small[i]; };
 
     int64_t m_tiles_total = 0;
     for (int64_t i = 0; i < groups; ++i) {
