@@ -125,11 +125,21 @@ __device__ __forceinline__ void add_issuer_accs(uint32_t taddr, int nacc, float*
     }
 }
 
-template <int BN>
+// PLAIN: whole tiles only (no stream-K workspace, no split K). Its instantiation compiles the
+// schedule with those fixed, which drops the stream-K and split-K paths: the MLA projections
+// (whole tiles) ran ~4 % faster that way (N = 576: 18.35 -> 17.6 us; N = 1536: 23.2 -> 22.3 us).
+template <int BN, bool PLAIN>
 __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     gemm_bs_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmArgs g, const __grid_constant__ GroupTable gt, const int stages,
-                   const StreamK sk) {
+                   const StreamK sk_arg) {
+    StreamK sk = sk_arg;
+    if constexpr (PLAIN) {
+        sk.parts = nullptr;
+        sk.flags = nullptr;
+        sk.ksplit = 1;
+        sk.dp_tiles = 0;
+    }
     using Cfg = BsCfg<BN>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
@@ -893,20 +903,24 @@ cudaError_t launch_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const Gemm
     const int smem = bs_smem<BN>(stream_k);
     if (ska.ksplit > 1 && split_recv_bytes(BN, ska.ksplit) > stages * Cfg::STAGE)
         return cudaErrorInvalidValue;
-    cudaError_t e = set_smem(gemm_bs_kernel<BN>, kSmemLimit);
+    const bool plain = !stream_k && ska.ksplit <= 1;
+    auto kernel = plain ? gemm_bs_kernel<BN, true> : gemm_bs_kernel<BN, false>;
+    cudaError_t e = set_smem(kernel, kSmemLimit);
     if (e != cudaSuccess) return e;
     const int tiles = gt.tile_off[gt.num_groups];
     if (tiles == 0) return cudaSuccess;
     StreamK sk = {nullptr, nullptr, 0, 1};
     const int grid = stream_k_grid(ska, tiles, g.K / BK, num_sms, &sk);
-    e = launch_pdl_cluster(gemm_bs_kernel<BN>, grid, Cfg::THREADS, smem, stream, sk.ksplit,
-                           stream_k, tmA, tmB, g, gt, stages, sk);
+    e = launch_pdl_cluster(kernel, grid, Cfg::THREADS, smem, stream, sk.ksplit, stream_k, tmA, tmB,
+                           g, gt, stages, sk);
     if (e == cudaSuccess || !stream_k) return e;
     // The runtime could not place every CTA of the stream-K grid at once (fewer SMs available
     // to this context than the plan assumed): whole tiles instead, which need no co-residency.
     cudaGetLastError();
     const StreamK whole = {nullptr, nullptr, 0, 1};
-    return launch_pdl_cluster(gemm_bs_kernel<BN>, tiles < num_sms ? tiles : num_sms,
+    e = set_smem(gemm_bs_kernel<BN, true>, kSmemLimit);
+    if (e != cudaSuccess) return e;
+    return launch_pdl_cluster(gemm_bs_kernel<BN, true>, tiles < num_sms ? tiles : num_sms,
                               Cfg::THREADS, bs_smem<BN>(false), stream, 1, false, tmA, tmB, g,
                               gt, bs_stages<BN>(false), whole);
 }
@@ -915,11 +929,11 @@ template <int BN>
 int split_clusters_bs(int S) {
     using Cfg = BsCfg<BN>;
     if (split_recv_bytes(BN, S) > bs_stages<BN>(false) * Cfg::STAGE) return 0;
-    if (set_smem(gemm_bs_kernel<BN>, kSmemLimit) != cudaSuccess) {
+    if (set_smem(gemm_bs_kernel<BN, false>, kSmemLimit) != cudaSuccess) {
         cudaGetLastError();
         return 0;
     }
-    return max_active_clusters(reinterpret_cast<const void*>(gemm_bs_kernel<BN>), Cfg::THREADS,
+    return max_active_clusters(reinterpret_cast<const void*>(gemm_bs_kernel<BN, false>), Cfg::THREADS,
                                bs_smem<BN>(false), S);
 }
 
