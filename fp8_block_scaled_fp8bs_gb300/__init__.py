@@ -288,7 +288,7 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False,
 def act_quant_gemm(x, b, b_s, scale_fmt="fp32", weights_constant=False, workspace="auto",
                    quant_in_kernel=False):
     """linear() on the FP8 path: x bf16 [M,K] -> (c bf16 [M,N], y e4m3 [M,K], s fp32
-    [M,K/128]): act_quant then the GEMM (quant_in_kernel: one kernel, M <= 64); see fp8_gemm
+    [M,K/128]): act_quant then the GEMM (quant_in_kernel: one kernel, M <= 16); see fp8_gemm
     for `workspace`."""
     import torch
     _require(x, torch.bfloat16, 2, "x")

@@ -135,21 +135,6 @@ bool make_map_bf16_sw128(CUtensorMap* map, const void* base, int64_t rows, int64
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The same over a row-major bf16 matrix [rows, K], box {128 elements, box_rows}, no swizzle
-// (the decode GEMM quantises these rows itself).
-bool make_map_bf16(CUtensorMap* map, const void* base, int64_t rows, int64_t K, int box_rows) {
-    EncodeTiledFn enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
-    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
-    const cuuint32_t box[2] = {128u, static_cast<cuuint32_t>(box_rows)};
-    const cuuint32_t estr[2] = {1u, 1u};
-    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-               box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 int status_of(cudaError_t e) { return e == cudaSuccess ? FP8BS_OK : FP8BS_ERR_CUDA; }
 
 // Stream-K plans (see StreamKArgs in kernels.h). Whole tiles for all but the last one to two
@@ -517,9 +502,10 @@ int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b, const 
         if (workspace_bytes < fp8bs::stream_k_workspace(sms)) return FP8BS_ERR_INVALID_ARG;
     }
     const bool ue8m0 = scale_fmt == FP8BS_SCALE_UE8M0;
-    if (in_kernel && M <= 64) {
-        // One launch: the decode GEMM quantises the rows of each K block it reads.
-        const int MT = M <= 16 ? 16 : M <= 32 ? 32 : 64;
+    if (in_kernel && M <= 16) {
+        // One launch: every CTA of the decode GEMM quantises x (at most 16 rows) before its
+        // main loop.
+        const int MT = 16;
         GemmArgs g;
         g.a_s = s;
         g.b_s = b_s;
@@ -538,13 +524,13 @@ int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void* b, const 
         const int row_tiles = (g.M + MT - 1) / MT;
         if (fp8bs::plan_gemm_swapab(MT, false, row_tiles, g.N, g.K, sms) == 1 &&
             fp8bs::plan_gemm_swapab(MT, true, row_tiles, g.N, g.K, sms) == 1) {
-            CUtensorMap tmA, tmB;
-            if (!make_map(&tmB, b, N, K, 128) || !make_map_bf16(&tmA, x, M, K, MT))
-                return FP8BS_ERR_CUDA;
+            // x is read directly (no tensor map): tmB stands in for the unused map of A.
+            CUtensorMap tmB;
+            if (!make_map(&tmB, b, N, K, 128)) return FP8BS_ERR_CUDA;
             const int64_t rows[2] = {0, M};
             fp8bs::GroupTable gt;
             fp8bs::fill_row_tiles(&gt, rows, 1, MT);
-            return status_of(fp8bs::launch_gemm_swapab(tmB, tmA, g, gt, MT, fq, 1, false, st));
+            return status_of(fp8bs::launch_gemm_swapab(tmB, tmB, g, gt, MT, fq, 1, false, st));
         }
         // K too long to stage the scales, or a split K loop: two launches below.
     }

@@ -13,12 +13,14 @@
 // Two ways in for the activations:
 //   quantised (fp8bs_gemm): TMA brings e4m3 rows of A; their scales are staged in shared memory
 //       transposed to [kb][m] before the main loop.
-//   bf16 (fp8bs_act_quant_gemm, FUSED): TMA brings each K block's bf16 rows of x, and four
-//       quantiser warps turn them into the e4m3 tile the MMA reads (128-byte swizzle) and the
-//       block's scales, with act_quant's arithmetic ("DeepSeek-V3 Administrator & Developer
-//       Guide", §8.5.1) -- every CTA quantises the rows it needs, so no kernel and no grid-wide
-//       synchronisation stands between the previous layer and this GEMM; the CTAs of the first
-//       weight slab also write y and s.
+//   bf16 (fp8bs_act_quant_gemm, FUSED; at most 16 rows): before its main loop every CTA reads
+//       x (bf16) and quantises all of it with act_quant's arithmetic ("DeepSeek-V3 Administrator
+//       & Developer Guide", §8.5.1) into a resident e4m3 operand -- one 16-row tile per K block
+//       in the layout TMA would have written (128-byte swizzle) -- and its block scales, while
+//       the weight ring fills. No kernel and no grid-wide synchronisation stands between the
+//       previous layer and this GEMM; the CTAs of the first weight slab also write y and s.
+//       (Quantising each K block as its stage arrived, with a proxy fence per block, ran at
+//       ~1030 clk per K block against ~700 for the weight stream.)
 #include "gemm_common.cuh"
 #include "quant_math.cuh"
 
@@ -28,34 +30,27 @@ namespace {
 
 template <int MT, bool FUSED>
 struct SwapCfg {
+    static_assert(!FUSED || MT == 16, "in-kernel quantisation: 16-row tiles");
     static constexpr int EPI_WARPS = 4;
     static constexpr int Q_WARPS = FUSED ? 4 : 0;   // quantiser warps, after the promotion warps
     static constexpr int Q_WARP0 = 2 + EPI_WARPS;
     static constexpr int S_WARPS = FUSED ? 0 : 1;   // scale warp (quantised input), same place
     static constexpr int THREADS = 64 + 32 * (EPI_WARPS + Q_WARPS + S_WARPS);
-    static constexpr int X_TILE = MT * BK;          // e4m3 activation rows per stage
-    static constexpr int XB_TILE = FUSED ? MT * BK * 2 : 0;   // bf16 rows per stage (FUSED)
-    static constexpr int STAGE = A_TILE + X_TILE + XB_TILE;
-    static constexpr int TX_BYTES = A_TILE + (FUSED ? XB_TILE : X_TILE);  // bytes TMA brings
+    static constexpr int X_TILE = MT * BK;          // e4m3 activation rows of one K block
+    // A stage: a weight tile and (quantised input) the activation tile; FUSED keeps the
+    // activations resident instead.
+    static constexpr int STAGE = A_TILE + (FUSED ? 0 : X_TILE);
+    static constexpr int TX_BYTES = STAGE;          // bytes TMA brings per stage
     static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * MT);
 };
 
-// Shared-memory bytes after the stages, for a CTA that takes nkb K blocks: transposed scales
-// [nkb][MT], then (quantised input) the raw a_s rows [MT][nkb] or (FUSED) a ready count per K
-// block, the b_s row, and (FUSED) one "quantised" barrier per stage.
+// Shared-memory bytes after the stages, for a CTA that takes nkb K blocks: (FUSED) the
+// resident e4m3 activation tiles [nkb][MT x 128], then the transposed scales [nkb][MT], then
+// (quantised input) the raw a_s rows [MT][nkb], and the b_s row.
 template <int MT, bool FUSED>
 __host__ __device__ constexpr int swap_scale_bytes(int nkb) {
-    return nkb * MT * 4 + (FUSED ? nkb * 4 : nkb * MT * 4) + ((nkb + 3) & ~3) * 4 + 16;
-}
-
-// Bounded spin until *p == target (a shared-memory count written by other warps).
-__device__ __forceinline__ bool spin_until_equal(const int* p, int target) {
-    const volatile int* v = p;
-    if (*v == target) return true;
-    const uint64_t t0 = global_timer_ns();
-    while (*v != target)
-        if (global_timer_ns() - t0 > kWaitLimitNs) return false;
-    return true;
+    return (FUSED ? nkb * MT * BK : 0) + nkb * MT * 4 + (FUSED ? 0 : nkb * MT * 4) +
+           ((nkb + 3) & ~3) * 4 + 16;
 }
 
 // Bounded spin until *p >= target.
@@ -96,8 +91,8 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = align_1024(smem_raw);
     uint8_t* sW = smem;                                   // [stages][128 x 128] weights
-    uint8_t* sX = smem + stages * A_TILE;                 // [stages][MT x 128] e4m3 activations
-    uint8_t* sXb = sX + stages * Cfg::X_TILE;             // [stages][MT x 128] bf16 (FUSED)
+    // [stages][MT x 128] e4m3 activations, or (FUSED) [num_kb][MT x 128] resident
+    uint8_t* sX = smem + stages * A_TILE;
     const int num_kb = g.K / BK;
     // This CTA's slab and K blocks kb_lo .. kb_lo + nkb - 1 (all of them unless split).
     const int S = PLAIN ? 1 : ksplit;
@@ -105,13 +100,11 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     const int slab = blockIdx.x / S;
     const int kb_lo = (blockIdx.x - slab * S) * num_kb / S;
     const int nkb = (blockIdx.x - slab * S + 1) * num_kb / S - kb_lo;
-    float* sAs = reinterpret_cast<float*>(sXb + stages * Cfg::XB_TILE);  // [nkb][MT]
+    float* sAs = reinterpret_cast<float*>(sX + (FUSED ? num_kb : stages) * Cfg::X_TILE);
     float* sRaw = sAs + nkb * MT;      // a_s rows m0 .. m0+MT-1, this CTA's K blocks: [MT][nkb]
-    int* sReady = reinterpret_cast<int*>(sRaw);          // FUSED: [num_kb] quantiser warps done
-    float* sBs = sRaw + (FUSED ? nkb : nkb * MT);        // b_s row of this slab: [nkb]
+    float* sBs = sRaw + (FUSED ? 0 : nkb * MT);          // b_s row of this slab: [nkb]
     uint8_t* ring_mem = reinterpret_cast<uint8_t*>(sBs + ((nkb + 3) & ~3));
     const Ring ring = carve_ring(ring_mem, stages);
-    uint64_t* qfull = reinterpret_cast<uint64_t*>(ring_mem + ring_bytes(stages));  // FUSED
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -144,11 +137,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
         *sScaleDone = 0;
-        if constexpr (FUSED) {
-            for (int s = 0; s < stages; ++s) mbar_init(&qfull[s], Cfg::Q_WARPS);
-            fence_barrier_init();
-        }
-        tma_prefetch_desc(&tmA);
+        if constexpr (!FUSED) tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         // Weights the caller declared constant need not wait for the kernels before this one:
         // the ring starts filling while they finish.
@@ -160,9 +149,6 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             }
         }
     }
-    if constexpr (FUSED) {
-        for (int i = threadIdx.x; i < num_kb; i += Cfg::THREADS) sReady[i] = 0;
-    }
     // `early`: this launch reads nothing the kernel just before it writes (the second of two
     // launches over disjoint groups), so it starts its work at once and waits for that kernel
     // only before exiting -- its own completion then still implies the other's.
@@ -172,6 +158,70 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         const int t = threadIdx.x - 64;
         for (int i = t; i < num_kb; i += 32 * Cfg::EPI_WARPS) cp_async_4(sBs + i, bs_row + i);
         cp_async_commit();
+    }
+    if constexpr (FUSED) {
+        // Every warp quantises x whole. Task t: row t / num_kb, K block t % num_kb; eight lanes
+        // per task, lane l taking elements 16 (l % 8) .. +15 of the block (quant_block16's
+        // layout), four tasks per warp at a time, and each lane loads BATCH tasks before it
+        // quantises any. Loop bounds are warp-uniform: quant_block16 shuffles across the warp.
+        constexpr int NW = Cfg::THREADS / 32;
+        constexpr int BATCH = 4;
+        const int sub = lane >> 3;
+        const int chunk = lane & 7;
+        const int rows = scale_rows;
+        const int tasks = rows * num_kb;
+        const bool writer = blockIdx.x == 0;              // first slab: also write y and s
+        for (int base = warp * 4; base < tasks; base += NW * 4 * BATCH) {
+            uint32_t w[BATCH][8];
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                const int t = base + b * NW * 4 + sub;
+                uint4 v0 = make_uint4(0, 0, 0, 0), v1 = v0;
+                if (t < tasks) {
+                    const int row = t / num_kb;
+                    const int kb = t - row * num_kb;
+                    const uint4* src =
+                        fq.x + ((static_cast<int64_t>(m0 + row) * g.K + kb * BK + chunk * 16) >> 3);
+                    v0 = __ldg(src);
+                    v1 = __ldg(src + 1);
+                }
+                w[b][0] = v0.x; w[b][1] = v0.y; w[b][2] = v0.z; w[b][3] = v0.w;
+                w[b][4] = v1.x; w[b][5] = v1.y; w[b][6] = v1.z; w[b][7] = v1.w;
+            }
+#pragma unroll
+            for (int b = 0; b < BATCH; ++b) {
+                if (base + b * NW * 4 >= tasks) break;
+                const int t = base + b * NW * 4 + sub;
+                uint32_t out[4];
+                const float sc = fq.ue8m0 ? quant_block16<true>(w[b], out)
+                                          : quant_block16<false>(w[b], out);
+                if (t < tasks) {
+                    const int row = t / num_kb;
+                    const int kb = t - row * num_kb;
+                    const uint4 q = make_uint4(out[0], out[1], out[2], out[3]);
+                    *reinterpret_cast<uint4*>(sX + kb * Cfg::X_TILE + (row >> 3) * 1024 +
+                                              (row & 7) * 128 + ((chunk ^ (row & 7)) << 4)) = q;
+                    if (chunk == 0) sAs[kb * MT + row] = sc;
+                    if (writer) {
+                        const int64_t grow = m0 + row;
+                        fq.y[(grow * g.K + kb * BK + chunk * 16) >> 4] = q;
+                        if (chunk == 0) fq.s[grow * num_kb + kb] = sc;
+                    }
+                }
+            }
+        }
+        // Rows past M: zero codes and zero scales in every K block.
+        for (int i = threadIdx.x; i < (MT - rows) * num_kb * 8; i += Cfg::THREADS) {
+            const int row = rows + i / (num_kb * 8);
+            const int rem = i - (row - rows) * num_kb * 8;
+            const int kb = rem >> 3;
+            const int ch = rem & 7;
+            *reinterpret_cast<uint4*>(sX + kb * Cfg::X_TILE + (row >> 3) * 1024 + (row & 7) * 128 +
+                                      ((ch ^ (row & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+            if (ch == 0) sAs[kb * MT + row] = 0.0f;
+        }
+        // The tiles are read next by the tensor core (async proxy), after the block barrier.
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     if (!FUSED && warp == Cfg::Q_WARP0) {
         if (S == 1) {
@@ -206,9 +256,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *ring.tmem_holder;
-    // Activations on the first stages: e4m3 rows of A, or (FUSED) bf16 rows of x.
-    uint8_t* const sAct = FUSED ? sXb : sX;
-    constexpr int ACT_TILE = FUSED ? Cfg::XB_TILE : Cfg::X_TILE;
+    // Activations on the first stages (quantised input; FUSED holds them already).
     if (threadIdx.x == 0) {
         // fill the whole ring at once
         for (int i = 0; i < prefill; ++i) {
@@ -217,7 +265,8 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 mbar_arrive_expect_tx(&ring.full[i], Cfg::TX_BYTES);
                 tma_load_2d_hint(sW + i * A_TILE, &tmB, &ring.full[i], kb * BK, b_row, stream);
             }
-            tma_load_2d_hint(sAct + i * ACT_TILE, &tmA, &ring.full[i], kb * BK, m0, keep);
+            if constexpr (!FUSED)
+                tma_load_2d_hint(sX + i * Cfg::X_TILE, &tmA, &ring.full[i], kb * BK, m0, keep);
         }
     }
 
@@ -236,8 +285,9 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 mbar_arrive_expect_tx(&ring.full[stage], Cfg::TX_BYTES);
                 tma_load_2d_hint(sW + stage * A_TILE, &tmB, &ring.full[stage], kb * BK, b_row,
                                  stream);
-                tma_load_2d_hint(sAct + stage * ACT_TILE, &tmA, &ring.full[stage], kb * BK, m0,
-                                 keep);
+                if constexpr (!FUSED)
+                    tma_load_2d_hint(sX + stage * Cfg::X_TILE, &tmA, &ring.full[stage], kb * BK,
+                                     m0, keep);
                 ++issued;
                 if (++stage == stages) {
                     stage = 0;
@@ -253,14 +303,13 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             uint32_t phase = 0, tphase = 0;
             for (int kb = 0; kb < nkb; ++kb) {
                 if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
-                    !mbar_wait(&ring.full[stage], phase) ||
-                    (FUSED && !mbar_wait(&qfull[stage], phase))) {
+                    !mbar_wait(&ring.full[stage], phase)) {
                     record_error(FP8BS_DEVERR_MMA_WAIT);
                     break;
                 }
                 tc_fence_after();
                 const uint32_t w_addr = smem_addr(sW + stage * A_TILE);
-                const uint32_t x_addr = smem_addr(sX + stage * Cfg::X_TILE);
+                const uint32_t x_addr = smem_addr(sX + (FUSED ? kb : stage) * Cfg::X_TILE);
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(buf * MT);
 #pragma unroll
                 for (int j = 0; j < BK / MMA_K; ++j)
@@ -297,78 +346,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             }
         }
     } else if (FUSED && warp >= Cfg::Q_WARP0) {
-        // Quantiser warps: per K block, 8 lanes per row of MT: lane l of a group takes elements
-        // 16 (l % 8) .. +15 of its row, i.e. one 16-byte chunk of the row's 128 e4m3 codes,
-        // stored at chunk (l % 8) ^ (row % 8) of the row (128-byte swizzle, 8-row atoms of 1024
-        // bytes: the layout TMA would have written).
-        const int qw = warp - Cfg::Q_WARP0;
-        const int sub = lane >> 3;                        // row within the warp's four
-        const int chunk = lane & 7;
-        const bool writer = blockIdx.x == 0;              // first slab: also write y and s
-        const int rows = scale_rows;                      // rows of x; the rest stay zero
-        constexpr int PASSES = MT / 16;
-        // Rows past M are zero codes in every stage (written once, never overwritten).
-        for (int i = threadIdx.x - Cfg::Q_WARP0 * 32; i < stages * MT * 8; i += Cfg::Q_WARPS * 32) {
-            const int st = i / (MT * 8), row = (i / 8) % MT, ch = i % 8;
-            if (row >= rows)
-                *reinterpret_cast<uint4*>(sX + st * Cfg::X_TILE + (row >> 3) * 1024 +
-                                          (row & 7) * 128 + ((ch ^ (row & 7)) << 4)) =
-                    make_uint4(0, 0, 0, 0);
-        }
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int kb = 0; kb < num_kb; ++kb) {
-            if (!warp_wait(&ring.full[stage], phase)) {
-                if (lane == 0) record_error(FP8BS_DEVERR_PRODUCER_WAIT);
-                break;
-            }
-            const uint8_t* xb = sXb + stage * Cfg::XB_TILE;
-            uint8_t* xq = sX + stage * Cfg::X_TILE;
-            // This warp's rows pass * 16 + qw * 4 + sub: all passes with a row of x are issued
-            // together (independent chains), passes of padding only are skipped (warp-uniform).
-            uint32_t w[PASSES][8];
-#pragma unroll
-            for (int pass = 0; pass < PASSES; ++pass) {
-                const int row = pass * 16 + qw * 4 + sub;
-                if (pass * 16 + qw * 4 < rows) {
-                    const uint4 v0 = *reinterpret_cast<const uint4*>(xb + row * 256 + chunk * 32);
-                    const uint4 v1 =
-                        *reinterpret_cast<const uint4*>(xb + row * 256 + chunk * 32 + 16);
-                    w[pass][0] = v0.x; w[pass][1] = v0.y; w[pass][2] = v0.z; w[pass][3] = v0.w;
-                    w[pass][4] = v1.x; w[pass][5] = v1.y; w[pass][6] = v1.z; w[pass][7] = v1.w;
-                }
-            }
-#pragma unroll
-            for (int pass = 0; pass < PASSES; ++pass) {
-                if (pass * 16 + qw * 4 >= rows) continue;
-                const int row = pass * 16 + qw * 4 + sub;
-                uint32_t out[4];
-                const float sc = fq.ue8m0 ? quant_block16<true>(w[pass], out)
-                                          : quant_block16<false>(w[pass], out);
-                const uint4 q = make_uint4(out[0], out[1], out[2], out[3]);
-                *reinterpret_cast<uint4*>(xq + (row >> 3) * 1024 + (row & 7) * 128 +
-                                          ((chunk ^ (row & 7)) << 4)) = q;
-                if (chunk == 0) sAs[kb * MT + row] = sc;
-                if (writer && row < rows) {
-                    const int64_t grow = m0 + row;
-                    fq.y[(grow * g.K + kb * BK + chunk * 16) >> 4] = q;
-                    if (chunk == 0) fq.s[grow * num_kb + kb] = sc;
-                }
-            }
-            // The tile is read next by the tensor core (async proxy), the scales by the
-            // promotion warps.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&qfull[stage]);
-                atomicAdd(&sReady[kb], 1);
-            }
-            if (++stage == stages) {
-                stage = 0;
-                phase ^= 1;
-            }
-        }
+        // Quantiser warps: their part was the prologue.
     } else {
         // Promotion warps.
         if constexpr (FUSED) {
@@ -389,8 +367,8 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 ok = false;
                 break;
             }
-            // FUSED: this block's a_s (written by the quantiser warps, long before the MMA that
-            // just finished could run) times b_s; otherwise the staged products.
+            // FUSED: this block's a_s (quantised in the prologue) times b_s; otherwise the
+            // staged products.
             float sb = 1.0f;
             if constexpr (!FUSED) {
                 if (!spin_until_at_least(sScaleDone, kb + 1)) {
@@ -400,15 +378,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 }
                 __threadfence_block();
             }
-            if constexpr (FUSED) {
-                if (!spin_until_equal(&sReady[kb], Cfg::Q_WARPS)) {
-                    if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
-                    ok = false;
-                    break;
-                }
-                __threadfence_block();
-                sb = sBs[kb];
-            }
+            if constexpr (FUSED) sb = sBs[kb];
             tc_fence_after();
             const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
                                    static_cast<uint32_t>(buf * MT);
@@ -543,13 +513,12 @@ template <int MT, bool FUSED>
 bool swap_smem(int nkb, int* stages_out, int* smem_out) {
     using Cfg = SwapCfg<MT, FUSED>;
     const int scale_bytes = swap_scale_bytes<MT, FUSED>(nkb);
-    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages) + (FUSED ? 8 * kMaxStages : 0);
+    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages);
     int stages = (kSmemLimit - fixed) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
-    if (stages < 2) return false;   // K too large for the scale staging
+    if (stages < 2) return false;   // K too large for the scale staging (FUSED: the activations)
     *stages_out = stages;
-    *smem_out = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages) +
-                (FUSED ? 8 * stages : 0);
+    *smem_out = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages);
     return true;
 }
 
@@ -637,14 +606,7 @@ bool check_gemm_swapab(int MT, int K, int ksplit) {
 }
 
 int plan_gemm_swapab(int MT, bool fused, int row_tiles, int N, int K, int num_sms) {
-    if (fused) {
-        switch (MT) {
-            case 16: return plan_swap<16, true>(row_tiles, N, K, num_sms);
-            case 32: return plan_swap<32, true>(row_tiles, N, K, num_sms);
-            case 64: return plan_swap<64, true>(row_tiles, N, K, num_sms);
-            default: return 0;
-        }
-    }
+    if (fused) return MT == 16 ? plan_swap<16, true>(row_tiles, N, K, num_sms) : 0;
     switch (MT) {
         case 16: return plan_swap<16, false>(row_tiles, N, K, num_sms);
         case 32: return plan_swap<32, false>(row_tiles, N, K, num_sms);
@@ -669,14 +631,9 @@ cudaError_t launch_gemm_swapab(const CUtensorMap& tmB, const CUtensorMap& tmA,
                                const GemmArgs& g, const GroupTable& gt, int MT,
                                const FusedQuant& fq, int ksplit, bool early,
                                cudaStream_t stream) {
-    if (fq.x) {
-        switch (MT) {
-            case 16: return launch_swap<16, true>(tmB, tmA, g, gt, fq, ksplit, early, stream);
-            case 32: return launch_swap<32, true>(tmB, tmA, g, gt, fq, ksplit, early, stream);
-            case 64: return launch_swap<64, true>(tmB, tmA, g, gt, fq, ksplit, early, stream);
-            default: return cudaErrorInvalidValue;
-        }
-    }
+    if (fq.x)
+        return MT == 16 ? launch_swap<16, true>(tmB, tmA, g, gt, fq, ksplit, early, stream)
+                        : cudaErrorInvalidValue;
     switch (MT) {
         case 16: return launch_swap<16, false>(tmB, tmA, g, gt, fq, ksplit, early, stream);
         case 32: return launch_swap<32, false>(tmB, tmA, g, gt, fq, ksplit, early, stream);

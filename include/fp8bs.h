@@ -129,7 +129,7 @@ FP8BS_API int fp8bs_gemm(const void* a, const float* a_s, const void* b, const f
  * it could have written (all inputs, or all but b and b_s with the flag above).
  */
 #define FP8BS_GEMM_WEIGHTS_CONSTANT 0x1u
-/* fp8bs_act_quant_gemm only: quantise the activations inside the GEMM kernel (M <= 64). */
+/* fp8bs_act_quant_gemm only: quantise the activations inside the GEMM kernel (M <= 16). */
 #define FP8BS_GEMM_QUANT_IN_KERNEL 0x2u
 FP8BS_API int fp8bs_gemm_ex(const void* a, const float* a_s, const void* b, const float* b_s,
                             void* c, int64_t M, int64_t N, int64_t K, int scale_fmt,
@@ -221,11 +221,15 @@ FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
  * item 3: act_quant, then fp8_gemm; §8.5.1 and §8.5.3), as one call. By default two kernels
  * run back to back (the GEMM starts while act_quant finishes and, with
  * FP8BS_GEMM_WEIGHTS_CONSTANT, streams its weights meanwhile). With
- * FP8BS_GEMM_QUANT_IN_KERNEL and M <= 64 one kernel does both: each CTA of the GEMM quantises
- * the rows of every K block it reads, as act_quant would, and the CTAs of the first 128
- * columns also write y and s. Where the separate GEMM would split each weight slab's K loop
- * between several CTAs (few slabs, see fp8bs_gemm_plan), the two launches run instead. On GB300 at decode sizes this single kernel measured slower than
- * the two (the quantisation sits on every K block's critical path), so it is not the default.
+ * FP8BS_GEMM_QUANT_IN_KERNEL and M <= 16 one kernel does both: before its main loop every CTA
+ * of the GEMM reads x and quantises it whole, as act_quant would, into shared memory (while
+ * its weight stages fill), and the CTAs of the first 128 columns also write y and s. The two
+ * launches run instead where the separate GEMM would split each weight slab's K loop between
+ * several CTAs (few slabs, see fp8bs_gemm_plan) or where the quantised x (16 x K bytes) does
+ * not fit in shared memory beside two weight stages (K up to 11264). On GB300 at decode
+ * sizes the single kernel measured no faster than the two (N = 18432, K = 7168: 25.7 against
+ * 25.1 us at M = 1, 30.7 against 25.4 us at M = 8: every CTA quantises all of x), so it is not
+ * the default.
  *
  *   x      [in]  bf16 [M, K], 16-byte aligned.
  *   y      [out] e4m3 [M, K], 16-byte aligned: the quantised activations, as fp8bs_act_quant.

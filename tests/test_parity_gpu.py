@@ -570,7 +570,7 @@ def test_gemm_ue8m0_deterministic():
 
 # ------------------------------------------------------------------------------ act_quant + GEMM
 # fp8bs_act_quant_gemm: act_quant then the GEMM in one call, or (FP8BS_GEMM_QUANT_IN_KERNEL,
-# M <= 64) one kernel that quantises the activations itself; y, s and C must equal those of the
+# M <= 16) one kernel that quantises the activations itself; y, s and C must equal those of the
 # two separate calls bit for bit.
 
 def separate_act_quant_gemm(xt, bt, bst, fmt, ws):
@@ -581,8 +581,12 @@ def separate_act_quant_gemm(xt, bt, bst, fmt, ws):
 
 @pytest.mark.parametrize("fmt", ["fp32", "ue8m0"])
 @pytest.mark.parametrize("M,N,K", [
-    (1, 18432, 7168), (8, 2048, 7168), (32, 576, 1024), (64, 18432, 7168), (3, 20480, 256),
-    (17, 1000, 18432),     # M <= 64: the one-kernel form applies; N tail, long K
+    # M <= 16: the one-kernel form applies where the separate GEMM would not split K (more
+    # than 76 weight slabs, or too few K blocks to split)
+    (1, 18432, 7168), (3, 20480, 256), (16, 10000, 2048), (5, 12000, 4096), (9, 1000, 128),
+    (8, 2048, 7168),       # 16 slabs: the separate GEMM splits K, so two launches
+    (7, 1000, 18432),      # K too long for the resident activations: two launches
+    (17, 1000, 18432), (32, 576, 1024), (64, 18432, 7168),   # M > 16: two launches
     (100, 1536, 2048), (128, 4096, 512),   # two launches whatever the flag (swapped)
     (300, 1024, 512),      # two launches, normal orientation
 ])

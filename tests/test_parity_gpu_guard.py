@@ -142,7 +142,9 @@ def test_grouped_gemm_guard_bands(fmt, counts, N):
 
 
 @pytest.mark.parametrize("M,N,K,flags", [(17, 1000, 512, 2), (40, 2048, 7168, 3),
-                                         (300, 1000, 512, 1)])
+                                         (300, 1000, 512, 1),
+                                         (13, 10000, 1024, 2),    # one kernel (M <= 16)
+                                         (16, 18432, 2048, 3)])
 def test_act_quant_gemm_guard_bands(M, N, K, flags):
     x = dev_bf16(synth.activations(M, K, seed=M, name="guardX", outlier_frac=0.01))
     b, b_s = synth.weights(N, K, seed=N, name="guardB")
