@@ -840,6 +840,13 @@ def run_profile(case: str, launches: int, warmup: int):
         y = torch.empty((2048, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
         s = torch.empty((2048, K_DIM // 128), dtype=torch.float32, device="cuda")
         fn = lambda: g.act_quant(x, y, s, 2048, K_DIM, 1)  # noqa: E731
+    elif case.startswith("act_quant_decode"):
+        # act_quant at a decode size: act_quant_decode1 .. act_quant_decode64 rows of 7168
+        M = int(case[len("act_quant_decode"):] or 64)
+        x = g.bf16(synth.decode(M))
+        y = torch.empty((M, K_DIM), dtype=torch.float8_e4m3fn, device="cuda")
+        s = torch.empty((M, K_DIM // 128), dtype=torch.float32, device="cuda")
+        fn = lambda: g.act_quant(x, y, s, M, K_DIM)  # noqa: E731
     elif case == "act_quant":
         rows, _ = synth.moe_routing(0)
         x = g.bf16(synth.activations(1024, K_DIM, 0, "moe/tokens", outlier_frac=0.01)[rows])
