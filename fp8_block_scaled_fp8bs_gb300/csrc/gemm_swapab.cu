@@ -35,13 +35,21 @@ struct SwapCfg {
     static constexpr int Q_WARPS = FUSED ? 4 : 0;   // quantiser warps, after the promotion warps
     static constexpr int Q_WARP0 = 2 + EPI_WARPS;
     static constexpr int S_WARPS = FUSED ? 0 : 1;   // scale warp (quantised input), same place
-    static constexpr int THREADS = 64 + 32 * (EPI_WARPS + Q_WARPS + S_WARPS);
+    // MMA issuers: warp 1 and the last warp take the K blocks in turn, each into its own pair of
+    // TMEM buffers. One thread issuing alone spends ~70 clk per tcgen05 instruction, 4 MMAs and
+    // 2 commits per K block: that, not the weight stream, had set the pace (N = 18432, M = 1:
+    // 22.7 us, 20.7 us with the MMAs left out; N = 7168, K = 18432: 28.3 against 22.6 us).
+    static constexpr int ISSUERS = 2;
+    static constexpr int ISSUER2 = 2 + EPI_WARPS + Q_WARPS + S_WARPS;
+    static constexpr int NBUF = 2 * ISSUERS;        // TMEM partial buffers (K block kb: kb % 4)
+    static constexpr int THREADS = 64 + 32 * (EPI_WARPS + Q_WARPS + S_WARPS + ISSUERS - 1);
     static constexpr int X_TILE = MT * BK;          // e4m3 activation rows of one K block
     // A stage: a weight tile and (quantised input) the activation tile; FUSED keeps the
     // activations resident instead.
     static constexpr int STAGE = A_TILE + (FUSED ? 0 : X_TILE);
     static constexpr int TX_BYTES = STAGE;          // bytes TMA brings per stage
-    static constexpr uint32_t TMEM_COLS = tmem_cols_for(2 * MT);
+    static constexpr uint32_t TMEM_COLS = tmem_cols_for(NBUF * MT);
+    static constexpr int BAR_BYTES = 2 * NBUF * 8;  // tfull[NBUF], tempty[NBUF] after the ring
 };
 
 // Shared-memory bytes after the stages, for a CTA that takes nkb K blocks: (FUSED) the
@@ -105,6 +113,9 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     float* sBs = sRaw + (FUSED ? 0 : nkb * MT);          // b_s row of this slab: [nkb]
     uint8_t* ring_mem = reinterpret_cast<uint8_t*>(sBs + ((nkb + 3) & ~3));
     const Ring ring = carve_ring(ring_mem, stages);
+    // The partial buffers' barriers (the ring's own two pairs serve one issuer only).
+    uint64_t* tfull = reinterpret_cast<uint64_t*>(ring_mem + ring_bytes(stages));
+    uint64_t* tempty = tfull + Cfg::NBUF;
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -136,6 +147,12 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     int* sScaleDone = reinterpret_cast<int*>(ring.tmem_holder + 1);
     if (threadIdx.x == 0) {
         init_ring(ring, stages, Cfg::EPI_WARPS);
+        for (int b = 0; b < Cfg::NBUF; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], Cfg::EPI_WARPS);
+        }
+        mbar_init(ring.drain, Cfg::ISSUERS);       // each issuer commits its final drain
+        fence_barrier_init();
         *sScaleDone = 0;
         if constexpr (!FUSED) tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -296,14 +313,23 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
             }
             if (!ok) drain_tma(ring, stages, issued);
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == Cfg::ISSUER2) {
         if (lane == 0) {
             constexpr uint32_t idesc = idesc_e4m3_f32(BM, MT);
-            int stage = 0, buf = 0;
-            uint32_t phase = 0, tphase = 0;
+            const int me = warp == 1 ? 0 : 1;         // this issuer's K blocks: kb % 2 == me
+            int stage = 0;
+            uint32_t phase = 0;
             for (int kb = 0; kb < nkb; ++kb) {
-                if (!mbar_wait(&ring.tempty[buf], tphase ^ 1) ||
-                    !mbar_wait(&ring.full[stage], phase)) {
+                if ((kb & 1) != me) {                   // the other issuer's K block
+                    if (++stage == stages) {
+                        stage = 0;
+                        phase ^= 1;
+                    }
+                    continue;
+                }
+                const int buf = kb & (Cfg::NBUF - 1);
+                const uint32_t tphase = static_cast<uint32_t>(kb / Cfg::NBUF) & 1u;
+                if (!mbar_wait(&tempty[buf], tphase ^ 1) || !mbar_wait(&ring.full[stage], phase)) {
                     record_error(FP8BS_DEVERR_MMA_WAIT);
                     break;
                 }
@@ -316,13 +342,11 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                     mma_f8(d_tmem, smem_desc_k_sw128(w_addr + j * MMA_K),
                            smem_desc_k_sw128(x_addr + j * MMA_K), idesc, j > 0 ? 1u : 0u);
                 mma_commit(&ring.empty[stage]);
-                mma_commit(&ring.tfull[buf]);
+                mma_commit(&tfull[buf]);
                 if (++stage == stages) {
                     stage = 0;
                     phase ^= 1;
                 }
-                buf ^= 1;
-                if (buf == 0) tphase ^= 1;
             }
             mma_commit(ring.drain);
             if (!mbar_wait(ring.drain, 0, kDrainLimitNs)) record_error(FP8BS_DEVERR_DRAIN_WAIT);
@@ -362,7 +386,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
         uint32_t tphase = 0;
         bool ok = true;
         for (int kb = 0; kb < nkb; ++kb) {
-            if (!warp_wait(&ring.tfull[buf], tphase)) {
+            if (!warp_wait(&tfull[buf], tphase)) {
                 if (lane == 0) record_error(FP8BS_DEVERR_EPILOGUE_WAIT);
                 ok = false;
                 break;
@@ -411,7 +435,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                         if (c + 1 == nch) {
                             tc_fence_before();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                            if (lane == 0) mbar_arrive(&tempty[buf]);
                         }
 #pragma unroll
                         for (int i = 0; i < 32; i += 4) {
@@ -428,7 +452,7 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 tmem_wait_ld_16(v);
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ring.tempty[buf]);
+                if (lane == 0) mbar_arrive(&tempty[buf]);
 #pragma unroll
                 for (int i = 0; i < 16; i += 4) {
                     const float4 a4 = scales4(i);
@@ -436,8 +460,10 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                     fma2_into(acc + i + 2, v[i + 2], v[i + 3], a4.z, a4.w);
                 }
             }
-            buf ^= 1;
-            if (buf == 0) tphase ^= 1;
+            if (++buf == Cfg::NBUF) {
+                buf = 0;
+                tphase ^= 1;
+            }
         }
         if (S == 1) {
             if (ok && n < g.N) {
@@ -513,12 +539,12 @@ template <int MT, bool FUSED>
 bool swap_smem(int nkb, int* stages_out, int* smem_out) {
     using Cfg = SwapCfg<MT, FUSED>;
     const int scale_bytes = swap_scale_bytes<MT, FUSED>(nkb);
-    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages);
+    const int fixed = 1024 + scale_bytes + ring_bytes(kMaxStages) + Cfg::BAR_BYTES;
     int stages = (kSmemLimit - fixed) / Cfg::STAGE;
     if (stages > kMaxStages) stages = kMaxStages;
     if (stages < 2) return false;   // K too large for the scale staging (FUSED: the activations)
     *stages_out = stages;
-    *smem_out = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages);
+    *smem_out = 1024 + stages * Cfg::STAGE + scale_bytes + ring_bytes(stages) + Cfg::BAR_BYTES;
     return true;
 }
 
