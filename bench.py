@@ -47,7 +47,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # kernel (gemm_swapab_kernel), from ncu captures of its M=1 and M=64 launches (their mean),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "5d1d6b76d642fd10", "per_launch_mb": (134.93 + 135.38) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "19919296a13af9eb", "per_launch_mb": (134.99 + 135.12) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting

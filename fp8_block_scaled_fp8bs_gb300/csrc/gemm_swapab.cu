@@ -425,6 +425,33 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
                 const int nch = PLAIN ? NCH : (scale_rows + 31) >> 5;
                 float va[32], vb[32];
                 tmem_ld_32cols(taddr, va);
+                if (!PLAIN && NCH == 2 && nch == 2) {
+                    // General launches at MT = 64 (split K, grouped): both chunks in flight
+                    // together, one round trip, the buffer back, then both folded in. (The
+                    // N = 7168, K = 18432 down-projection at M = 64, split two ways: 34.4 ->
+                    // 32.7 us. The plain launch measured no better this way.)
+                    tmem_ld_32cols(taddr + 32, vb);
+                    tmem_wait_ld_32(va);
+                    tmem_wait_ld_32(vb);
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[buf]);
+#pragma unroll
+                    for (int c = 0; c < 2; ++c) {
+                        const float* cur = c ? vb : va;
+#pragma unroll
+                        for (int i = 0; i < 32; i += 4) {
+                            const float4 a4 = scales4(c * 32 + i);
+                            fma2_into(acc + c * 32 + i, cur[i + 0], cur[i + 1], a4.x, a4.y);
+                            fma2_into(acc + c * 32 + i + 2, cur[i + 2], cur[i + 3], a4.z, a4.w);
+                        }
+                    }
+                    if (++buf == Cfg::NBUF) {
+                        buf = 0;
+                        tphase ^= 1;
+                    }
+                    continue;
+                }
                 tmem_wait_ld_32(va);
 #pragma unroll
                 for (int c = 0; c < NCH; ++c) {
