@@ -11,15 +11,17 @@
 // M > 128 a slab is read from HBM about once and the other tiles of x find it in L2.
 //   warp 0          weight producer: per K block the e4m3 tile (the HBM stream) into the
 //                   weight ring; a slot is free as soon as the dequantisers have read it
-//   warp 3 (lane 0) x producer: the bf16 rows of x (128-byte swizzle, 64-wide K halves) into
-//                   the x ring; a slot is free once the MMAs reading it are done. Warp 3 is an
-//                   epilogue warp, idle until the end of the K loop.
-//   warps 1, 2      MMA issuers. XT = 1: K block kb to issuer kb % 2; XT = 2: issuer t takes
-//                   tile t of x for every K block. Per K block 8 x tcgen05.mma kind::f16
-//                   (K = 16) into the issuer's own TMEM accumulator for the whole K loop (the
-//                   block scale is inside W'). One thread issuing alone is held to about one
-//                   small MMA per 60-80 clk and stalls at its next barrier wait until the
-//                   tensor core has caught up; two issuers keep the pipe fed.
+//   warp 1 + ISSUERS (lane 0) x producer: the bf16 rows of x (128-byte swizzle, 64-wide K
+//                   halves) into the x ring; a slot is free once the MMAs reading it are done.
+//                   It is an epilogue warp, idle until the end of the K loop.
+//   warps 1 .. ISSUERS  MMA issuers (lane 0). XT = 1: K block kb to issuer kb % ISSUERS (four
+//                   at MT <= 64, two at MT = 128); XT = 2: issuer t takes tile t of x for
+//                   every K block. Per K block 8 x tcgen05.mma kind::f16 (K = 16) into the
+//                   issuer's own TMEM accumulator for the whole K loop (the block scale is
+//                   inside W'). One thread issuing alone is held to about one small MMA per
+//                   60-80 clk and stalls at its next barrier wait until the tensor core has
+//                   caught up. With two issuers the decode rows still ran 32 us against 26 us
+//                   with the MMAs left out (M = 1, N = 18432, K = 7168), hence four there.
 //   warps 2 .. 5    epilogue: the accumulators to bf16 y (summed for XT = 1)
 //   warps 6 .. 21   dequantisers, two groups of eight taking K blocks in turn (a warp's barrier
 //                   waits and arrivals cost a few hundred clk per K block, which the other
@@ -49,7 +51,10 @@ struct LinCfg {
     static constexpr int DQ_GROUPS = 2;                  // groups, taking K blocks in turn
     static constexpr int DQ_WARPS = DQ_GROUP * DQ_GROUPS;
     static constexpr int DQ0 = 2 + EPI_WARPS;            // first dequantiser warp
-    static constexpr int X_PRODUCER = 3;                 // an epilogue warp, idle until the end
+    // MMA issuers: warps 1 .. ISSUERS. Four where four accumulators fit beside the W' slots in
+    // TMEM (one tile of x, MT <= 64), else two.
+    static constexpr int ISSUERS = (XT == 1 && MT <= 64) ? 4 : 2;
+    static constexpr int X_PRODUCER = 1 + ISSUERS;       // an epilogue warp, idle until the end
     static constexpr int THREADS = 32 * (2 + EPI_WARPS + DQ_WARPS);
     static constexpr int W_TILE = BM * BK;               // e4m3 weight tile (128 x 128)
     static constexpr int HALF = 64;                      // bf16 K elements per 128-byte row
@@ -64,12 +69,13 @@ struct LinCfg {
     static constexpr int SW_FIT = (kSmemLimit - 1024 - BAR_BYTES - SX * X_SLOT) / W_TILE;
     static constexpr int SW = SW_FIT > kMaxStages ? kMaxStages : SW_FIT;   // weight ring slots
     static_assert(SW >= 2, "shared memory");
-    static constexpr int ISSUERS = 2;                    // MMA issuers: warps 1 .. ISSUERS
     static constexpr int ACC_COLS = MT > 64 ? MT : 64;   // TMEM: accumulator i at ACC_COLS i,
     static constexpr int W_COL0 = ISSUERS * ACC_COLS;    // then the W' slots of 64 columns
     static constexpr int W_COLS = BK / 2;                // (bf16 pairs)
     static constexpr int SB = 4;                         // W' slots
     static constexpr uint32_t TMEM_COLS = 512;
+    static_assert(W_COL0 + SB * W_COLS <= static_cast<int>(TMEM_COLS), "TMEM columns");
+    static_assert(X_PRODUCER >= 2 && X_PRODUCER < 2 + EPI_WARPS, "x producer: an epilogue warp");
     static constexpr int MMA_PER_KB = XT;                // issuer commits per K block
     static constexpr int SMEM = 1024 + SW * W_TILE + SX * X_SLOT + BAR_BYTES;
 };
