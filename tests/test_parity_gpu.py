@@ -178,6 +178,27 @@ def test_gemm_shapes_full_compare(M, N, K):
     assert_gemm_close(run_gemm(a, a_s, b, b_s), oracle.gemm(a, a_s, b, b_s), f"{M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("M,N,K", [
+    (1, 300, 384), (20, 500, 384), (50, 700, 384), (120, 900, 384),   # three K blocks, each MT
+    (7, 9800, 1152), (64, 9800, 2176), (128, 9800, 1408),            # 9, 17, 11: buffers wrap
+])                                                  # (77 slabs: too many to split K)
+def test_decode_two_issuers_odd_k_blocks(M, N, K):
+    """The decode kernel's two MMA issuers take alternate K blocks, each into its own pair of
+    TMEM buffers: an odd count leaves one issuer a block more, and more than four blocks wrap
+    the buffers. Every element against the oracle, two calls bit-identical."""
+    p = fp8bs.fp8bs_gemm_plan(M, N, K, fp8bs.SCALE_FP32, False)
+    assert p["kernel"] == fp8bs.KERNEL_SWAPPED and p["ksplit"] == 1, p
+    x = synth.activations(M, K, seed=M + N + K, name="issA", outlier_frac=0.01)
+    a, a_s = oracle.act_quant(x)
+    b, b_s = synth.weights(N, K, seed=M + 2 * N + K, name="issB")
+    args = (dev_e4m3(a), dev_f32(a_s), dev_e4m3(b), dev_f32(b_s), "fp32")
+    c1 = fp8bs.fp8_gemm(*args, workspace=None)
+    c2 = fp8bs.fp8_gemm(*args, workspace=None)
+    torch.cuda.synchronize()
+    assert torch.equal(c1.view(torch.int16), c2.view(torch.int16))
+    assert_gemm_close(host_bf16_f64(c1), oracle.gemm(a, a_s, b, b_s), f"decode {M}x{N}x{K}")
+
+
 def test_gemm_fp32_stream_k_against_oracle():
     """fp32 scales with a workspace: 180 tiles of 128 x 192 on the SMs share their K loops
     (each owner starts from the next CTA's partial); every element matches the oracle, and two
