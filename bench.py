@@ -6,8 +6,10 @@ Headline workload (one JSON line on rank 0): the decode configuration -- for eac
 M in {1, 8, 32, 64}: act_quant of a bf16 [M, 7168] activation, then fp8_gemm against an e4m3
 [18432, 7168] weight with 128x128 fp32 block scales. One step runs the four (act_quant, gemm)
 pairs; each M uses its own weight matrix, so a step streams 4 x 132 MB of weights and no
-weight is resident in L2 (129 MB) when it is read again. The metric is algorithmic bytes
-moved per second (GB/s): weights, weight scales, activations, codes, scales and outputs.
+weight is resident in L2 (129 MB) when it is read again. The timed steps replay CUDA graphs of
+ten steps each (the same launches; the steps launched one by one are timed too and reported as
+eager_ms_per_step). The metric is algorithmic bytes moved per second (GB/s): weights, weight
+scales, activations, codes, scales and outputs.
 
 Also reported (rank 0, N=1): prefill GEMM TFLOPS, weight_dequant / act_quant GB/s, the MoE
 expert GEMMs and the ue8m0 MLA projections, each against its roofline; the CPU oracle on a
@@ -334,12 +336,57 @@ def decode_step(g: Gpu, state):
                          K_DIM, 0, WEIGHTS_CONSTANT)
 
 
+GRAPH_STEPS = 10   # decode steps per captured CUDA graph
+
+
+def capture_steps(g: Gpu, state, n):
+    """A CUDA graph of n decode steps, captured on a side stream (the launches keep their
+    programmatic-dependent-launch attributes inside the graph)."""
+    torch = g.torch
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    main_stream, main_sh = g.stream, g.sh
+    g.stream, g.sh = side, side.cuda_stream
+    try:
+        with torch.cuda.stream(side):
+            decode_step(g, state)                   # kernel attributes set outside the capture
+            side.synchronize()
+            with torch.cuda.graph(graph, stream=side):
+                for _ in range(n):
+                    decode_step(g, state)
+    finally:
+        g.stream, g.sh = main_stream, main_sh
+    torch.cuda.synchronize()
+    return graph
+
+
 def run_decode(g: Gpu, steps, warmup, rank, world, clocks_path):
+    """The timed decode steps, replayed from CUDA graphs of GRAPH_STEPS steps (plus one graph for
+    the remainder): exactly `steps` steps, the same launches as decode_step, without the host's
+    launch overhead between them -- the way a serving loop runs decode. Also returns the same
+    number of steps launched one by one (eager), for comparison."""
     torch = g.torch
     state = decode_setup(g)
     for _ in range(warmup):
         decode_step(g, state)
     torch.cuda.synchronize()
+    full, rest = divmod(steps, GRAPH_STEPS)
+    graph = capture_steps(g, state, GRAPH_STEPS) if full else None
+    tail = capture_steps(g, state, rest) if rest else None
+    for _ in range(2):
+        if graph is not None:
+            graph.replay()
+        if tail is not None:
+            tail.replay()
+    torch.cuda.synchronize()
+    # eager, for comparison (not the reported value)
+    e0, e1 = g.event(), g.event()
+    e0.record()
+    for _ in range(steps):
+        decode_step(g, state)
+    e1.record()
+    torch.cuda.synchronize()
+    eager_ms = e0.elapsed_time(e1)
     sampler = ClockSampler(torch.cuda.current_device(), clocks_path)
     with sampler:
         time.sleep(0.25)
@@ -347,14 +394,17 @@ def run_decode(g: Gpu, steps, warmup, rank, world, clocks_path):
         torch.cuda.synchronize()
         t0, t1 = g.event(), g.event()
         t0.record()
-        for k in range(steps):
-            decode_step(g, state)
+        for _ in range(full):
+            graph.replay()
+        if tail is not None:
+            tail.replay()
         t1.record()
         torch.cuda.synchronize()
         barrier(world)
         time.sleep(0.25)
     ms_total = t0.elapsed_time(t1)
-    return ms_total, decode_gemm_launch_ms(g, state, max(3, min(steps, 100))), sampler.summary()
+    return (ms_total, eager_ms, decode_gemm_launch_ms(g, state, max(3, min(steps, 100))),
+            sampler.summary())
 
 
 def decode_gemm_launch_ms(g: Gpu, state, rounds):
@@ -956,8 +1006,10 @@ def main(argv=None):
     os.makedirs(args.out_dir, exist_ok=True)
     clocks_path = os.path.join(args.out_dir, f"clocks_rank{rank}.csv")
 
-    ms_total, per_m, clocks = run_decode(g, args.steps, args.warmup, rank, world, clocks_path)
+    ms_total, eager_ms, per_m, clocks = run_decode(g, args.steps, args.warmup, rank, world,
+                                                   clocks_path)
     ms_total = max_over_ranks(ms_total, world, "cuda")
+    eager_ms = max_over_ranks(eager_ms, world, "cuda")
     e2e_ms, h2d, d2h = run_decode_e2e(g, args.steps, args.warmup, world)
     e2e_ms = max_over_ranks(e2e_ms, world, "cuda")
 
@@ -984,6 +1036,8 @@ def main(argv=None):
 
     line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "step_launch": f"CUDA graphs of {GRAPH_STEPS} steps",
+            "eager_ms_per_step": round(eager_ms / args.steps, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3",
             "data": "synthetic", "config": workload_config(),
             "clocks": clocks, "roofline": roofline,
