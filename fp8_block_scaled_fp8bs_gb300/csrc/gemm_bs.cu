@@ -167,13 +167,8 @@ __global__ void __launch_bounds__(BsCfg<BN>::THREADS, 1)
     grid_dependency_wait();
     grid_launch_dependents();
     if (threadIdx.x == 0) {
-        init_ring(ring, stages, Cfg::EPI_WARPS, 1 + Cfg::SF_WARPS);
-        if constexpr (Cfg::ISSUERS > 1) {
-            // every issuer commits each finished buffer and its final drain
-            for (int b = 0; b < 2; ++b) mbar_init(&ring.tfull[b], Cfg::ISSUERS);
-            mbar_init(ring.drain, Cfg::ISSUERS);
-            fence_barrier_init();
-        }
+        // every issuer commits each finished buffer and its final drain
+        init_ring(ring, stages, Cfg::EPI_WARPS, 1 + Cfg::SF_WARPS, Cfg::ISSUERS);
         if (stream_k) {
             mbar_init(part_bar, 1);
             fence_barrier_init();

@@ -92,17 +92,19 @@ constexpr int ring_bytes(int stages) { return (2 * stages + 5) * 8 + 16; }
 
 // full[s] completes on `full_count` arrivals plus the stage's TMA bytes (the producer's
 // arrive.expect_tx is one arrival; the block-scaled kernel adds its scale-factor warps).
+// tfull[b] and drain complete on one commit from each of `issuers` MMA-issuing threads. (Each
+// barrier is initialised once: re-initialising a live mbarrier is undefined.)
 __device__ __forceinline__ void init_ring(const Ring& r, int stages, uint32_t epi_warps,
-                                          uint32_t full_count = 1) {
+                                          uint32_t full_count = 1, uint32_t issuers = 1) {
     for (int s = 0; s < stages; ++s) {
         mbar_init(&r.full[s], full_count);
         mbar_init(&r.empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
-        mbar_init(&r.tfull[b], 1);
+        mbar_init(&r.tfull[b], issuers);
         mbar_init(&r.tempty[b], epi_warps);
     }
-    mbar_init(r.drain, 1);
+    mbar_init(r.drain, issuers);
     fence_barrier_init();
 }
 

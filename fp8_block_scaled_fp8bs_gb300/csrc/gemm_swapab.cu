@@ -146,12 +146,12 @@ __global__ void __launch_bounds__(SwapCfg<MT, FUSED>::THREADS, 1)
     // Quantised input: the scale warp counts here the K blocks of sAs it has filled.
     int* sScaleDone = reinterpret_cast<int*>(ring.tmem_holder + 1);
     if (threadIdx.x == 0) {
-        init_ring(ring, stages, Cfg::EPI_WARPS);
+        // each issuer commits its final drain (the ring's own tfull / tempty go unused)
+        init_ring(ring, stages, Cfg::EPI_WARPS, 1, Cfg::ISSUERS);
         for (int b = 0; b < Cfg::NBUF; ++b) {
             mbar_init(&tfull[b], 1);
             mbar_init(&tempty[b], Cfg::EPI_WARPS);
         }
-        mbar_init(ring.drain, Cfg::ISSUERS);       // each issuer commits its final drain
         fence_barrier_init();
         *sScaleDone = 0;
         if constexpr (!FUSED) tma_prefetch_desc(&tmA);
