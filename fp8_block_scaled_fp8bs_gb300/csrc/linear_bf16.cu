@@ -96,7 +96,9 @@ __device__ __forceinline__ void dequant8(uint32_t lo, uint32_t hi, float sc, uin
             const __nv_fp8x2_storage_t pair =
                 static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * h)) & 0xFFFFu);
             const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
-            out[2 * i + h] = bf16x2(__fmul_rn(f.x, sc), __fmul_rn(f.y, sc));
+            // both products in one packed multiply (each rounded to nearest as __fmul_rn)
+            const float2 p = __fmul2_rn(f, make_float2(sc, sc));
+            out[2 * i + h] = bf16x2(p.x, p.y);
         }
     }
 }
