@@ -688,6 +688,26 @@ def test_linear_bf16_prefill_sampled_rows():
     assert_gemm_close(got, oracle.linear_bf16(x[rows], w, w_s), "bf16 path prefill rows")
 
 
+def test_linear_bf16_phases_with_a_partial_last_phase():
+    """4352 rows of x at K = 7168 make 17 pairs of 128-row tiles, which the kernel runs in
+    phases of 8 (a quarter of L2 each): 8, 8 and 1. Whole rows from every tile pair (first and
+    last of each) and whole columns across all rows, against the oracle."""
+    M, N, K = 4352, 1000, synth.DIM
+    x = synth.activations(M, K, seed=11, name="phaseX", outlier_frac=0.01)
+    w, w_s = synth.weights(N, K, seed=12, name="phaseW")
+    y = fp8bs.linear_bf16(dev_bf16(x), dev_e4m3(w), dev_f32(w_s))
+    torch.cuda.synchronize()
+    rows = np.unique(np.r_[np.arange(0, M, 256), np.arange(255, M, 256), 4096, 4351])
+    got = host_bf16_f64(y[torch.from_numpy(rows).to(y.device)])
+    assert_gemm_close(got, oracle.linear_bf16(x[rows], w, w_s), "bf16 phases: rows")
+    cols = np.array([0, 127, 128, 511, 999])
+    got = host_bf16_f64(y[:, torch.from_numpy(cols).to(y.device)])
+    # one weight row at a time, with the scale row of its 128-row block
+    ref = np.concatenate([oracle.linear_bf16(x, w[c:c + 1], w_s[c // 128:c // 128 + 1])
+                          for c in cols], axis=1)
+    assert_gemm_close(got, ref, "bf16 phases: cols")
+
+
 def test_linear_bf16_large_block_scales():
     """Block scales of 2^8 and above, mixed with small ones in one weight: the dequantisers'
     fp32 product and bf16 rounding must hold at any finite scale."""
