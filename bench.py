@@ -49,7 +49,7 @@ FP8_OVER_BF16 = 2.0  # nominal dense ratio (4.5 vs 2.25 PFLOP/s)
 # kernel (gemm_swapab_kernel), from ncu captures of its M=1 and M=64 launches (their mean),
 # valid only for the kernel sources they were taken on (DECODE_KERNEL_SOURCES, first 16 hex
 # digits of their SHA-256); for any other source the bench reports traffic as null.
-DECODE_TRAFFIC_MB = {"kernel_sha": "d8f9ed1c4b091800", "per_launch_mb": (135.02 + 135.41) / 2}
+DECODE_TRAFFIC_MB = {"kernel_sha": "ef1125afebf8d989", "per_launch_mb": (134.93 + 135.32) / 2}
 
 
 # ----------------------------------------------------------------------------- accounting

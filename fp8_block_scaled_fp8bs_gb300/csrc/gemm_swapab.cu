@@ -1,8 +1,9 @@
 // gemm_swapab.cu -- FP8 GEMM with fp32 block scales for few rows of A (decode, M <= 128):
 // 128 rows of B take the MMA's M side and the MT (16, 32, 64 or 128) rows of A its N side, so
 // the weight stream fills the tensor core's 128 lanes and every SM streams its own 128-row
-// weight slab. The promotion warps fold each K block's TMEM partial into fp32 registers with
-// the combined scale a_s[m, kb] * b_s[slab, kb], as in gemm_tn.cu.
+// weight slab. Two MMA issuers take the K blocks in turn, each into its own pair of TMEM
+// buffers, and the promotion warps fold each K block's partial into fp32 registers with the
+// combined scale a_s[m, kb] * b_s[slab, kb], as in gemm_tn.cu.
 //
 // Split K (quantised input only): when the slabs alone would leave most SMs idle (N = 2048 or
 // 576 at decode: 16 or 5 slabs on 152 SMs), S CTAs, launched as one thread-block cluster, share
