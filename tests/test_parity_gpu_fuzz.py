@@ -120,3 +120,17 @@ def test_act_quant_and_dequant_random_shapes(i):
     torch.cuda.synchronize()
     assert np.array_equal(d.view(torch.int16).cpu().numpy().view(np.uint16),
                           oracle.weight_dequant(w, w_s)), f"case {i}: weight_dequant {N}x{Kw}"
+
+
+def test_campaign_script_runs_clean():
+    """tests/fuzz_campaign.py at a small size, with seeds of its own: every family (plan-chosen,
+    explicit configurations, grouped, act_quant + GEMM, bf16 path) against the oracle, in a
+    separate process as it is run by hand at larger sizes."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, os.path.join(here, "fuzz_campaign.py"), "--plan", "60",
+                        "--config", "80", "--grouped", "20", "--fused", "30", "--bf16", "20",
+                        "--base", "20000"], capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stdout[-3000:] + r.stderr[-3000:]
