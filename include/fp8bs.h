@@ -13,6 +13,12 @@
  * Conventions shared by every entry point:
  *   - Every pointer is a DEVICE pointer into memory the caller owns; the library allocates and
  *     frees nothing and keeps no per-call state, so calls from several host threads are safe.
+ *     Exceptions, marked "host memory allowed" below: act_quant's input x and the bf16 output
+ *     of the GEMMs and of the bf16 path may also point into pinned (page-locked) host memory,
+ *     as cudaHostAlloc, cudaMallocHost or cudaHostRegister provide it. The kernels then read or
+ *     write it in place over the host link (NVLink-C2C on GB300), with no staging copy; the
+ *     bytes still cross the link once. Those kernels access x and C with plain loads and
+ *     stores, never with the tensor memory accelerator, which only reads device memory.
  *   - Matrices are row-major and contiguous. bf16 is the 16-bit brain float; e4m3 is
  *     float8_e4m3fn (1 byte, largest magnitude 448, no infinity).
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is only enqueued:
@@ -60,7 +66,7 @@ typedef enum {
  * fp8bs_act_quant -- quantise bf16 activations to e4m3 with one fp32 scale per 1x128 block.
  * ("DeepSeek-V3 Administrator & Developer Guide", §8.5.1.)
  *
- *   x  [in]  bf16 [M, K], 16-byte aligned.
+ *   x  [in]  bf16 [M, K], 16-byte aligned; host memory allowed.
  *   y  [out] e4m3 [M, K], 16-byte aligned.
  *   s  [out] fp32 [M, K/128], 4-byte aligned: s[m, b] is the scale of x[m, 128b : 128b+128].
  *   M >= 0, K >= 0 with K % 128 == 0.
@@ -98,7 +104,7 @@ FP8BS_API int fp8bs_weight_dequant(const void* w, const float* s, void* y, int64
  *   a_s  [in]  fp32 [M, K/128], 4-byte aligned (per row, per 128-wide K block).
  *   b    [in]  e4m3 [N, K], 16-byte aligned (a Linear weight, out x in).
  *   b_s  [in]  fp32 [ceil(N/128), K/128], 4-byte aligned (per 128x128 block of b).
- *   c    [out] bf16 [M, N], 16-byte aligned.
+ *   c    [out] bf16 [M, N], 16-byte aligned; host memory allowed.
  *   M >= 0, N >= 0, K >= 0 with K % 128 == 0.
  *   scale_fmt: FP8BS_SCALE_FP32: a_s and b_s are any positive finite fp32 values.
  *              FP8BS_SCALE_UE8M0: the caller promises that every a_s and b_s value is a power
@@ -231,7 +237,8 @@ FP8BS_API int fp8bs_gemm_workspace_size(size_t* bytes);
  * 25.1 us at M = 1, 30.7 against 25.4 us at M = 8: every CTA quantises all of x), so it is not
  * the default.
  *
- *   x      [in]  bf16 [M, K], 16-byte aligned.
+ *   x      [in]  bf16 [M, K], 16-byte aligned; host memory allowed (also with
+ *          FP8BS_GEMM_QUANT_IN_KERNEL, where the GEMM's CTAs read it).
  *   y      [out] e4m3 [M, K], 16-byte aligned: the quantised activations, as fp8bs_act_quant.
  *   s      [out] fp32 [M, K/128], 4-byte aligned: their scales, as fp8bs_act_quant.
  *   b, b_s, c, M, N, K, scale_fmt, flags  as in fp8bs_gemm_ex (a = y, a_s = s); scale_fmt
@@ -258,7 +265,7 @@ FP8BS_API int fp8bs_act_quant_gemm(const void* x, void* y, float* s, const void*
  *   x    [in]  bf16 [M, K], 16-byte aligned.
  *   w    [in]  e4m3 [N, K], 16-byte aligned.
  *   w_s  [in]  fp32 [ceil(N/128), K/128], 4-byte aligned.
- *   y    [out] bf16 [M, N], 16-byte aligned.
+ *   y    [out] bf16 [M, N], 16-byte aligned; host memory allowed.
  *   M >= 0, N >= 0, K >= 0 with K % 128 == 0.
  *   flags: 0 or FP8BS_GEMM_WEIGHTS_CONSTANT (as in fp8bs_gemm_ex).
  *
@@ -299,7 +306,8 @@ FP8BS_API int fp8bs_gemm_noalloc(const void* a, const float* a_s, const void* b,
  *   a_s         [in]  fp32 [T, K/128], 4-byte aligned.
  *   b           [in]  e4m3 [groups, N, K] (the experts' weights stacked), 16-byte aligned.
  *   b_s         [in]  fp32 [groups, ceil(N/128), K/128], 4-byte aligned.
- *   c           [out] bf16 [T, N], 16-byte aligned: row r of group i is A[r] . B[i]^T.
+ *   c           [out] bf16 [T, N], 16-byte aligned (host memory allowed): row r of group
+ *                     i is A[r] . B[i]^T.
  *   row_offsets [in]  HOST array of groups+1 non-decreasing row offsets, row_offsets[0] == 0,
  *                     T = row_offsets[groups]; empty groups are allowed.
  *   groups      0 .. 256.  N >= 0, K >= 0 with K % 128 == 0.  scale_fmt as in fp8bs_gemm
