@@ -208,23 +208,59 @@ def _stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-def _require(t, dtype, ndim, name):
+def _require(t, dtype, ndim, name, host_ok=False):
+    """t must be a contiguous CUDA tensor of dtype and rank ndim; with host_ok, a pinned host
+    tensor is accepted too (the kernels that read x or write C reach pinned host memory in
+    place)."""
     import torch
-    if not isinstance(t, torch.Tensor) or not t.is_cuda:
-        raise TypeError(f"{name} must be a CUDA tensor")
+    if not isinstance(t, torch.Tensor) or not (t.is_cuda or (host_ok and t.is_pinned())):
+        raise TypeError(f"{name} must be a CUDA tensor" + (" or a pinned host tensor" if host_ok
+                                                          else ""))
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if t.dim() != ndim or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
 
 
+def _output(out, shape, device):
+    """The bf16 output: a new CUDA tensor, or the caller's `out` (CUDA or pinned host), checked
+    to be a contiguous bf16 tensor of exactly `shape` so that no kernel writes past its end."""
+    import torch
+    if out is None:
+        return torch.empty(shape, dtype=torch.bfloat16, device=device)
+    _require(out, torch.bfloat16, len(shape), "out", host_ok=True)
+    if tuple(out.shape) != tuple(shape):
+        raise ValueError(f"out must have shape {tuple(shape)}, got {tuple(out.shape)}")
+    return out
+
+
+def _workspace_args(workspace):
+    """(pointer, bytes) of a stream-K workspace: None, or a contiguous uint8 CUDA tensor (its
+    size is checked by the library against fp8bs_gemm_workspace_size)."""
+    import torch
+    if workspace is None:
+        return 0, 0
+    _require(workspace, torch.uint8, workspace.dim() if isinstance(workspace, torch.Tensor) else 1,
+             "workspace")
+    return workspace.data_ptr(), workspace.numel()
+
+
+def _cuda_device(*tensors):
+    import torch
+    for t in tensors:
+        if t.is_cuda:
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
+
+
 def act_quant(x, scale_fmt="fp32"):
     """x: bf16 [M,K] (K % 128 == 0) -> (y float8_e4m3fn [M,K], s float32 [M,K/128])."""
     import torch
-    _require(x, torch.bfloat16, 2, "x")
+    _require(x, torch.bfloat16, 2, "x", host_ok=True)
     M, K = x.shape
-    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
-    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=x.device)
+    dev = _cuda_device(x)
+    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=dev)
+    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=dev)
     fp8bs_act_quant(x.data_ptr(), y.data_ptr(), s.data_ptr(), M, K, _fmt(scale_fmt), _stream())
     return y, s
 
@@ -274,11 +310,10 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False,
     if b.shape[1] != K or tuple(a_s.shape) != (M, K // BLOCK) or \
             tuple(b_s.shape) != (-(-N // BLOCK), K // BLOCK):
         raise ValueError("operand or scale shapes do not match")
-    c = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=a.device)
+    c = _output(out, (M, N), a.device)
     if isinstance(workspace, str) and workspace == "auto":
         workspace = gemm_workspace(a.device)
-    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
-        if workspace is not None else (0, 0)
+    ws_ptr, ws_bytes = _workspace_args(workspace)
     fp8bs_gemm_ws(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
                   M, N, K, _fmt(scale_fmt), GEMM_WEIGHTS_CONSTANT if weights_constant else 0,
                   ws_ptr, ws_bytes, _stream())
@@ -286,25 +321,24 @@ def fp8_gemm(a, a_s, b, b_s, scale_fmt="fp32", out=None, weights_constant=False,
 
 
 def act_quant_gemm(x, b, b_s, scale_fmt="fp32", weights_constant=False, workspace="auto",
-                   quant_in_kernel=False):
+                   quant_in_kernel=False, out=None):
     """linear() on the FP8 path: x bf16 [M,K] -> (c bf16 [M,N], y e4m3 [M,K], s fp32
     [M,K/128]): act_quant then the GEMM (quant_in_kernel: one kernel, M <= 16); see fp8_gemm
-    for `workspace`."""
+    for `workspace`. x and `out` (c) may be pinned host tensors."""
     import torch
-    _require(x, torch.bfloat16, 2, "x")
+    _require(x, torch.bfloat16, 2, "x", host_ok=True)
     _require(b, torch.float8_e4m3fn, 2, "b")
     _require(b_s, torch.float32, 2, "b_s")
     M, K = x.shape
     N = b.shape[0]
     if b.shape[1] != K or tuple(b_s.shape) != (-(-N // BLOCK), K // BLOCK):
         raise ValueError("operand or scale shapes do not match")
-    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=x.device)
-    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=x.device)
-    c = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    y = torch.empty((M, K), dtype=torch.float8_e4m3fn, device=b.device)
+    s = torch.empty((M, K // BLOCK), dtype=torch.float32, device=b.device)
+    c = _output(out, (M, N), b.device)
     if isinstance(workspace, str) and workspace == "auto":
-        workspace = gemm_workspace(x.device)
-    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel() * workspace.element_size()) \
-        if workspace is not None else (0, 0)
+        workspace = gemm_workspace(b.device)
+    ws_ptr, ws_bytes = _workspace_args(workspace)
     flags = (GEMM_WEIGHTS_CONSTANT if weights_constant else 0) | \
         (GEMM_QUANT_IN_KERNEL if quant_in_kernel else 0)
     fp8bs_act_quant_gemm(x.data_ptr(), y.data_ptr(), s.data_ptr(), b.data_ptr(), b_s.data_ptr(),
@@ -323,7 +357,7 @@ def linear_bf16(x, w, w_s, weights_constant=False, out=None):
     N = w.shape[0]
     if w.shape[1] != K or tuple(w_s.shape) != (-(-N // BLOCK), -(-K // BLOCK)):
         raise ValueError("operand or scale shapes do not match")
-    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    y = _output(out, (M, N), x.device)
     fp8bs_linear_bf16(x.data_ptr(), w.data_ptr(), w_s.data_ptr(), y.data_ptr(), M, N, K,
                       GEMM_WEIGHTS_CONSTANT if weights_constant else 0, _stream())
     return y
@@ -343,7 +377,7 @@ def fp8_gemm_grouped(a, a_s, b, b_s, row_offsets, scale_fmt="fp32", out=None):
     if len(offs) != G + 1 or offs[0] != 0 or offs[-1] != T or b.shape[2] != K or \
             tuple(a_s.shape) != (T, K // BLOCK) or tuple(b_s.shape) != (G, -(-N // BLOCK), K // BLOCK):
         raise ValueError("operand, scale or offset shapes do not match")
-    c = out if out is not None else torch.empty((T, N), dtype=torch.bfloat16, device=a.device)
+    c = _output(out, (T, N), a.device)
     fp8bs_gemm_grouped(a.data_ptr(), a_s.data_ptr(), b.data_ptr(), b_s.data_ptr(), c.data_ptr(),
                        offs, G, N, K, _fmt(scale_fmt), _stream())
     return c

@@ -216,3 +216,20 @@ def test_gemm_config_argument_checks(lib, args, expect):
 def test_probe_occupy_argument_checks(lib):
     assert lib.fp8bs_probe_occupy(0, 1000, None) == INVALID
     assert lib.fp8bs_probe_occupy(2000, 1000, None) == INVALID
+
+
+def test_tensor_helpers_check_out_and_workspace_before_any_launch():
+    """The binding's tensor helpers check a caller's `out` (contiguous bf16 of exactly the
+    result's shape, on the GPU or in pinned host memory) and workspace (a uint8 CUDA tensor)
+    before anything reaches the library, so that no kernel can write past their ends."""
+    import torch
+    from fp8_block_scaled_fp8bs_gb300 import _output, _workspace_args
+    with pytest.raises(TypeError):          # pageable host memory is not reachable in place
+        _output(torch.empty(3, 4, dtype=torch.bfloat16), (3, 4), "cpu")
+    with pytest.raises(TypeError):
+        _output(torch.empty(3, 4, dtype=torch.float32), (3, 4), "cpu")
+    with pytest.raises(TypeError):
+        _workspace_args(torch.zeros(16, dtype=torch.uint8))
+    with pytest.raises(TypeError):
+        _workspace_args(bytearray(16))
+    assert _workspace_args(None) == (0, 0)

@@ -166,3 +166,64 @@ def test_grouped_and_bf16_path_write_to_host_memory():
         assert torch.equal(bits(yd), bits(yh))
         assert_gemm_close(host_bf16_f64(yh), oracle.linear_bf16(xb, b[0], b_s[0]),
                           f"bf16 path y in host memory, M={M}")
+
+
+def test_tensor_helpers_take_pinned_host_x_and_out():
+    """The binding's helpers with host tensors: act_quant and act_quant_gemm on a pinned x,
+    fp8_gemm, act_quant_gemm, linear_bf16 and fp8_gemm_grouped into a pinned `out`; each equal
+    bit for bit to the same helper on device tensors."""
+    M, N, K = 8, 1000, 1024
+    x = synth.activations(M, K, seed=3, name="hostHx", outlier_frac=0.01)
+    b, b_s = synth.weights(N, K, seed=4, name="hostHb")
+    xd, B, BS = dev_bf16(x), dev_e4m3(b), dev_f32(b_s)
+    xh = xd.cpu().pin_memory()
+    yd, sd = fp8bs.act_quant(xd)
+    yh, sh = fp8bs.act_quant(xh)
+    assert yh.is_cuda and torch.equal(bits(yd), bits(yh)) and torch.equal(bits(sd), bits(sh))
+    cd, _, _ = fp8bs.act_quant_gemm(xd, B, BS, weights_constant=True)
+    out = pinned_like(cd)
+    ch, _, _ = fp8bs.act_quant_gemm(xh, B, BS, weights_constant=True, out=out)
+    torch.cuda.synchronize()
+    assert ch is out and torch.equal(bits(cd), bits(ch))
+    out = pinned_like(cd)
+    fp8bs.fp8_gemm(yd, sd, B, BS, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(out), bits(cd))
+    out = pinned_like(cd)
+    fp8bs.linear_bf16(xd, B, BS, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(out), bits(fp8bs.linear_bf16(xd, B, BS)))
+    offs = [0, 3, 8]
+    stack_b, stack_s = torch.stack([B, B]), torch.stack([BS, BS])
+    gd = fp8bs.fp8_gemm_grouped(yd, sd, stack_b, stack_s, offs)
+    out = pinned_like(gd)
+    fp8bs.fp8_gemm_grouped(yd, sd, stack_b, stack_s, offs, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(bits(out), bits(gd))
+
+
+def test_tensor_helpers_reject_a_wrong_out_before_launching():
+    M, N, K = 8, 1000, 1024
+    x = synth.activations(M, K, seed=5, name="hostBad", outlier_frac=0.01)
+    b, b_s = synth.weights(N, K, seed=6, name="hostBadB")
+    xd, B, BS = dev_bf16(x), dev_e4m3(b), dev_f32(b_s)
+    y, s = fp8bs.act_quant(xd)
+    torch.cuda.synchronize()
+    guard = torch.full((M * N + 4096,), float("nan"), dtype=torch.bfloat16, device="cuda")
+    short = guard[:M * N - 1].view(-1)                 # one element short of C
+    with pytest.raises(ValueError):
+        fp8bs.fp8_gemm(y, s, B, BS, out=short.view(1, -1))
+    with pytest.raises(ValueError):
+        fp8bs.fp8_gemm(y, s, B, BS, out=guard[:M * (N - 8)].view(M, N - 8))
+    with pytest.raises(ValueError):
+        fp8bs.linear_bf16(xd, B, BS, out=guard[:(M - 1) * N].view(M - 1, N))
+    with pytest.raises(ValueError):
+        fp8bs.act_quant_gemm(xd, B, BS, out=guard[:M * N].view(N, M))
+    with pytest.raises(TypeError):
+        fp8bs.fp8_gemm(y, s, B, BS, out=torch.empty((M, N), dtype=torch.float32, device="cuda"))
+    with pytest.raises(TypeError):
+        fp8bs.fp8_gemm(y, s, B, BS, out=torch.empty((M, N), dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        fp8bs.fp8_gemm(y, s, B, BS, workspace=torch.zeros(1 << 20, dtype=torch.uint8))
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(guard.float()).all()), "a rejected call wrote to the buffer"
