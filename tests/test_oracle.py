@@ -233,6 +233,31 @@ def test_gemm_matches_numpy_matmul_of_dequantised_operands():
     assert np.max(np.abs(c - ref)) <= 1e-12 * np.max(np.abs(ref))
 
 
+def test_gemm_matches_a_naive_triple_loop_on_a_tiny_ragged_shape():
+    """The block-scaled sum of "DeepSeek-V3 Administrator & Developer Guide" §8.5.3 written out
+    as plain nested Python loops over m, n, K blocks and k, in binary64, from torch's decoding of
+    the codes: N = 130 spans two 128-row weight-scale blocks and K = 256 two K blocks, so a
+    wrong scale index, a dropped block or a transposed operand shows."""
+    x = synth.activations(3, 256, seed=12, name="loopA", outlier_frac=0.05)
+    a, a_s = oracle.act_quant(x)
+    b, b_s = synth.weights(130, 256, seed=12, name="loopB")
+    av, bv = torch_decode(a), torch_decode(b)
+    c = oracle.gemm(a, a_s, b, b_s)
+    for m in range(3):
+        for n in range(130):
+            total, size = 0.0, 0.0
+            for kb in range(2):
+                part, part_abs = 0.0, 0.0
+                for k in range(128 * kb, 128 * kb + 128):
+                    p = float(av[m, k]) * float(bv[n, k])
+                    part += p
+                    part_abs += abs(p)
+                scale = float(a_s[m, kb]) * float(b_s[n // 128, kb])
+                total += scale * part
+                size += scale * part_abs
+            assert abs(c[m, n] - total) <= 1e-14 * size, (m, n)
+
+
 def test_gemm_closed_forms():
     K = 512
     ones_a = np.full((3, K), 0x38, np.uint8)  # 1.0
